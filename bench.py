@@ -1,0 +1,427 @@
+"""Benchmark of the speculative-decoding verify step on GB300.
+
+One step = the whole hot path on one batch: kv_append -> spec_verify_attn ->
+spec_rejection_sample -> kv_rollback, four C-ABI calls on one stream.
+
+Default workload: the Llama-3-8B-shaped batch (32 sequences, contexts
+U[512, 4096], K = 5, 32 q / 8 kv heads of dim 128, bf16 KV in 16-token
+blocks, vocab 128256, T = 1). The cache state evolves from step to step like
+a decode loop (each step keeps a_b + 1 tokens per sequence); the step inputs
+(logits, drafts, uniforms) are the same every step, so every step makes the
+same decisions and the bytes each step reads are known exactly.
+
+Prints one JSON line. `--impl reference` times the fp64 CPU oracle on the
+host cores instead (bounded samples of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "spec-verify seqs/s & tokens/s; achieved HBM TB/s vs 8 TB/s (1 GB300)"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+ATTN_SOURCES = ["attn_tc.cu", "attn_simt.cu"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--config", default="llama8b", choices=["llama8b", "llama70b", "contbatch", "tree"])
+    p.add_argument("--temperature", type=float, default=1.0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# workload
+# ----------------------------------------------------------------------------
+def make_case(name, temperature, steps_total, seed_offset=0):
+    from speculative_decoding_verify_paged_gb300 import workloads as W
+    if name == "llama8b":
+        case = W.llama8b(seed=1 + seed_offset, temperature=temperature, growth_tokens=6 * steps_total)
+        desc = ("llama3-8b-shaped verify: B=32, ctx U[512,4096], K=5, 32q/8kv heads, head_dim 128, bf16 KV "
+                "in 16-token blocks (shuffled pool), vocab 128256, bf16 logits, T=%g" % temperature)
+    elif name == "llama70b":
+        case = W.llama70b(seed=2 + seed_offset, temperature=temperature)
+        desc = "llama3-70b-shaped verify: B=128, ctx U[512,640], K=4, 64q/8kv, bf16, bs16, vocab 128256"
+    elif name == "contbatch":
+        case = W.contbatch(seed=3 + seed_offset)
+        desc = "continuous-batching mix: B=256, lognormal ctx, K_b U{2..8}, bs128, fragmented pool"
+    else:
+        case = W.tree(seed=5 + seed_offset)
+        desc = "tree verify: B=16, ctx 8192, 61 rows (60-node tree), bs64, vocab 32000, greedy"
+    return case, desc
+
+
+def attn_bytes(ctx_plus_n, step, state):
+    """Algorithmic bytes of one attention launch: every visible K and V row once,
+    Q in, O out."""
+    el = 2 if state.dtype == "bf16" else 4
+    kv = int(ctx_plus_n.sum()) * 2 * state.num_kv_heads * state.head_dim * el
+    qo = 2 * step.total_q * step.num_q_heads * state.head_dim * el
+    return kv + qo
+
+
+def sampler_bytes(step):
+    el = 2 if step.logits_dtype == "bf16" else 4
+    rows = step.total_q if step.temperature == 0.0 or step.mask_kind == "tree" else 2 * step.total_q - len(step.n_q)
+    return rows * step.vocab * el
+
+
+def attn_flops(ctx, step, G):
+    # 4 * Hq * D * sum_b n_b * (c_b + (n_b + 1) / 2) for causal rows
+    n = step.n_q.astype(np.float64)
+    return float(4 * step.num_q_heads * step.q.shape[-1] * (n * (ctx + (n + 1) / 2)).sum())
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled: bool):
+        self.proc = None
+        self.path = None
+        if not enabled:
+            return
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing
+# ----------------------------------------------------------------------------
+def oracle_sample_step(case, seqs):
+    """The oracle's verify step restricted to the sequences `seqs`: append, fp64
+    attention, sampler (or tree walk), rollback. Returns the seconds it took.
+    The oracle writes the appended rows straight into the case's host pools
+    (the same rows into the same free blocks on every call)."""
+    import oracle
+    from speculative_decoding_verify_paged_gb300 import workloads as W
+    st, sp = case.state, case.step
+    seqs = np.asarray(seqs, np.int64)
+    sub = W.KVState(st.block_size, st.num_blocks, st.max_blocks_per_seq, st.num_kv_heads, st.head_dim, st.dtype,
+                    st.k_pool, st.v_pool, st.block_table[seqs].copy(), st.seq_lens[seqs].copy(),
+                    st.free_list.copy(), st.free_top)
+    n_q = sp.n_q[seqs]
+    cu = np.concatenate([[0], np.cumsum(n_q)]).astype(np.int32)
+    rows = np.concatenate([np.arange(sp.cu_q[b], sp.cu_q[b + 1]) for b in seqs])
+    drows = np.concatenate([np.arange(sp.cu_q[b] - b, sp.cu_q[b + 1] - b - 1) for b in seqs]).astype(np.int64)
+    sub_step = W.StepInputs(n_q, cu, sp.num_q_heads, sp.q[rows], sp.new_k[rows], sp.new_v[rows], sp.vocab,
+                            sp.logits_dtype, sp.target_logits[rows], sp.draft_logits[drows],
+                            sp.draft_tokens[drows], sp.u_accept[drows], sp.u_resample[seqs], sp.temperature,
+                            sp.mask_kind, None if sp.tree_mask is None else sp.tree_mask[rows],
+                            None if sp.parent is None else sp.parent[rows])
+    okv = oracle.OracleKV(sub, with_pools=False)
+    okv.k_pool, okv.v_pool = st.k_pool, st.v_pool
+    t0 = time.perf_counter()
+    assert okv.append(sub_step) is None
+    oracle.paged_attention(okv.as_state(), sub_step)
+    if sp.mask_kind == "tree":
+        r = oracle.tree_greedy(sub_step)
+        okv.rollback(sub_step, r.accept_cnt, path_nodes=r.path_nodes)
+    else:
+        r = oracle.rejection_sample(sub_step)
+        okv.rollback(sub_step, r.accept_cnt)
+    return time.perf_counter() - t0
+
+
+def cpu_seqs_for(case, budget_s=15.0):
+    """How many sequences of the batch fit the CPU budget (estimated from one)."""
+    t1 = oracle_sample_step(case, [0])
+    n = max(1, min(case.state.batch, int(budget_s / max(t1, 1e-3))))
+    return n, t1
+
+
+# ----------------------------------------------------------------------------
+# native arm
+# ----------------------------------------------------------------------------
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attn_traffic_record():
+    """DRAM traffic of the attention kernel from a committed ncu summary, valid
+    only while the kernel sources are unchanged (matching hash)."""
+    path = os.path.join(PROFILES, "attn_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    h = hashlib.sha256()
+    for name in ATTN_SOURCES:
+        h.update(open(os.path.join(ROOT, "speculative_decoding_verify_paged_gb300", "csrc", name), "rb").read())
+    return rec if rec.get("sources_sha256") == h.hexdigest() else None
+
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+    from speculative_decoding_verify_paged_gb300 import step as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    steps_total = args.steps + args.warmup + 2
+    case, desc = make_case(args.config, args.temperature, steps_total, seed_offset=rank)
+    st, sp = case.state, case.step
+    G = sp.num_q_heads // st.num_kv_heads
+    growth = 6 * steps_total if args.config == "llama8b" else 0
+    msl = int((st.seq_lens + sp.n_q).max()) + growth + 16
+
+    kv = S.device_kv(st, dev)
+    d = S.DeviceStep.from_host(sp, dev)
+    buf = S.StepBuffers.make(kv, d, msl, dev)
+    stream = torch.cuda.current_stream(dev)
+    c0 = kv.seq_lens.clone()
+
+    def one_step(ev=None):
+        S.append(kv, d, buf, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        S.attention(kv, d, buf, msl, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        S.sample(d, buf, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        S.rollback(kv, d, buf, stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0, "device status set during warm-up"
+    start_lens = kv.seq_lens.clone()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local, not args.no_clocks and rank == 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for s in range(args.steps):
+        one_step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    assert int(buf.status.item()) == 0, "device status set during the timed steps"
+    attn_ms = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
+    samp_ms = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
+
+    end_lens = kv.seq_lens.cpu().numpy().astype(np.int64)
+    sl = start_lens.cpu().numpy().astype(np.int64)
+    per_step_keep = (end_lens - sl) // args.steps  # a_b + 1, identical every step
+    emitted = int((end_lens - sl).sum())
+    # attention bytes, exactly, step by step: c_b(s) = c_b(start) + s * (a_b + 1)
+    ab = 0
+    fl = 0.0
+    for s in range(args.steps):
+        ctx = sl + s * per_step_keep
+        ab += attn_bytes(ctx + sp.n_q, sp, st)
+        fl += attn_flops(ctx, sp, G)
+    attn_bytes_avg = ab / args.steps
+    attn_ms_avg = float(np.mean(attn_ms))
+    samp_ms_avg = float(np.mean(samp_ms))
+
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed_ms = float(t.item())
+    B = st.batch
+    seqs_total = B * args.steps * world
+    value = seqs_total / (elapsed_ms / 1e3)
+
+    e2e = None if args.no_e2e else run_e2e(args, kv, d, buf, msl, sp, dev, stream, world)
+    hbm_peak, peak_kind = peaks()
+    achieved = attn_bytes_avg / (attn_ms_avg / 1e3) / 1e9
+    traffic = attn_traffic_record()
+    line = {
+        "metric": METRIC, "value": value, "unit": "seqs/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if st.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded numpy PCG64; no dataset or weights)",
+        "config": {"workload": desc, "global_batch": B * world, "scored_tokens_per_step": sp.total_q,
+                   "l2": "inputs larger than L2: each step streams the whole KV prefix (>300 MB) and the "
+                         "logits; L2 is 129 MB", "state": "cache evolves across steps (a_b+1 tokens kept)"},
+        "tokens_per_s": emitted * world / (elapsed_ms / 1e3),
+        "scored_tokens_per_s": sp.total_q * args.steps * world / (elapsed_ms / 1e3),
+        "mean_tokens_per_seq_step": emitted / (B * args.steps),
+        "roofline": {"kernel": "spec_verify_attn (split-KV attention + combine)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS, "peak_source": peak_kind,
+                     "traffic": (traffic["bytes_per_launch_scaled"] if traffic else None),
+                     "algorithmic_bytes_per_launch": attn_bytes_avg, "avg_launch_ms": attn_ms_avg,
+                     "tflops": fl / args.steps / (attn_ms_avg / 1e3) / 1e12},
+        "sampler_roofline": {"kernel": "spec_rejection_sample", "bound": "hbm",
+                             "achieved": sampler_bytes(sp) / (samp_ms_avg / 1e3) / 1e9, "peak": hbm_peak,
+                             "unit": "GB/s", "frac": sampler_bytes(sp) / (samp_ms_avg / 1e3) / 1e9 / hbm_peak,
+                             "algorithmic_bytes_per_launch": sampler_bytes(sp), "avg_launch_ms": samp_ms_avg},
+        "hbm_gbs_step": (attn_bytes_avg + sampler_bytes(sp)) / (elapsed_ms / args.steps / 1e3) / 1e9,
+        "gpu_launches": S.launches_per_step(d, msl, kv) * args.steps,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu:
+        n, t1 = cpu_seqs_for(case)
+        seqs = list(range(n))
+        t = oracle_sample_step(case, seqs)
+        line["cpu_baseline"] = {"value": n / t, "unit": "seqs/s", "cores": 1, "kind": "oracle",
+                                "sample": f"one verify step of {n} of the {B} sequences (fp64 C oracle: append, "
+                                          f"attention, sampler, rollback), {t:.1f} s, single thread"}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def run_e2e(args, kv, d, buf, msl, sp, dev, stream, world):
+    """The same step through the public API with the step's inputs in pinned host
+    memory: H2D of the inputs, the four calls, D2H of the results, every step."""
+    import torch
+    from speculative_decoding_verify_paged_gb300 import step as S
+    host = S.DeviceStep.tensors_of(sp, lambda x: S._host(x, pin=True))
+    names = [k for k, v in host.items() if v is not None]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    out_h = [torch.empty(buf.accept.shape, dtype=torch.int32).pin_memory(),
+             torch.empty(buf.out_tok.shape, dtype=torch.int32).pin_memory(),
+             torch.empty(buf.num_out.shape, dtype=torch.int32).pin_memory()]
+    d2h = sum(t.numel() * 4 for t in out_h)
+
+    def step_e2e():
+        for k in names:
+            getattr(d, k).copy_(host[k], non_blocking=True)
+        S.run_step(kv, d, buf, msl, stream)
+        out_h[0].copy_(buf.accept, non_blocking=True)
+        out_h[1].copy_(buf.out_tok, non_blocking=True)
+        out_h[2].copy_(buf.num_out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step_e2e()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(10, args.steps // 2)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(n):
+        step_e2e()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": d.batch * n * world / (ms / 1e3), "unit": "seqs/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms / n, "steps": n}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    case, desc = make_case(args.config, args.temperature, args.steps + args.warmup + 2)
+    n, t1 = cpu_seqs_for(case, budget_s=0.5)
+    seqs = list(range(n))
+    for _ in range(args.warmup):
+        oracle_sample_step(case, seqs)
+    ts = [oracle_sample_step(case, seqs) for _ in range(args.steps)]
+    total = float(np.sum(ts))
+    value = n * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "seqs/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy PCG64; no dataset or weights)",
+        "config": {"workload": desc, "global_batch": case.state.batch},
+        "cpu_baseline": {"value": value, "unit": "seqs/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the oracle's verify step for {n} of the {case.state.batch} "
+                                   f"sequences (fp64 C, single thread)"},
+        "e2e": {"value": value, "unit": "seqs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify, the batched speculative-decoding
+ * verification step over a paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * One verify step for a continuous batch is four calls on one CUDA stream:
+ *
+ *   sv_kv_append              write the K_b+1 new K/V rows of every sequence
+ *                             into its blocks, taking blocks from the free list
+ *   sv_spec_verify_attn       (K_b+1)-query GQA attention over the paged cache,
+ *                             causal or tree mask
+ *   sv_spec_rejection_sample  vocab-wide softmax of target and draft logits,
+ *                             accept test, first-reject scan and residual
+ *                             resample (or greedy / tree-greedy acceptance)
+ *   sv_kv_rollback            truncate every sequence at its accepted length
+ *
+ * Conventions shared by every call:
+ *  - Pointers are DEVICE pointers owned by the caller, unless stated. The
+ *    library never allocates, frees or keeps a pointer after a call returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream). Nothing synchronises with the host.
+ *  - The return value reports what the host can see: argument errors
+ *    (SV_ERR_INVALID_ARG / SV_ERR_UNSUPPORTED / SV_ERR_WORKSPACE, nothing is
+ *    launched) and launch errors (SV_ERR_CUDA).
+ *  - Errors found on the device go to `status_dev`, one int32 in device
+ *    memory. A kernel records its error only if the word still holds SV_OK
+ *    (the first error wins). sv_kv_append and sv_kv_rollback do nothing at all
+ *    while the word holds an error, so a failed step leaves the cache as it
+ *    was; the caller clears the word (writes 0) to go on.
+ *  - No C++ exception crosses this ABI.
+ *
+ * Query rows are ragged: sequence b owns rows cu_q[b] .. cu_q[b+1]-1 (n_b of
+ * them, 1 <= n_b <= max_q_per_seq <= 64). Row 0 of a sequence is the last
+ * emitted token; rows 1..n_b-1 are its draft tokens (chain) or its draft-tree
+ * nodes in BFS order (tree). Arrays on the draft side (draft logits, draft
+ * tokens, accept uniforms) have one entry per row except row 0: the entry of
+ * row i >= 1 sits at index cu_q[b] - b + i - 1.
+ *
+ * The method (pages on speculative decoding, cited by title and section):
+ *  - the target scores the K drafts plus one bonus position in one pass
+ *    ("Speculative decoding and continuous batching in practice", sec. 1.2);
+ *  - accept x with probability min(1, p(x)/q(x)); on the first rejection draw
+ *    from norm(max(0, p - q)) and drop the rest of the draft ("Speculative
+ *    decoding principles and a vLLM production setup", sec. 2.1-2.2);
+ *  - a block table maps each sequence's logical KV blocks to physical ones,
+ *    and blocks are taken only when the current one is full ("LLM serving:
+ *    speculative decoding and PagedAttention memory management",
+ *    PagedAttention section);
+ *  - on rejection only whole blocks of rejected positions go back, accepted
+ *    entries stay in place (vLLM page, sec. 3.1); tree drafts are verified in
+ *    one pass under a tree mask (vLLM page, sec. 3.2 and 5.2).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sv_status {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,   /* host: a pointer, size or enum is invalid */
+  SV_ERR_UNSUPPORTED = 2,   /* host: valid but not built (e.g. head_dim > 256) */
+  SV_ERR_CUDA = 3,          /* host: a CUDA launch or attribute call failed */
+  SV_ERR_OUT_OF_BLOCKS = 4, /* device: the free list holds too few blocks */
+  SV_ERR_TIMEOUT = 5,       /* device: a bounded wait inside a kernel gave up */
+  SV_ERR_BAD_BLOCK_ID = 6,  /* device: a block id outside [0, num_blocks) */
+  SV_ERR_BAD_LENGTH = 7,    /* device: a length, accept count or path entry out of range */
+  SV_ERR_BAD_TOKEN = 8,     /* device: a token id outside [0, vocab) */
+  SV_ERR_NONFINITE = 9,     /* device: a NaN or +inf logit, or a row without finite logits */
+  SV_ERR_WORKSPACE = 10     /* host: workspace missing or smaller than required */
+} sv_status;
+
+typedef enum sv_dtype { SV_DTYPE_BF16 = 0, SV_DTYPE_F32 = 1 } sv_dtype;
+
+typedef enum sv_mask_kind { SV_MASK_CAUSAL = 0, SV_MASK_TREE = 1 } sv_mask_kind;
+
+/*
+ * One layer's paged KV cache. Every pointer is a caller-owned device pointer.
+ *   k_pool, v_pool   [num_blocks, num_kv_heads, block_size, head_dim] of dtype,
+ *                    head-major inside a block: the rows of one (block, head)
+ *                    are contiguous (block_size * head_dim elements)
+ *   block_table      int32 [batch, max_blocks_per_seq]: logical -> physical
+ *                    block; -1 marks "no block"
+ *   seq_lens         int32 [batch]: committed tokens c_b (KV rows kept)
+ *   free_list        int32 [num_blocks]: a stack of free physical ids; entries
+ *                    [0, *free_top) are valid, entry *free_top-1 is the top
+ *   free_top         int32 [1]
+ * block_size: a power of two in [1, 256]; head_dim: a multiple of 8 in
+ * [8, 256]; dtype: SV_DTYPE_BF16 or SV_DTYPE_F32.
+ */
+typedef struct sv_paged_kv {
+  void *k_pool;
+  void *v_pool;
+  int32_t *block_table;
+  int32_t *seq_lens;
+  int32_t *free_list;
+  int32_t *free_top;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t max_blocks_per_seq;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t batch;
+  int32_t dtype;
+} sv_paged_kv;
+
+/*
+ * sv_kv_append -- write the new K/V rows of every sequence into the cache.
+ *
+ * Sequence b needs ceil((c_b + n_b) / bs) - ceil(c_b / bs) new blocks (a block
+ * is taken only when the current one is full). They are popped from the free
+ * list in (sequence, logical block) order: the top entry goes to sequence 0's
+ * first new block. Row j of sequence b (new_k[cu_q[b] + j]) is then written at
+ * logical position c_b + j: physical block block_table[b][(c_b+j) / bs], slot
+ * (c_b+j) % bs, for every KV head. seq_lens is not changed (the new rows are
+ * pending until sv_kv_rollback).
+ *   new_k, new_v  [total_q, num_kv_heads, head_dim] of kv->dtype
+ *   cu_q          int32 [batch + 1], cu_q[0] = 0, cu_q[batch] = total_q
+ *   status_dev    int32 [1], required
+ * All or nothing: if the blocks would not fit the block table
+ * (SV_ERR_BAD_LENGTH), the free list is too short (SV_ERR_OUT_OF_BLOCKS), or a
+ * popped id is out of range (SV_ERR_BAD_BLOCK_ID), nothing is written.
+ * Popped free-list entries are overwritten with -1.
+ */
+sv_status sv_kv_append(const sv_paged_kv *kv, const void *new_k, const void *new_v, const int32_t *cu_q,
+                       int32_t total_q, int32_t *status_dev, void *stream);
+
+/*
+ * Workspace bytes sv_spec_verify_attn needs for these sizes (split-KV partial
+ * results: per split, query row and query head, head_dim floats plus one
+ * log-sum-exp). max_seq_len bounds c_b + n_b over the batch.
+ */
+size_t sv_spec_verify_attn_workspace_bytes(const sv_paged_kv *kv, int32_t num_q_heads, int32_t total_q,
+                                           int32_t max_q_per_seq, int32_t max_seq_len);
+
+/*
+ * sv_spec_verify_attn -- (K+1)-query grouped-query attention over the paged
+ * cache, after sv_kv_append has written the step's rows.
+ *
+ * For sequence b with L_b = c_b + n_b tokens (c_b = seq_lens[b]), query row i
+ * (0 <= i < n_b) and query head h (KV head h / (num_q_heads / num_kv_heads)):
+ *   out[row][h] = sum_t softmax_t(scale * <q[row][h], k_t>) v_t
+ * over the visible t < L_b: all committed t < c_b, plus new row j = t - c_b
+ * when j <= i (SV_MASK_CAUSAL) or when bit j of tree_mask[row] is set
+ * (SV_MASK_TREE: the row's ancestors and itself; the caller sets the bits).
+ * Softmax and accumulation are fp32; a row that sees no key gets zeros.
+ *   q, out      [total_q, num_q_heads, head_dim] of kv->dtype
+ *   cu_q        int32 [batch + 1]
+ *   tree_mask   uint64 [total_q] for SV_MASK_TREE, else NULL
+ *   max_seq_len an upper bound of c_b + n_b (sizes the launch; a longer
+ *               sequence sets SV_ERR_BAD_LENGTH and its rows are not written)
+ *   workspace   device scratch of at least sv_spec_verify_attn_workspace_bytes
+ *   status_dev  int32 [1] or NULL
+ * Block ids outside [0, num_blocks) set SV_ERR_BAD_BLOCK_ID; the rows of that
+ * sequence are then undefined, no out-of-bounds memory is touched.
+ */
+sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, const int32_t *cu_q,
+                              int32_t num_q_heads, int32_t total_q, int32_t max_q_per_seq,
+                              int32_t max_seq_len, float scale, int32_t mask_kind, const uint64_t *tree_mask,
+                              void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream);
+
+/*
+ * sv_spec_rejection_sample -- lossless verification of chain drafts.
+ *
+ * Target row cu_q[b] + i holds the logits of the position that draft token
+ * x_{i+1} fills (row 0 scores x_1; row n_b-1 is the bonus position). With
+ * temperature T > 0: p = softmax(l_target / T), q = softmax(l_draft / T) over
+ * the vocabulary; for i = 0..K_b-1 (K_b = n_b - 1) x is accepted iff
+ * u_accept < min(1, p(x)/q(x)) (q(x) == 0 counts as accept); a_b is the first
+ * rejected i, or K_b. Then one token y is drawn by inverse CDF with
+ * u_resample[b]: from norm(max(0, p_a - q_a)) when a_b < K_b (from p_a if that
+ * residual has no mass), from p_K when every draft was accepted: y is the
+ * smallest index whose inclusive prefix sum exceeds u_resample[b] times the
+ * total mass. With T == 0 (greedy): x is accepted while it equals the target
+ * argmax (lowest index on ties) and y is the argmax of row a_b; draft_logits,
+ * u_accept and u_resample are not read and may be NULL.
+ *   target_logits  [total_q, vocab] of logits_dtype (bf16 or f32)
+ *   draft_logits   [total_q - batch, vocab]
+ *   draft_tokens   int32 [total_q - batch]
+ *   u_accept       float [total_q - batch], in [0, 1)
+ *   u_resample     float [batch], in [0, 1)
+ *   accept_count   int32 [batch] out: a_b
+ *   out_tokens     int32 [batch, max_q_per_seq] out: x_1..x_a, y, then -1
+ *   num_out        int32 [batch] out: a_b + 1
+ *   status_dev     int32 [1] or NULL: SV_ERR_NONFINITE for NaN/+inf logits,
+ *                  SV_ERR_BAD_TOKEN for a draft token outside the vocabulary
+ * Arithmetic is fp32; decisions equal the exact ones except when a uniform
+ * lies within about 1e-6 of its threshold.
+ */
+sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_logits, int32_t logits_dtype,
+                                   int32_t vocab, int32_t batch, const int32_t *cu_q, int32_t total_q,
+                                   int32_t max_q_per_seq, const int32_t *draft_tokens, const float *u_accept,
+                                   const float *u_resample, float temperature, int32_t *accept_count,
+                                   int32_t *out_tokens, int32_t *num_out, int32_t *status_dev, void *stream);
+
+/*
+ * sv_tree_greedy_accept -- greedy verification of a draft tree (the tree mode
+ * of the sampler). Row 0 of a sequence is the root; node row j >= 1 has parent
+ * row parent[cu_q[b] + j] and token node_tokens[cu_q[b] - b + j - 1]. From the
+ * root, move to the child (lowest row first) whose token equals the argmax of
+ * the current node's target row, while there is one; y = argmax of the last
+ * node's row.
+ *   parent        int32 [total_q]: parent row within the sequence, -1 for row 0
+ *   accept_count  int32 [batch] out: a_b, the accepted path length
+ *   path_nodes    int32 [batch, max_q_per_seq] out: rows of the accepted
+ *                 nodes in path order, then -1 (input of sv_kv_rollback)
+ *   out_tokens    int32 [batch, max_q_per_seq] out: path tokens, y, then -1
+ *   num_out       int32 [batch] out: a_b + 1
+ */
+sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype, int32_t vocab, int32_t batch,
+                                const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq,
+                                const int32_t *node_tokens, const int32_t *parent, int32_t *accept_count,
+                                int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out,
+                                int32_t *status_dev, void *stream);
+
+/*
+ * sv_kv_rollback -- keep each sequence's accepted prefix, give back the rest.
+ *
+ * The new length is c_b + a_b + 1: the last emitted token and the a_b
+ * accepted rows keep their KV where it is; the resampled token has no KV yet.
+ * With path_nodes (tree drafts), the accepted path's rows are first copied, in
+ * path order, to logical positions c_b + 1 .. c_b + a_b. Blocks with logical
+ * index >= ceil(new_len / bs) that held this step's rows are pushed on the
+ * free list in sequence order, highest logical block first, and their block
+ * table entries set to -1. seq_lens[b] becomes the new length.
+ *   cu_q          int32 [batch + 1] (the step's rows, as given to sv_kv_append)
+ *   accept_count  int32 [batch]: 0 <= a_b <= n_b - 1
+ *   path_nodes    int32 [batch, max_q_per_seq] or NULL (chain drafts)
+ *   status_dev    int32 [1], required
+ * All or nothing: an accept count or path entry out of range sets
+ * SV_ERR_BAD_LENGTH and changes nothing.
+ */
+sv_status sv_kv_rollback(const sv_paged_kv *kv, const int32_t *cu_q, const int32_t *accept_count,
+                         const int32_t *path_nodes, int32_t max_q_per_seq, int32_t *status_dev, void *stream);
+
+/* A static, human-readable name of a status code. */
+const char *sv_status_string(int32_t status);
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+int32_t sv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

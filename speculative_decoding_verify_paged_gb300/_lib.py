@@ -1,0 +1,205 @@
+"""ctypes binding of libspecverify (include/spec_verify.h).
+
+Argument marshalling only: every function takes torch CUDA tensors, passes
+their device pointers and the current CUDA stream to the C ABI, and raises
+SVError on a non-OK return. Nothing here computes any part of the verify
+step, and nothing falls back to the CPU: a missing library or a CPU tensor is
+an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+
+SV_OK = 0
+SV_DTYPE_BF16, SV_DTYPE_F32 = 0, 1
+SV_MASK_CAUSAL, SV_MASK_TREE = 0, 1
+STATUS_NAMES = {
+    0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_CUDA",
+    4: "SV_ERR_OUT_OF_BLOCKS", 5: "SV_ERR_TIMEOUT", 6: "SV_ERR_BAD_BLOCK_ID", 7: "SV_ERR_BAD_LENGTH",
+    8: "SV_ERR_BAD_TOKEN", 9: "SV_ERR_NONFINITE", 10: "SV_ERR_WORKSPACE",
+}
+
+EXPORTS = ("sv_kv_append", "sv_spec_verify_attn_workspace_bytes", "sv_spec_verify_attn",
+           "sv_spec_rejection_sample", "sv_tree_greedy_accept", "sv_kv_rollback", "sv_status_string",
+           "sv_version")
+
+
+class SVError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)}")
+
+
+class sv_paged_kv(ctypes.Structure):
+    _fields_ = [
+        ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+        ("free_list", ctypes.c_void_p), ("free_top", ctypes.c_void_p),
+        ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("batch", ctypes.c_int32), ("dtype", ctypes.c_int32),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libspecverify.so (building it with nvcc first if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            if not build_if_missing:
+                raise RuntimeError(f"{p} is not built")
+            from . import build as _build
+            _build.build()
+        lib = ctypes.CDLL(p)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        KVP = ctypes.POINTER(sv_paged_kv)
+        sig = {
+            "sv_kv_append": (I, [KVP, P, P, P, I, P, P]),
+            "sv_spec_verify_attn_workspace_bytes": (S, [KVP, I, I, I, I]),
+            "sv_spec_verify_attn": (I, [KVP, P, P, P, I, I, I, I, F, I, P, P, S, P, P]),
+            "sv_spec_rejection_sample": (I, [P, P, I, I, I, P, I, I, P, P, P, F, P, P, P, P, P]),
+            "sv_tree_greedy_accept": (I, [P, I, I, I, P, I, I, P, P, P, P, P, P, P, P]),
+            "sv_kv_rollback": (I, [KVP, P, P, P, I, P, P]),
+            "sv_status_string": (ctypes.c_char_p, [I]),
+            "sv_version": (I, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().sv_status_string(int(code)).decode()
+    except Exception:  # the library may be what failed to load
+        return STATUS_NAMES.get(int(code), f"status {code}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("libspecverify takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libspecverify takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int, what: str):
+    if rc != SV_OK:
+        raise SVError(rc, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SV_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return SV_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+@dataclass
+class PagedKV:
+    """One layer's paged KV cache held in torch CUDA tensors (see sv_paged_kv)."""
+
+    k_pool: torch.Tensor  # [num_blocks, num_kv_heads, block_size, head_dim]
+    v_pool: torch.Tensor
+    block_table: torch.Tensor  # int32 [batch, max_blocks_per_seq]
+    seq_lens: torch.Tensor  # int32 [batch]
+    free_list: torch.Tensor  # int32 [num_blocks]
+    free_top: torch.Tensor  # int32 [1]
+
+    def struct(self) -> sv_paged_kv:
+        nb, hkv, bs, d = self.k_pool.shape
+        return sv_paged_kv(
+            _ptr(self.k_pool), _ptr(self.v_pool), _ptr(self.block_table), _ptr(self.seq_lens),
+            _ptr(self.free_list), _ptr(self.free_top), nb, bs, self.block_table.shape[1], hkv, d,
+            self.seq_lens.shape[0], _dtype_code(self.k_pool))
+
+    @property
+    def batch(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+
+def kv_append(kv: PagedKV, new_k: torch.Tensor, new_v: torch.Tensor, cu_q: torch.Tensor,
+              status: torch.Tensor, stream=None) -> None:
+    s = kv.struct()
+    _check(load().sv_kv_append(ctypes.byref(s), _ptr(new_k), _ptr(new_v), _ptr(cu_q), int(new_k.shape[0]),
+                               _ptr(status), _stream(stream)), "sv_kv_append")
+
+
+def spec_verify_attn_workspace_bytes(kv: PagedKV, num_q_heads: int, total_q: int, max_q: int,
+                                     max_seq_len: int) -> int:
+    s = kv.struct()
+    return int(load().sv_spec_verify_attn_workspace_bytes(ctypes.byref(s), num_q_heads, total_q, max_q,
+                                                          max_seq_len))
+
+
+def spec_verify_attn(kv: PagedKV, q: torch.Tensor, out: torch.Tensor, cu_q: torch.Tensor, *, max_q: int,
+                     max_seq_len: int, scale: float, mask_kind: int = SV_MASK_CAUSAL,
+                     tree_mask: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     status: Optional[torch.Tensor] = None, stream=None) -> None:
+    s = kv.struct()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().sv_spec_verify_attn(ctypes.byref(s), _ptr(q), _ptr(out), _ptr(cu_q), int(q.shape[1]),
+                                      int(q.shape[0]), int(max_q), int(max_seq_len), float(scale), int(mask_kind),
+                                      _ptr(tree_mask), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)),
+           "sv_spec_verify_attn")
+
+
+def spec_rejection_sample(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor], cu_q: torch.Tensor,
+                          draft_tokens: Optional[torch.Tensor], u_accept: Optional[torch.Tensor],
+                          u_resample: Optional[torch.Tensor], temperature: float, accept_count: torch.Tensor,
+                          out_tokens: torch.Tensor, num_out: torch.Tensor, *, status: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    batch = int(cu_q.shape[0]) - 1
+    _check(load().sv_spec_rejection_sample(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), int(target_logits.shape[1]), batch,
+        _ptr(cu_q), int(target_logits.shape[0]), int(out_tokens.shape[1]), _ptr(draft_tokens), _ptr(u_accept),
+        _ptr(u_resample), float(temperature), _ptr(accept_count), _ptr(out_tokens), _ptr(num_out), _ptr(status),
+        _stream(stream)), "sv_spec_rejection_sample")
+
+
+def tree_greedy_accept(target_logits: torch.Tensor, cu_q: torch.Tensor, node_tokens: torch.Tensor,
+                       parent: torch.Tensor, accept_count: torch.Tensor, path_nodes: torch.Tensor,
+                       out_tokens: torch.Tensor, num_out: torch.Tensor, *, status: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    batch = int(cu_q.shape[0]) - 1
+    _check(load().sv_tree_greedy_accept(
+        _ptr(target_logits), _dtype_code(target_logits), int(target_logits.shape[1]), batch, _ptr(cu_q),
+        int(target_logits.shape[0]), int(out_tokens.shape[1]), _ptr(node_tokens), _ptr(parent),
+        _ptr(accept_count), _ptr(path_nodes), _ptr(out_tokens), _ptr(num_out), _ptr(status), _stream(stream)),
+        "sv_tree_greedy_accept")
+
+
+def kv_rollback(kv: PagedKV, cu_q: torch.Tensor, accept_count: torch.Tensor, status: torch.Tensor, *,
+                max_q: int, path_nodes: Optional[torch.Tensor] = None, stream=None) -> None:
+    s = kv.struct()
+    _check(load().sv_kv_rollback(ctypes.byref(s), _ptr(cu_q), _ptr(accept_count), _ptr(path_nodes), int(max_q),
+                                 _ptr(status), _stream(stream)), "sv_kv_rollback")

@@ -1,0 +1,534 @@
+// Fused verification sampler: one thread-block cluster per sequence.
+//
+// What it computes ("Speculative decoding and continuous batching in
+// practice", sec. 1.2; "Speculative decoding principles and a vLLM production
+// setup", sec. 2.1-2.2; greedy form: "LLM inference optimisation: speculative
+// decoding and dynamic batching", engineering section):
+//   p_i = softmax(l_target,i / T), q_i = softmax(l_draft,i / T);
+//   accept x_i iff u_i < min(1, p_i(x_i) / q_i(x_i)), scanning i in order;
+//   at the first rejection a, draw y from norm(max(0, p_a - q_a)) by inverse
+//   CDF with u'; if all K drafts pass, draw y from p_K.
+//   Greedy: accept while x_i == argmax p_i; y = argmax p_a.
+//   Tree greedy: walk from the root to the child whose token is the argmax of
+//   the current node's row; y = argmax of the last node's row.
+//
+// How: the vocabulary is cut into C equal chunks, one per CTA of the cluster.
+//   phase 1  every CTA streams its chunk of every row of the sequence (target
+//            rows and draft rows) once with 16-byte loads and keeps a running
+//            (max, sum of exp2) per row (argmax for greedy modes); work items
+//            are (row, 1024-element sub-chunk) pairs spread over the warps.
+//   phase 2  cluster barrier; every CTA combines the C partial results of
+//            every row through distributed shared memory in rank order, so all
+//            CTAs hold identical row statistics and take identical decisions.
+//   phase 3  (T > 0) every CTA computes the weights w_v (residual or p) over
+//            its chunk and their sum; after a cluster barrier the prefix over
+//            ranks tells which CTA holds the crossing u' * S; that CTA rescans
+//            its chunk (block-wide prefix sums, same order) and finds y.
+// All reductions run in a fixed order, so results are deterministic.
+#include <cooperative_groups.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "sv_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace sv {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxQ = 64;
+constexpr int kMaxRows = 2 * kMaxQ;  // target + draft rows of one sequence
+constexpr int kSub = 1024;           // elements per work item
+constexpr int kMaxSub = 16;          // => at most 16384 elements per CTA chunk
+constexpr int kSegPer = 8;           // phase 3: elements per thread per segment
+constexpr int kSeg = kThreads * kSegPer;
+
+template <typename T> struct VecTraits;
+template <> struct VecTraits<__nv_bfloat16> { static constexpr int N = 8; };
+template <> struct VecTraits<float> { static constexpr int N = 4; };
+
+// Load the 32 values a lane owns in [e0, e1) of a row (1024-element item).
+// Vector layout: vector u of the lane covers e0 + (u*32 + lane)*N .. +N.
+// Scalar layout: value k of the lane is e0 + k*32 + lane.
+template <typename T, bool VEC>
+__device__ __forceinline__ void load_item(const T *__restrict__ row, int e0, int e1, int lane, float (&v)[32],
+                                          int (&idx)[32]) {
+  if constexpr (VEC) {
+    constexpr int N = VecTraits<T>::N;
+    constexpr int U = 32 / N;
+    uint4 raw[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + (u * 32 + lane) * N;
+      if (e < e1) raw[u] = __ldg(reinterpret_cast<const uint4 *>(row + e));
+      else raw[u] = make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + (u * 32 + lane) * N;
+      const T *t = reinterpret_cast<const T *>(&raw[u]);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        v[u * N + k] = to_f32(t[k]);
+        idx[u * N + k] = (e + k < e1) ? e + k : -1;  // chunks are multiples of N: all or none valid
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int e = e0 + k * 32 + lane;
+      v[k] = e < e1 ? to_f32(row[e]) : 0.f;
+      idx[k] = e < e1 ? e : -1;
+    }
+  }
+}
+
+// (max, sum) pair combine in the exp2 domain; m == -inf means "empty".
+__device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) {
+    m = mn;
+    s = 0.f;
+    return;
+  }
+  s = s * exp2f(m - mn) + s2 * exp2f(m2 - mn);
+  m = mn;
+}
+
+// argmax combine: larger value wins, lower index on ties; idx -1 = empty.
+__device__ __forceinline__ void am_combine(float &v, int &i, float v2, int i2) {
+  if (i2 < 0) return;
+  if (i < 0 || v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+// Block-wide exclusive scan of one float per thread (fixed order).
+__device__ float block_excl_scan_f(float x, float *warp_buf /*[kWarps]*/, float *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_buf[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    float w = lane < kWarps ? warp_buf[lane] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kWarps) warp_buf[lane] = w;
+  }
+  __syncthreads();
+  const float excl_in_warp = __shfl_up_sync(0xffffffffu, inc, 1);
+  float excl = (lane == 0 ? 0.f : excl_in_warp);
+  if (warp > 0) excl = warp_buf[warp - 1] + excl;
+  *total = warp_buf[kWarps - 1];
+  __syncthreads();
+  return excl;
+}
+
+struct Smem {
+  float pm[kMaxRows][kMaxSub];  // per item: max (z domain) or best value
+  float ps[kMaxRows][kMaxSub];  // per item: sum of exp2, or best index (as int bits)
+  float rm[kMaxRows];           // per row, this CTA's chunk (cluster-visible)
+  float rs[kMaxRows];
+  int ri[kMaxRows];
+  float tl[kMaxQ];  // target logit of the draft token, if this CTA owns it (cluster-visible)
+  float dl[kMaxQ];
+  float M[kMaxRows];  // per row, whole vocabulary (after phase 2)
+  float Z[kMaxRows];
+  int am[kMaxRows];
+  float gtl[kMaxQ], gdl[kMaxQ];
+  float S[2];  // phase 3: this CTA's weight sum per pass (cluster-visible)
+  float warp_buf[kWarps];
+  float seg_total;
+  int a;
+  int bad;
+  int y_min, y_last;
+  int owner, no_cross, fallback;
+  float P_owner, target;
+};
+
+template <typename T, bool VEC, int MODE>
+__global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ Smem sm;
+
+  const int V = args.vocab;
+  const int t0 = args.cu_q[b];
+  const int n = args.cu_q[b + 1] - t0;
+  const int K = n - 1;
+  const int d0 = t0 - b;
+  const int lo = min(V, rank * args.chunk), hi = min(V, lo + args.chunk);
+  const int len = hi - lo;
+  const int nsub = (len + kSub - 1) / kSub;
+  const int rows = (MODE == kStochastic) ? n + K : n;
+  const T *tgt = reinterpret_cast<const T *>(args.tgt);
+  const T *drf = reinterpret_cast<const T *>(args.drf);
+  const float coef = args.coef;
+
+  // rows outside [0, total_q) or more than max_q rows: nothing is read or written.
+  // Every CTA of the cluster takes this exit together (same b), before any barrier.
+  if (n < 1 || n > args.max_q || t0 < 0 || t0 + n > args.total_q) {
+    if (rank == 0 && tid == 0) record(args.status, SV_ERR_BAD_LENGTH);
+    return;
+  }
+  if (tid == 0) sm.bad = 0;
+  __syncthreads();
+
+  // ---------------- phase 1: per-item partial statistics ----------------
+  int bad = 0;
+  const int items = rows * nsub;
+  for (int it = warp; it < items; it += kWarps) {
+    const int r = it / nsub, s = it % nsub;
+    const T *row = (r < n) ? tgt + (size_t)(t0 + r) * V : drf + (size_t)(d0 + (r - n)) * V;
+    const int e0 = lo + s * kSub, e1 = min(hi, e0 + kSub);
+    float v[32];
+    int idx[32];
+    load_item<T, VEC>(row, e0, e1, lane, v, idx);
+    if constexpr (MODE == kStochastic) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (idx[k] >= 0) {
+          bad |= (v[k] != v[k]) | (v[k] == INFINITY);
+          m = fmaxf(m, v[k] * coef);
+        }
+      float sum = 0.f;
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (idx[k] >= 0) sum += exp2f(fmaf(v[k], coef, -m));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+        ms_combine(m, sum, m2, s2);
+      }
+      if (lane == 0) {
+        sm.pm[r][s] = m;
+        sm.ps[r][s] = sum;
+      }
+    } else {
+      float best = 0.f;
+      int bi = -1;
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (idx[k] >= 0) {
+          bad |= (v[k] != v[k]);
+          am_combine(best, bi, v[k], idx[k]);
+        }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        am_combine(best, bi, v2, i2);
+      }
+      if (lane == 0) {
+        sm.pm[r][s] = best;
+        sm.ps[r][s] = __int_as_float(bi);
+      }
+    }
+  }
+  // token logits of the draft tokens this CTA owns
+  if constexpr (MODE == kStochastic) {
+    if (tid < K) {
+      const int x = args.draft_tok[d0 + tid];
+      if (x < 0 || x >= V) {
+        record(args.status, SV_ERR_BAD_TOKEN);
+      } else if (x >= lo && x < hi) {
+        sm.tl[tid] = to_f32(tgt[(size_t)(t0 + tid) * V + x]);
+        sm.dl[tid] = to_f32(drf[(size_t)(d0 + tid) * V + x]);
+      }
+    }
+  }
+  if (bad) atomicOr(&sm.bad, 1);
+  __syncthreads();
+  if (tid < rows) {
+    if constexpr (MODE == kStochastic) {
+      float m = -INFINITY, s = 0.f;
+      for (int k = 0; k < nsub; ++k) ms_combine(m, s, sm.pm[tid][k], sm.ps[tid][k]);
+      sm.rm[tid] = m;
+      sm.rs[tid] = s;
+    } else {
+      float best = 0.f;
+      int bi = -1;
+      for (int k = 0; k < nsub; ++k) am_combine(best, bi, sm.pm[tid][k], __float_as_int(sm.ps[tid][k]));
+      sm.rm[tid] = best;
+      sm.ri[tid] = bi;
+    }
+  }
+  if (tid == 0 && sm.bad) record(args.status, SV_ERR_NONFINITE);
+  cluster.sync();
+
+  // ---------------- phase 2: combine across the cluster ----------------
+  if (tid < rows) {
+    if constexpr (MODE == kStochastic) {
+      float m = -INFINITY, s = 0.f;
+      for (int q = 0; q < C; ++q) {
+        const float m2 = *cluster.map_shared_rank(&sm.rm[tid], q);
+        const float s2 = *cluster.map_shared_rank(&sm.rs[tid], q);
+        ms_combine(m, s, m2, s2);
+      }
+      sm.M[tid] = m;
+      sm.Z[tid] = s;
+    } else {
+      float best = 0.f;
+      int bi = -1;
+      for (int q = 0; q < C; ++q)
+        am_combine(best, bi, *cluster.map_shared_rank(&sm.rm[tid], q), *cluster.map_shared_rank(&sm.ri[tid], q));
+      sm.am[tid] = bi;
+    }
+  }
+  if constexpr (MODE == kStochastic) {
+    if (tid < K) {
+      const int x = args.draft_tok[d0 + tid];
+      const int owner = (x >= 0 && x < V) ? min(x / args.chunk, C - 1) : 0;
+      sm.gtl[tid] = *cluster.map_shared_rank(&sm.tl[tid], owner);
+      sm.gdl[tid] = *cluster.map_shared_rank(&sm.dl[tid], owner);
+    }
+  }
+  __syncthreads();
+
+  if constexpr (MODE == kGreedy) {
+    if (rank == 0 && tid == 0) {
+      int a = K;
+      for (int i = 0; i < K; ++i)
+        if (args.draft_tok[d0 + i] != sm.am[i]) {
+          a = i;
+          break;
+        }
+      int32_t *o = args.out_tok + (size_t)b * args.max_q;
+      for (int j = 0; j < args.max_q; ++j) o[j] = j < a ? args.draft_tok[d0 + j] : -1;
+      o[a] = sm.am[a];
+      args.accept[b] = a;
+      args.num_out[b] = a + 1;
+    }
+  } else if constexpr (MODE == kTree) {
+    if (rank == 0 && tid == 0) {
+      int32_t *o = args.out_tok + (size_t)b * args.max_q;
+      int32_t *path = args.path + (size_t)b * args.max_q;
+      for (int j = 0; j < args.max_q; ++j) {
+        o[j] = -1;
+        path[j] = -1;
+      }
+      int cur = 0, a = 0, am = sm.am[0];
+      bool ok = true;
+      for (int j = 1; j < n; ++j) {
+        const int p = args.parent[t0 + j];
+        ok &= (p >= 0 && p < n && p != j);
+      }
+      if (!ok) record(args.status, SV_ERR_BAD_LENGTH);
+      while (ok && a < n - 1) {
+        am = sm.am[cur];
+        int next = -1;
+        for (int j = 1; j < n; ++j)
+          if (args.parent[t0 + j] == cur && args.draft_tok[d0 + j - 1] == am) {
+            next = j;
+            break;
+          }
+        if (next < 0) break;
+        path[a] = next;
+        o[a] = am;
+        ++a;
+        cur = next;
+      }
+      am = sm.am[cur];
+      o[a] = am;
+      args.accept[b] = a;
+      args.num_out[b] = a + 1;
+    }
+  } else {
+    // ---------------- accept scan (identical in every CTA) ----------------
+    if (tid == 0) {
+      int a = K;
+      for (int i = 0; i < K; ++i) {
+        const float Zt = sm.Z[i], Zd = sm.Z[n + i];
+        const float p = exp2f(fmaf(sm.gtl[i], coef, -sm.M[i])) / Zt;
+        const float q = exp2f(fmaf(sm.gdl[i], coef, -sm.M[n + i])) / Zd;
+        const float thr = q > 0.f ? fminf(1.f, p / q) : 1.f;
+        if (!(args.u_acc[d0 + i] < thr)) {
+          a = i;
+          break;
+        }
+      }
+      sm.a = a;
+      for (int r = 0; r < rows; ++r)
+        if (!(sm.Z[r] > 0.f)) sm.bad = 1;
+      if (sm.bad && rank == 0) record(args.status, SV_ERR_NONFINITE);
+    }
+    __syncthreads();
+    const int a = sm.a;
+    const T *trow = tgt + (size_t)(t0 + a) * V;
+    const T *drow = (a < K) ? drf + (size_t)(d0 + a) * V : nullptr;
+    const float Mt = sm.M[a], invZt = 1.f / sm.Z[a];
+    const float Md = (a < K) ? sm.M[n + a] : 0.f, invZd = (a < K) ? 1.f / sm.Z[n + a] : 0.f;
+    const float ur = args.u_res[b];
+
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool resid = (a < K) && pass == 0;
+      auto weight = [&](int e) -> float {
+        const float p = exp2f(fmaf(to_f32(trow[e]), coef, -Mt)) * invZt;
+        if (!resid) return p;
+        const float q = exp2f(fmaf(to_f32(drow[e]), coef, -Md)) * invZd;
+        return fmaxf(p - q, 0.f);
+      };
+      // this CTA's weight sum, by segments of kSeg elements (fixed order)
+      float carry = 0.f;
+      for (int s0 = lo; s0 < hi; s0 += kSeg) {
+        float local = 0.f;
+        const int e = s0 + tid * kSegPer;
+#pragma unroll
+        for (int k = 0; k < kSegPer; ++k)
+          if (e + k < hi) local += weight(e + k);
+        float seg_total;
+        block_excl_scan_f(local, sm.warp_buf, &seg_total);
+        carry = carry + seg_total;
+      }
+      if (tid == 0) sm.S[pass] = carry;
+      cluster.sync();
+      if (tid == 0) {
+        float S = 0.f;
+        for (int q = 0; q < C; ++q) S = S + *cluster.map_shared_rank(&sm.S[pass], q);
+        const float target = ur * S;
+        float cum = 0.f;
+        int owner = -1, last_pos = -1;
+        float P = 0.f;
+        for (int q = 0; q < C; ++q) {
+          const float Sq = *cluster.map_shared_rank(&sm.S[pass], q);
+          const float prev = cum;
+          cum = cum + Sq;
+          if (Sq > 0.f) last_pos = q;
+          if (owner < 0 && cum > target) {
+            owner = q;
+            P = prev;
+          }
+        }
+        sm.no_cross = 0;
+        if (owner < 0) {
+          owner = last_pos;
+          sm.no_cross = 1;
+        }
+        sm.owner = owner;
+        sm.P_owner = P;
+        sm.target = target;
+        sm.fallback = (resid && !(S > 0.f)) ? 1 : 0;
+        sm.y_min = INT_MAX;
+        sm.y_last = -1;
+      }
+      __syncthreads();
+      if (sm.fallback) continue;  // residual without mass: draw from p_a instead
+      if (rank == sm.owner) {
+        const float P = sm.P_owner, target = sm.target;
+        float carry2 = 0.f;
+        for (int s0 = lo; s0 < hi; s0 += kSeg) {
+          float w[kSegPer];
+          float local = 0.f;
+          const int e = s0 + tid * kSegPer;
+#pragma unroll
+          for (int k = 0; k < kSegPer; ++k) {
+            w[k] = (e + k < hi) ? weight(e + k) : 0.f;
+            local += w[k];
+          }
+          float seg_total;
+          const float excl = block_excl_scan_f(local, sm.warp_buf, &seg_total);
+          float inc = 0.f;
+#pragma unroll
+          for (int k = 0; k < kSegPer; ++k) {
+            inc += w[k];
+            if (w[k] > 0.f) {
+              if (!sm.no_cross && P + (carry2 + (excl + inc)) > target) atomicMin(&sm.y_min, e + k);
+              atomicMax(&sm.y_last, e + k);
+            }
+          }
+          carry2 = carry2 + seg_total;
+        }
+        __syncthreads();
+        if (tid == 0) {
+          const int y = (sm.y_min != INT_MAX) ? sm.y_min : sm.y_last;
+          int32_t *o = args.out_tok + (size_t)b * args.max_q;
+          for (int j = 0; j < args.max_q; ++j) o[j] = j < a ? args.draft_tok[d0 + j] : -1;
+          o[a] = y;
+          args.accept[b] = a;
+          args.num_out[b] = a + 1;
+        }
+      }
+      break;
+    }
+  }
+  cluster.sync();  // keep this CTA's shared memory alive until every peer is done reading it
+}
+
+int pick_cluster(int batch, int vocab) {
+  const int sms = num_sms();
+  int C = (batch * 8 < 3 * sms) ? 16 : 8;
+  if ((vocab + 7) / 8 * 8 > 8 * kSub * kMaxSub) C = 16;
+  return C;
+}
+
+template <typename T, bool VEC, int MODE>
+cudaError_t launch_t(const SamplerArgs &a0, int C, cudaStream_t st) {
+  SamplerArgs a = a0;
+  auto kern = sampler_kernel<T, VEC, MODE>;
+  if (C > 8) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, a.batch, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <typename T, int MODE>
+cudaError_t launch_m(const SamplerArgs &a, int C, cudaStream_t st) {
+  const bool vec = ((size_t)a.vocab * sizeof(T)) % 16 == 0 && ((uintptr_t)a.tgt % 16 == 0) &&
+                   (a.drf == nullptr || (uintptr_t)a.drf % 16 == 0);
+  return vec ? launch_t<T, true, MODE>(a, C, st) : launch_t<T, false, MODE>(a, C, st);
+}
+
+template <typename T>
+cudaError_t launch_d(const SamplerArgs &a, int mode, int C, cudaStream_t st) {
+  switch (mode) {
+    case kStochastic: return launch_m<T, kStochastic>(a, C, st);
+    case kGreedy: return launch_m<T, kGreedy>(a, C, st);
+    default: return launch_m<T, kTree>(a, C, st);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sampler(const SamplerArgs &a0, int dtype, int mode, cudaStream_t st) {
+  SamplerArgs a = a0;
+  if (a.batch == 0) return cudaSuccess;
+  const int C = pick_cluster(a.batch, a.vocab);
+  a.chunk = ((a.vocab + C - 1) / C + 7) / 8 * 8;
+  return dtype == SV_DTYPE_BF16 ? launch_d<__nv_bfloat16>(a, mode, C, st) : launch_d<float>(a, mode, C, st);
+}
+
+bool sampler_supports(int vocab) { return vocab <= 16 * kSub * kMaxSub; }
+
+}  // namespace sv

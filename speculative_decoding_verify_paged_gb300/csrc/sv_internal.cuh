@@ -1,0 +1,118 @@
+// Internal declarations shared by the translation units of libspecverify.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// device status word: the first recorded error wins
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void record(int32_t *status, int32_t code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ bool status_set(const int32_t *status) {
+  return status != nullptr && *((volatile const int32_t *)status) != 0;
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// plain-data views of the ABI struct, passed by value to kernels
+// ---------------------------------------------------------------------------
+struct KV {
+  void *k_pool;
+  void *v_pool;
+  int32_t *block_table;
+  int32_t *seq_lens;
+  int32_t *free_list;
+  int32_t *free_top;
+  int num_blocks, block_size, max_blocks, num_kv_heads, head_dim, batch;
+  int elem_bytes;
+};
+
+inline KV make_kv(const sv_paged_kv &p) {
+  KV k;
+  k.k_pool = p.k_pool;
+  k.v_pool = p.v_pool;
+  k.block_table = p.block_table;
+  k.seq_lens = p.seq_lens;
+  k.free_list = p.free_list;
+  k.free_top = p.free_top;
+  k.num_blocks = p.num_blocks;
+  k.block_size = p.block_size;
+  k.max_blocks = p.max_blocks_per_seq;
+  k.num_kv_heads = p.num_kv_heads;
+  k.head_dim = p.head_dim;
+  k.batch = p.batch;
+  k.elem_bytes = p.dtype == SV_DTYPE_BF16 ? 2 : 4;
+  return k;
+}
+
+// Split-KV attention arguments.
+struct AttnArgs {
+  KV kv;
+  const void *q;
+  void *out;
+  const int32_t *cu_q;
+  const uint64_t *tree_mask;
+  float *ws_o;    // [max_splits, total_q, num_q_heads, head_dim]
+  float *ws_lse;  // [max_splits, total_q, num_q_heads]
+  int32_t *status;
+  int num_q_heads, total_q, max_q, max_seq_len, chunk, max_splits;
+  int mask_kind;
+  float scale_log2;  // scale * log2(e)
+};
+
+// How the key range of every sequence is split across CTAs.
+struct SplitPlan {
+  int chunk;       // tokens per split, a multiple of `granule`
+  int max_splits;  // ceil(max_seq_len / chunk)
+};
+SplitPlan plan_splits(int batch, int num_kv_heads, int max_seq_len, int granule);
+
+// kernels' host-side launchers (return a cudaError_t from the launch)
+cudaError_t launch_kv_append(const KV &kv, const void *new_k, const void *new_v, const int32_t *cu_q,
+                             int total_q, int32_t *status, cudaStream_t st);
+cudaError_t launch_kv_rollback(const KV &kv, const int32_t *cu_q, const int32_t *accept, const int32_t *path,
+                               int max_q, int32_t *status, cudaStream_t st);
+cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t st);
+cudaError_t launch_attn_combine(const AttnArgs &a, int dtype, cudaStream_t st);
+bool attn_tc_supported(const KV &kv, int num_q_heads, int max_q);
+cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
+
+struct SamplerArgs {
+  const void *tgt;
+  const void *drf;
+  const int32_t *cu_q;
+  const int32_t *draft_tok;  // chain drafts, or tree node tokens
+  const float *u_acc;
+  const float *u_res;
+  const int32_t *parent;
+  int32_t *accept;
+  int32_t *out_tok;
+  int32_t *num_out;
+  int32_t *path;
+  int32_t *status;
+  int vocab, batch, max_q, chunk, total_q;
+  float coef;  // log2(e) / temperature
+};
+enum SamplerMode { kStochastic = 0, kGreedy = 1, kTree = 2 };
+cudaError_t launch_sampler(const SamplerArgs &a, int dtype, int mode, cudaStream_t st);
+int num_sms();
+
+}  // namespace sv

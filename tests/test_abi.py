@@ -1,0 +1,77 @@
+"""The C-ABI library builds, loads and exports every symbol include/*.h
+declares; host-side argument checks answer without touching a GPU; the oracle
+and the library share no code."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+from speculative_decoding_verify_paged_gb300 import _lib as L
+from speculative_decoding_verify_paged_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \t\*]*?\b(sv_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("sv_kv_append", "sv_spec_verify_attn", "sv_kv_rollback", "sv_spec_rejection_sample"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\b(sv_\w+)$", out, flags=re.M))
+    assert exported == _declared() | set(L.EXPORTS)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.sv_version() >= 10000
+    for code, name in L.STATUS_NAMES.items():
+        assert L.status_string(code).startswith(name)
+
+
+def test_host_validation_without_gpu(lib):
+    s = L.sv_paged_kv()
+    # NULL cache, bad block size, missing status word: rejected on the host
+    assert lib.sv_kv_append(None, None, None, None, 0, None, None) == 1
+    s.block_size, s.head_dim, s.num_kv_heads, s.num_blocks, s.max_blocks_per_seq = 3, 128, 8, 16, 4
+    assert lib.sv_kv_rollback(ctypes.byref(s), None, None, None, 6, None, None) == 1
+    assert lib.sv_spec_rejection_sample(None, None, 7, 100, 1, None, 2, 2, None, None, None, 1.0,
+                                        None, None, None, None, None) == 1
+    assert lib.sv_spec_rejection_sample(None, None, 0, 100, 1, None, 2, 2, None, None, None, float("nan"),
+                                        None, None, None, None, None) == 1
+
+
+def test_oracle_and_library_share_no_code():
+    pkg = os.path.join(ROOT, "speculative_decoding_verify_paged_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h")):
+            text = open(path).read()
+            assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), path
+            assert "spec_oracle" not in text, path
+    for path in glob.glob(os.path.join(ROOT, "oracle", "*")):
+        if path.endswith((".py", ".c", ".h")):
+            text = open(path).read()
+            assert "speculative_decoding_verify_paged_gb300" not in text, path
+            assert "spec_verify.h" not in text, path

@@ -1,0 +1,145 @@
+"""GPU parity of sv_spec_verify_attn against the fp64 oracle.
+
+Bar: max-abs error <= 1e-2 * max|out| for bf16 KV with fp32 accumulation
+(the stated tolerance), 1e-4 for fp32 KV. Small cases are compared in full
+(several key tiles, several splits, ragged tails, every block size); the
+full-size workloads are compared on sampled sequences in the launch
+configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verify_paged_gb300 import _lib as L
+from speculative_decoding_verify_paged_gb300 import step as S
+from speculative_decoding_verify_paged_gb300 import workloads as W
+
+from _helpers import assert_attn_close, attn_as_f64, max_seq_len, rows_of, status_of, upload
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(case, seqs=None, rel=None, slack=0):
+    kv, d, buf = upload(case)
+    okv = oracle.OracleKV(case.state)
+    assert okv.append(case.step) is None
+    S.append(kv, d, buf)
+    msl = max_seq_len(case.state, case.step, slack)
+    if slack:
+        buf = S.StepBuffers.make(kv, d, msl)
+    S.attention(kv, d, buf, msl)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    ref = oracle.paged_attention(okv.as_state(), case.step, seqs=seqs)
+    got = attn_as_f64(buf.attn_out)
+    rows = None if seqs is None else rows_of(case.step, seqs)
+    if rel is None:
+        rel = 1e-4 if case.state.dtype == "f32" else 1e-2
+    return assert_attn_close(got, ref, rows, rel)
+
+
+def test_tiny_fp32():
+    _run(W.tiny())
+
+
+SMALL = {
+    # name: (seed, ctx, n_q, hq, hkv, d, bs, dtype)
+    "bf16-g4-bs16": (11, [700, 65, 1, 300], [6, 6, 6, 6], 32, 8, 128, 16, "bf16"),
+    "bf16-g8-bs16": (12, [513, 640, 100], [5, 5, 5], 64, 8, 128, 16, "bf16"),
+    "bf16-ragged-bs128": (13, [16, 900, 255, 129, 1], [3, 9, 2, 5, 1], 32, 8, 128, 128, "bf16"),
+    "bf16-bs64": (14, [191, 64, 63], [4, 4, 4], 16, 4, 128, 64, "bf16"),
+    "bf16-bs256": (15, [700, 255], [6, 2], 16, 2, 128, 256, "bf16"),
+    "bf16-d64": (16, [333, 47], [5, 3], 8, 2, 64, 16, "bf16"),
+    "f32-d128": (17, [400, 3], [6, 4], 8, 2, 128, 32, "f32"),
+    "bf16-empty-ctx": (18, [0, 0, 5], [1, 7, 2], 8, 2, 128, 16, "bf16"),
+    "bf16-mqa": (19, [200, 90], [5, 5], 8, 1, 128, 16, "bf16"),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_cases(name):
+    seed, ctx, nq, hq, hkv, d, bs, dt = SMALL[name]
+    case = W.custom(seed, batch=len(ctx), ctx_lens=ctx, n_q=nq, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                    block_size=bs, vocab=16, dtype=dt, use_bank=False)
+    _run(case)
+
+
+def test_small_case_with_loose_length_bound():
+    """max_seq_len well above the real lengths: more (empty) splits, same answer."""
+    case = W.custom(21, batch=3, ctx_lens=[100, 10, 250], n_q=[6, 6, 6], num_q_heads=32, num_kv_heads=8,
+                    head_dim=128, block_size=16, vocab=16, use_bank=False)
+    _run(case, slack=3000)
+
+
+def test_chain_tree_mask_equals_causal():
+    case = W.custom(22, batch=2, ctx_lens=[300, 70], n_q=[6, 4], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                    block_size=16, vocab=16, use_bank=False)
+    kv, d, buf = upload(case)
+    S.append(kv, d, buf)
+    msl = max_seq_len(case.state, case.step)
+    S.attention(kv, d, buf, msl)
+    causal = buf.attn_out.clone()
+    masks = np.concatenate([np.array([(1 << (i + 1)) - 1 for i in range(int(n))], np.uint64)
+                            for n in case.step.n_q])
+    d.tree_mask = torch.from_numpy(masks.view(np.int64)).cuda()
+    d.mask_kind = L.SV_MASK_TREE
+    S.attention(kv, d, buf, msl)
+    torch.cuda.synchronize()
+    assert torch.equal(causal, buf.attn_out)
+
+
+def test_tree_small():
+    case = W.tree(batch=2, ctx=333, vocab=256)
+    _run(case)
+
+
+@pytest.mark.parametrize("name,seqs", [("llama8b", [0, 5, 17, 31]), ("llama70b", [0, 63, 127])])
+def test_full_size_sampled(name, seqs):
+    _run(W.CONFIGS[name](), seqs=seqs)
+
+
+def test_contbatch_sampled():
+    case = W.contbatch()
+    lens = case.state.seq_lens
+    seqs = sorted({int(np.argmax(lens)), int(np.argmin(lens)), 7, 128, 255})
+    _run(case, seqs=seqs)
+
+
+def test_tree_full_size_sampled():
+    _run(W.tree(), seqs=[0, 15])
+
+
+def test_bad_block_id_is_reported():
+    case = W.custom(23, batch=2, ctx_lens=[100, 40], n_q=[3, 3], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                    block_size=16, vocab=16, use_bank=False)
+    kv, d, buf = upload(case)
+    S.append(kv, d, buf)
+    torch.cuda.synchronize()
+    kv.block_table[1, 0] = case.state.num_blocks + 5
+    S.attention(kv, d, buf, max_seq_len(case.state, case.step))
+    torch.cuda.synchronize()
+    assert status_of(buf) == 6
+
+
+def test_too_long_sequence_is_reported():
+    case = W.custom(24, batch=2, ctx_lens=[100, 40], n_q=[3, 3], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                    block_size=16, vocab=16, use_bank=False)
+    kv, d, buf = upload(case)
+    S.append(kv, d, buf)
+    S.attention(kv, d, buf, 50)  # sequence 0 has 103 tokens
+    torch.cuda.synchronize()
+    assert status_of(buf) == 7
+
+
+def test_workspace_is_checked():
+    case = W.custom(25, batch=1, ctx_lens=[2000], n_q=[6], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                    block_size=16, vocab=16, use_bank=False)
+    kv, d, buf = upload(case)
+    msl = max_seq_len(case.state, case.step)
+    need = L.spec_verify_attn_workspace_bytes(kv, 32, d.total_q, d.max_q, msl)
+    assert need > 0
+    with pytest.raises(L.SVError) as e:
+        L.spec_verify_attn(kv, d.q, buf.attn_out, d.cu_q, max_q=d.max_q, max_seq_len=msl, scale=d.scale,
+                           workspace=None, status=buf.status)
+    assert e.value.code == 10

@@ -1,0 +1,174 @@
+"""GPU parity of sv_spec_rejection_sample / sv_tree_greedy_accept against the
+oracle: accept counts and emitted tokens bit-exact, except at oracle-flagged
+near-ties (|u - min(1, p/q)| < 1e-4 or a CDF crossing within 1e-4), whose
+divergences must stay below 0.01% of the verified positions. Greedy and tree
+decisions are exact (argmax, lowest index on ties)."""
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+import oracle
+from speculative_decoding_verify_paged_gb300 import _lib as L
+from speculative_decoding_verify_paged_gb300 import step as S
+from speculative_decoding_verify_paged_gb300 import workloads as W
+
+from _helpers import compare_samples, gpu_sample_result, status_of, upload
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample(case):
+    kv, d, buf = upload(case)
+    S.sample(d, buf)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    return gpu_sample_result(buf)
+
+
+def _check(case):
+    got = _sample(case)
+    if case.step.mask_kind == "tree":
+        ref = oracle.tree_greedy(case.step)
+        compare_samples(case.step, got, ref, tree=True)
+    else:
+        ref = oracle.rejection_sample(case.step)
+        compare_samples(case.step, got, ref)
+    return got, ref
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_tiny(T):
+    _check(W.tiny(temperature=T))
+
+
+@pytest.mark.parametrize("name,T", [("llama8b", 1.0), ("llama8b", 0.0), ("llama70b", 1.0)])
+def test_full_size(name, T):
+    _check(W.CONFIGS[name](temperature=T))
+
+
+def test_contbatch_first_iteration():
+    _check(W.contbatch())
+
+
+def test_tree_full_size():
+    got, ref = _check(W.tree())
+    assert ref.accept_cnt.max() >= 2  # the trees do get walked
+
+
+@pytest.mark.parametrize("V,dtype", [(5, "f32"), (4099, "bf16"), (20000, "f32"), (131072, "bf16"),
+                                     (200000, "bf16")])
+def test_vocab_sizes(V, dtype):
+    """Odd vocabularies (scalar loads), cluster of 8 and of 16, chunks of many items."""
+    case = W.custom(31, batch=6, ctx_lens=[4] * 6, n_q=[1, 2, 3, 5, 7, 9], num_q_heads=1, num_kv_heads=1,
+                    head_dim=8, block_size=16, vocab=V, dtype=dtype, target_sigma=2.0, draft_coef=0.8,
+                    draft_sigma=1.0, use_bank=V > 50000)
+    _check(case)
+    case.step.temperature = 0.0
+    _check(case)
+
+
+def test_temperature_half():
+    case = W.custom(32, batch=16, ctx_lens=[4] * 16, n_q=[6] * 16, num_q_heads=1, num_kv_heads=1, head_dim=8,
+                    block_size=16, vocab=32000, temperature=0.5, use_bank=True)
+    _check(case)
+
+
+def test_greedy_ties_take_lowest_index():
+    V, B = 4096, 8
+    rng = np.random.default_rng(33)
+    tgt = np.zeros((B * 3, V), np.float32)
+    for r in range(B * 3):
+        pos = rng.choice(V, size=5, replace=False)
+        tgt[r, pos] = 7.0  # five-way tie at the maximum
+    case = W.custom(34, batch=B, ctx_lens=[1] * B, n_q=[3] * B, num_q_heads=1, num_kv_heads=1, head_dim=8,
+                    block_size=16, vocab=V, dtype="bf16", temperature=0.0, use_bank=False)
+    case.step.target_logits = W.to_bf16_bits(tgt)
+    am = np.argmax(tgt, axis=1).reshape(B, 3)
+    case.step.draft_tokens = am[:, :2].reshape(-1).astype(np.int32)
+    acc, tok, num = _sample(case)
+    assert (acc == 2).all()
+    np.testing.assert_array_equal(tok[:, 2], am[:, 2])
+
+
+def _chi2_ok(samples, p, min_p=1e-3):
+    obs = np.bincount(samples, minlength=p.shape[0]).astype(np.float64)
+    exp = p * samples.shape[0]
+    assert obs[exp == 0].sum() == 0
+    keep = exp > 0
+    return stats.chisquare(obs[keep], exp[keep]).pvalue > min_p
+
+
+@pytest.mark.parametrize("V", [4, 8, 16])
+def test_lossless_chi_square_on_gpu(V):
+    """Many sequences that share p and q: the first emitted token follows p,
+    the second (when emitted) follows p_2."""
+    rng = np.random.default_rng(200 + V)
+    K, trials = 3, 400_000
+    tgt_rows = (rng.standard_normal((K + 1, V)) * 1.5).astype(np.float32)
+    drf_rows = (0.6 * tgt_rows[:K] + rng.standard_normal((K, V))).astype(np.float32)
+    n_q = np.full(trials, K + 1, np.int32)
+    cu = np.concatenate([[0], np.cumsum(n_q)]).astype(np.int32)
+
+    def softmax(l):
+        w = np.exp(l.astype(np.float64) - l.max())
+        return w / w.sum()
+
+    qs = [softmax(drf_rows[i]) for i in range(K)]
+    x = np.stack([rng.choice(V, size=trials, p=qs[i]) for i in range(K)], 1).reshape(-1).astype(np.int32)
+    dev = "cuda"
+    tgt = torch.from_numpy(np.tile(tgt_rows, (trials, 1))).to(dev)
+    drf = torch.from_numpy(np.tile(drf_rows, (trials, 1))).to(dev)
+    ua = torch.from_numpy(rng.random(trials * K, dtype=np.float32)).to(dev)
+    ur = torch.from_numpy(rng.random(trials, dtype=np.float32)).to(dev)
+    acc = torch.empty(trials, dtype=torch.int32, device=dev)
+    tok = torch.empty((trials, K + 1), dtype=torch.int32, device=dev)
+    num = torch.empty(trials, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # the sampler takes at most 65535 sequences per call
+    for s in range(0, trials, 50_000):
+        e = min(trials, s + 50_000)
+        cu_s = torch.from_numpy((cu[s:e + 1] - cu[s]).astype(np.int32)).to(dev)
+        L.spec_rejection_sample(tgt[cu[s]:cu[e]], drf[s * K:e * K], cu_s, torch.from_numpy(x[s * K:e * K]).to(dev),
+                                ua[s * K:e * K], ur[s:e], 1.0, acc[s:e], tok[s:e], num[s:e], status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    tok = tok.cpu().numpy()
+    acc = acc.cpu().numpy()
+    assert _chi2_ok(tok[:, 0], softmax(tgt_rows[0]))
+    assert _chi2_ok(tok[acc >= 1, 1], softmax(tgt_rows[1]))
+
+
+def test_nan_logits_are_reported():
+    case = W.custom(35, batch=3, ctx_lens=[4] * 3, n_q=[4] * 3, num_q_heads=1, num_kv_heads=1, head_dim=8,
+                    block_size=16, vocab=1024, dtype="f32", use_bank=False)
+    case.step.target_logits = case.step.target_logits.copy()
+    case.step.target_logits[5, 17] = np.nan
+    kv, d, buf = upload(case)
+    S.sample(d, buf)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 9
+
+
+def test_bad_draft_token_is_reported():
+    case = W.custom(36, batch=2, ctx_lens=[4] * 2, n_q=[4] * 2, num_q_heads=1, num_kv_heads=1, head_dim=8,
+                    block_size=16, vocab=1024, dtype="f32", use_bank=False)
+    case.step.draft_tokens = case.step.draft_tokens.copy()
+    case.step.draft_tokens[2] = 5000
+    kv, d, buf = upload(case)
+    S.sample(d, buf)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 8
+
+
+def test_host_argument_errors():
+    case = W.tiny()
+    kv, d, buf = upload(case)
+    with pytest.raises(L.SVError) as e:
+        L.spec_rejection_sample(d.target_logits, d.draft_logits, d.cu_q, d.draft_tokens, d.u_accept, d.u_resample,
+                                -1.0, buf.accept, buf.out_tok, buf.num_out)
+    assert e.value.code == 1
+    with pytest.raises(L.SVError) as e:
+        L.spec_rejection_sample(d.target_logits, None, d.cu_q, d.draft_tokens, d.u_accept, d.u_resample,
+                                1.0, buf.accept, buf.out_tok, buf.num_out)
+    assert e.value.code == 1

@@ -1,0 +1,77 @@
+"""The whole verify step through the C ABI, iterated: the continuous-batching
+workload (256 sequences, lognormal contexts, K_b ~ U{2..8} redrawn every
+iteration, 128-token blocks from a fragmented free list) runs 10 iterations of
+append -> attention -> rejection sample -> rollback on the GPU and in the
+oracle. Block tables, seq_lens, the free list and every emitted token must be
+bit-exact at every iteration; attention is compared on sampled sequences."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verify_paged_gb300 import step as S
+from speculative_decoding_verify_paged_gb300 import workloads as W
+
+from _helpers import (assert_attn_close, assert_kv_equal, attn_as_f64, compare_samples, gpu_sample_result,
+                      rows_of, status_of)
+
+pytestmark = pytest.mark.gpu
+
+
+def _loop(case, iterations, steps_of, attn_check_iters, attn_seqs, with_pools):
+    st = case.state
+    kv = S.device_kv(st)
+    okv = oracle.OracleKV(st, with_pools=with_pools)
+    msl = int(st.seq_lens.max()) + 9 * iterations + 16
+    accepted = []
+    for it in range(iterations):
+        step = steps_of(it)
+        d = S.DeviceStep.from_host(step)
+        buf = S.StepBuffers.make(kv, d, msl)
+        S.append(kv, d, buf)
+        S.attention(kv, d, buf, msl)
+        S.sample(d, buf)
+        assert okv.append(step) is None
+        if it in attn_check_iters:
+            torch.cuda.synchronize()
+            ref = oracle.paged_attention(okv.as_state(), step, seqs=attn_seqs)
+            assert_attn_close(attn_as_f64(buf.attn_out), ref, rows_of(step, attn_seqs))
+        ref = oracle.rejection_sample(step)
+        got = gpu_sample_result(buf)
+        diverged = compare_samples(step, got, ref)
+        assert diverged == 0, "a near-tie diverged: later iterations are not comparable"
+        S.rollback(kv, d, buf)
+        okv.rollback(step, ref.accept_cnt)
+        torch.cuda.synchronize()
+        assert status_of(buf) == 0
+        assert_kv_equal(kv, okv, pools=False)
+        accepted.append(ref.accept_cnt)
+    return kv, okv, accepted
+
+
+def test_contbatch_ten_iterations():
+    case = W.contbatch()
+    sig = case.meta["sigma_b"]
+    steps = lambda it: case.step if it == 0 else W.contbatch_step(case.seed, it, batch=case.state.batch,
+                                                                   vocab=case.step.vocab, sigma_b=sig)
+    lens = case.state.seq_lens
+    seqs = sorted({int(np.argmax(lens)), 3, 200})
+    kv, okv, accepted = _loop(case, W.CONTBATCH_ITERS, steps, {0, W.CONTBATCH_ITERS - 1}, seqs, with_pools=True)
+    # acceptance spreads with the per-sequence draft noise
+    rate = np.mean(np.stack(accepted), axis=0)
+    assert rate[sig < 1.0].mean() > rate[sig > 2.5].mean()
+
+
+def test_llama8b_three_steps_with_pools():
+    """Pools bit-exact after three full steps (only the rows the steps wrote can differ)."""
+    case = W.llama8b(batch=6, ctx_range=(100, 900), vocab=4096)
+    kv, okv, _ = _loop(case, 3, lambda it: case.step if it == 0 else W.make_chain_step(
+        case.seed, case.step.n_q, num_q_heads=32, num_kv_heads=8, head_dim=128, qkv_dtype="bf16", vocab=4096,
+        logits_dtype="bf16", target_sigma=3.0, draft_coef=0.8, draft_sigma=1.5, temperature=1.0, stream=it),
+        {2}, [0, 5], with_pools=True)
+    kp, vp = S.to_bits(kv.k_pool), S.to_bits(kv.v_pool)
+    for b in range(case.state.batch):
+        for pos in range(okv.seq_lens[b]):
+            blk = okv.bt[b][pos // okv.bs]
+            np.testing.assert_array_equal(kp[blk, :, pos % okv.bs], okv.k_pool[blk, :, pos % okv.bs])
+            np.testing.assert_array_equal(vp[blk, :, pos % okv.bs], okv.v_pool[blk, :, pos % okv.bs])
