@@ -300,6 +300,7 @@ def run_native(args):
     seqs_total = B * args.steps * world
     value = seqs_total / (elapsed_ms / 1e3)
 
+    paths = attn_path_times(kv, d, buf, msl, stream)
     e2e = None if args.no_e2e else run_e2e(args, kv, d, buf, msl, sp, dev, stream, world)
     hbm_peak, peak_kind = peaks()
     achieved = attn_bytes_avg / (attn_ms_avg / 1e3) / 1e9
@@ -326,6 +327,7 @@ def run_native(args):
                              "unit": "GB/s", "frac": sampler_bytes(sp) / (samp_ms_avg / 1e3) / 1e9 / hbm_peak,
                              "algorithmic_bytes_per_launch": sampler_bytes(sp), "avg_launch_ms": samp_ms_avg},
         "hbm_gbs_step": (attn_bytes_avg + sampler_bytes(sp)) / (elapsed_ms / args.steps / 1e3) / 1e9,
+        "attn_paths_ms": paths,
         "gpu_launches": S.launches_per_step(d, msl, kv) * args.steps,
         "clocks": clk,
     }
@@ -342,6 +344,36 @@ def run_native(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
+
+
+def attn_path_times(kv, d, buf, msl, stream, reps=10):
+    """The attention call alone, timed with each implementation on the same cache
+    state (the step's rows appended once, rolled back after)."""
+    import torch
+    from speculative_decoding_verify_paged_gb300 import _lib as L
+    from speculative_decoding_verify_paged_gb300 import step as S
+    out = {}
+    S.append(kv, d, buf, stream)
+    for path in ("tensor_cores", "cuda_cores"):
+        try:
+            L.set_attn_path(path)
+            for _ in range(2):
+                S.attention(kv, d, buf, msl, stream)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                S.attention(kv, d, buf, msl, stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            out[path] = a.elapsed_time(b) / reps
+        except L.SVError:
+            out[path] = None
+        finally:
+            L.set_attn_path("auto")
+    S.sample(d, buf, stream)
+    S.rollback(kv, d, buf, stream)
+    torch.cuda.synchronize()
+    return out
 
 
 def run_e2e(args, kv, d, buf, msl, sp, dev, stream, world):

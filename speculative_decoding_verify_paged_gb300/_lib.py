@@ -30,7 +30,9 @@ STATUS_NAMES = {
 
 EXPORTS = ("sv_kv_append", "sv_spec_verify_attn_workspace_bytes", "sv_spec_verify_attn",
            "sv_spec_rejection_sample", "sv_tree_greedy_accept", "sv_kv_rollback", "sv_status_string",
-           "sv_version")
+           "sv_version", "sv_set_option")
+SV_OPT_ATTN_PATH = 1
+ATTN_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
 
 
 class SVError(RuntimeError):
@@ -78,6 +80,7 @@ def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CD
             "sv_kv_rollback": (I, [KVP, P, P, P, I, P, P]),
             "sv_status_string": (ctypes.c_char_p, [I]),
             "sv_version": (I, []),
+            "sv_set_option": (I, [I, I]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -86,6 +89,11 @@ def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CD
         if path is None:
             _lib = lib
         return lib
+
+
+def set_attn_path(path: str) -> None:
+    """Select the attention implementation: "auto", "cuda_cores" or "tensor_cores"."""
+    _check(load().sv_set_option(SV_OPT_ATTN_PATH, ATTN_PATHS[path]), "sv_set_option")
 
 
 def status_string(code: int) -> str:

@@ -20,10 +20,16 @@
 //   phase 2  cluster barrier; every CTA combines the C partial results of
 //            every row through distributed shared memory in rank order, so all
 //            CTAs hold identical row statistics and take identical decisions.
-//   phase 3  (T > 0) every CTA computes the weights w_v (residual or p) over
-//            its chunk and their sum; after a cluster barrier the prefix over
-//            ranks tells which CTA holds the crossing u' * S; that CTA rescans
-//            its chunk (block-wide prefix sums, same order) and finds y.
+//   phase 3  (T > 0) the row pair of the draw (target and draft row a, or the
+//            bonus row) is re-read. With a 128K vocabulary the residual CDF
+//            has intervals of ~1e-5, so this phase is exact where fp32 would
+//            not be: exponents carry log2(e)/T as a hi+lo pair, the weights
+//            are summed in 64-bit fixed point (2^-40 units, order-free and
+//            exact), the draft normaliser enters as the ratio Z_t/Z_d in
+//            hi+lo form, and the target is the integer floor(u' * S). Pass A
+//            sums the two normalisers, pass B each CTA's residual mass, and
+//            after a cluster barrier the prefix over ranks picks the CTA
+//            holding the crossing, which rescans its chunk (pass C).
 // All reductions run in a fixed order, so results are deterministic.
 #include <cooperative_groups.h>
 
@@ -86,15 +92,16 @@ __device__ __forceinline__ void load_item(const T *__restrict__ row, int e0, int
   }
 }
 
-// (max, sum) pair combine in the exp2 domain; m == -inf means "empty".
-__device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2) {
+// (max, sum) pair combine: m is a raw logit maximum, s = sum 2^((l - m) * coef);
+// m == -inf means "empty".
+__device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2, float coef) {
   const float mn = fmaxf(m, m2);
   if (mn == -INFINITY) {
     m = mn;
     s = 0.f;
     return;
   }
-  s = s * exp2f(m - mn) + s2 * exp2f(m2 - mn);
+  s = s * exp2f((m - mn) * coef) + s2 * exp2f((m2 - mn) * coef);
   m = mn;
 }
 
@@ -107,33 +114,51 @@ __device__ __forceinline__ void am_combine(float &v, int &i, float v2, int i2) {
   }
 }
 
-// Block-wide exclusive scan of one float per thread (fixed order).
-__device__ float block_excl_scan_f(float x, float *warp_buf /*[kWarps]*/, float *total) {
+// 2^(d * c) for d <= 0 with c = c_hi + c_lo: the product is carried to about
+// 2^-40 before exp2f, so no rounding of c or of d*c shifts all weights alike.
+__device__ __forceinline__ float exp2_acc(float d, float c_hi, float c_lo) {
+  const float xh = d * c_hi;
+  if (!(xh > -160.f)) return 0.f;  // -inf logits and underflow
+  const float xe = fmaf(d, c_hi, -xh) + d * c_lo;
+  return exp2f(xh) * fmaf(xe, 0.69314718055994531f, 1.0f);
+}
+
+// Weights in [0, 1] as 64-bit fixed point with 40 fractional bits: sums of up
+// to 2^23 of them are exact and independent of the order of addition.
+__device__ __forceinline__ long long to_fix(float w) { return __float2ll_rn(w * 1099511627776.0f); }
+
+__device__ long long block_sum_ll(long long x, long long *buf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float inc = x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  if (lane == 0) buf[warp] = x;
+  __syncthreads();
+  long long t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += buf[w];
+  __syncthreads();
+  return t;
+}
+
+__device__ long long block_excl_scan_ll(long long x, long long *buf, long long *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long inc = x;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, inc, o);
+    const long long y = __shfl_up_sync(0xffffffffu, inc, o);
     if (lane >= o) inc += y;
   }
-  if (lane == 31) warp_buf[warp] = inc;
+  if (lane == 31) buf[warp] = inc;
   __syncthreads();
-  if (warp == 0) {
-    float w = lane < kWarps ? warp_buf[lane] : 0.f;
+  long long before = 0, tot = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < kWarps) warp_buf[lane] = w;
+  for (int w = 0; w < kWarps; ++w) {
+    before += (w < warp) ? buf[w] : 0;
+    tot += buf[w];
   }
   __syncthreads();
-  const float excl_in_warp = __shfl_up_sync(0xffffffffu, inc, 1);
-  float excl = (lane == 0 ? 0.f : excl_in_warp);
-  if (warp > 0) excl = warp_buf[warp - 1] + excl;
-  *total = warp_buf[kWarps - 1];
-  __syncthreads();
-  return excl;
+  *total = tot;
+  return before + inc - x;
 }
 
 struct Smem {
@@ -148,14 +173,15 @@ struct Smem {
   float Z[kMaxRows];
   int am[kMaxRows];
   float gtl[kMaxQ], gdl[kMaxQ];
-  float S[2];  // phase 3: this CTA's weight sum per pass (cluster-visible)
-  float warp_buf[kWarps];
-  float seg_total;
+  long long zt, zd;     // phase 3: this CTA's fixed-point normalisers (cluster-visible)
+  long long S[2];       // phase 3: this CTA's fixed-point weight sum per pass (cluster-visible)
+  long long ll_buf[kWarps];
+  long long P_owner, target;
+  float rho_hi, rho_lo;
   int a;
   int bad;
   int y_min, y_last;
-  int owner, no_cross, fallback;
-  float P_owner, target;
+  int owner, fallback;
 };
 
 template <typename T, bool VEC, int MODE>
@@ -200,24 +226,24 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
     int idx[32];
     load_item<T, VEC>(row, e0, e1, lane, v, idx);
     if constexpr (MODE == kStochastic) {
-      float m = -INFINITY;
+      float m = -INFINITY;  // raw logit maximum (exact)
 #pragma unroll
       for (int k = 0; k < 32; ++k)
         if (idx[k] >= 0) {
           bad |= (v[k] != v[k]) | (v[k] == INFINITY);
-          m = fmaxf(m, v[k] * coef);
+          m = fmaxf(m, v[k]);
         }
       float sum = 0.f;
       if (m != -INFINITY) {
 #pragma unroll
         for (int k = 0; k < 32; ++k)
-          if (idx[k] >= 0) sum += exp2f(fmaf(v[k], coef, -m));
+          if (idx[k] >= 0) sum += exp2f((v[k] - m) * coef);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
         const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-        ms_combine(m, sum, m2, s2);
+        ms_combine(m, sum, m2, s2, coef);
       }
       if (lane == 0) {
         sm.pm[r][s] = m;
@@ -261,7 +287,7 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
   if (tid < rows) {
     if constexpr (MODE == kStochastic) {
       float m = -INFINITY, s = 0.f;
-      for (int k = 0; k < nsub; ++k) ms_combine(m, s, sm.pm[tid][k], sm.ps[tid][k]);
+      for (int k = 0; k < nsub; ++k) ms_combine(m, s, sm.pm[tid][k], sm.ps[tid][k], coef);
       sm.rm[tid] = m;
       sm.rs[tid] = s;
     } else {
@@ -282,7 +308,7 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
       for (int q = 0; q < C; ++q) {
         const float m2 = *cluster.map_shared_rank(&sm.rm[tid], q);
         const float s2 = *cluster.map_shared_rank(&sm.rs[tid], q);
-        ms_combine(m, s, m2, s2);
+        ms_combine(m, s, m2, s2, coef);
       }
       sm.M[tid] = m;
       sm.Z[tid] = s;
@@ -358,8 +384,8 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
       int a = K;
       for (int i = 0; i < K; ++i) {
         const float Zt = sm.Z[i], Zd = sm.Z[n + i];
-        const float p = exp2f(fmaf(sm.gtl[i], coef, -sm.M[i])) / Zt;
-        const float q = exp2f(fmaf(sm.gdl[i], coef, -sm.M[n + i])) / Zd;
+        const float p = exp2f((sm.gtl[i] - sm.M[i]) * coef) / Zt;
+        const float q = exp2f((sm.gdl[i] - sm.M[n + i]) * coef) / Zd;
         const float thr = q > 0.f ? fminf(1.f, p / q) : 1.f;
         if (!(args.u_acc[d0 + i] < thr)) {
           a = i;
@@ -373,89 +399,111 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
     }
     __syncthreads();
     const int a = sm.a;
+    const bool resid = a < K;
     const T *trow = tgt + (size_t)(t0 + a) * V;
-    const T *drow = (a < K) ? drf + (size_t)(d0 + a) * V : nullptr;
-    const float Mt = sm.M[a], invZt = 1.f / sm.Z[a];
-    const float Md = (a < K) ? sm.M[n + a] : 0.f, invZd = (a < K) ? 1.f / sm.Z[n + a] : 0.f;
+    const T *drow = resid ? drf + (size_t)(d0 + a) * V : nullptr;
+    const float Mt = sm.M[a], Md = resid ? sm.M[n + a] : 0.f;
+    const float chi = args.coef, clo = args.coef_lo;
     const float ur = args.u_res[b];
 
-    for (int pass = 0; pass < 2; ++pass) {
-      const bool resid = (a < K) && pass == 0;
-      auto weight = [&](int e) -> float {
-        const float p = exp2f(fmaf(to_f32(trow[e]), coef, -Mt)) * invZt;
-        if (!resid) return p;
-        const float q = exp2f(fmaf(to_f32(drow[e]), coef, -Md)) * invZd;
-        return fmaxf(p - q, 0.f);
-      };
-      // this CTA's weight sum, by segments of kSeg elements (fixed order)
-      float carry = 0.f;
-      for (int s0 = lo; s0 < hi; s0 += kSeg) {
-        float local = 0.f;
-        const int e = s0 + tid * kSegPer;
-#pragma unroll
-        for (int k = 0; k < kSegPer; ++k)
-          if (e + k < hi) local += weight(e + k);
-        float seg_total;
-        block_excl_scan_f(local, sm.warp_buf, &seg_total);
-        carry = carry + seg_total;
+    // ---- pass A: fixed-point normalisers of the row pair (residual draws) ----
+    if (resid) {
+      long long zt = 0, zd = 0;
+      for (int e = lo + tid; e < hi; e += kThreads) {
+        zt += to_fix(exp2_acc(to_f32(trow[e]) - Mt, chi, clo));
+        zd += to_fix(exp2_acc(to_f32(drow[e]) - Md, chi, clo));
       }
-      if (tid == 0) sm.S[pass] = carry;
+      zt = block_sum_ll(zt, sm.ll_buf);
+      zd = block_sum_ll(zd, sm.ll_buf);
+      if (tid == 0) {
+        sm.zt = zt;
+        sm.zd = zd;
+      }
+    }
+    cluster.sync();
+    if (resid && tid == 0) {
+      long long Zt = 0, Zd = 0;
+      for (int q = 0; q < C; ++q) {
+        Zt += *cluster.map_shared_rank(&sm.zt, q);
+        Zd += *cluster.map_shared_rank(&sm.zd, q);
+      }
+      // q_v enters as e_d * (Z_t / Z_d), carried as hi + lo
+      const double rho = Zd > 0 ? (double)Zt / (double)Zd : 0.0;
+      sm.rho_hi = (float)rho;
+      sm.rho_lo = (float)(rho - (double)sm.rho_hi);
+    }
+    __syncthreads();
+    const float rho_hi = sm.rho_hi, rho_lo = sm.rho_lo;
+
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool res_pass = resid && pass == 0;
+      // w_v proportional to max(0, p_v - q_v) (or to p_v), scaled by Z_t, in [0, 1]
+      auto weight = [&](int e) -> float {
+        const float et = exp2_acc(to_f32(trow[e]) - Mt, chi, clo);
+        if (!res_pass) return et;
+        const float ed = exp2_acc(to_f32(drow[e]) - Md, chi, clo);
+        return fmaxf(et - fmaf(ed, rho_hi, ed * rho_lo), 0.f);
+      };
+      // ---- pass B: this CTA's fixed-point mass ----
+      long long mass = 0;
+      for (int e = lo + tid; e < hi; e += kThreads) mass += to_fix(weight(e));
+      mass = block_sum_ll(mass, sm.ll_buf);
+      if (tid == 0) sm.S[pass] = mass;
       cluster.sync();
       if (tid == 0) {
-        float S = 0.f;
-        for (int q = 0; q < C; ++q) S = S + *cluster.map_shared_rank(&sm.S[pass], q);
-        const float target = ur * S;
-        float cum = 0.f;
+        long long S = 0;
+        for (int q = 0; q < C; ++q) S += *cluster.map_shared_rank(&sm.S[pass], q);
+        // the draw: the smallest v whose inclusive prefix exceeds u' * S
+        const long long target = (long long)floor((double)ur * (double)S);
+        long long cum = 0, P = 0;
         int owner = -1, last_pos = -1;
-        float P = 0.f;
         for (int q = 0; q < C; ++q) {
-          const float Sq = *cluster.map_shared_rank(&sm.S[pass], q);
-          const float prev = cum;
-          cum = cum + Sq;
-          if (Sq > 0.f) last_pos = q;
-          if (owner < 0 && cum > target) {
+          const long long Sq = *cluster.map_shared_rank(&sm.S[pass], q);
+          if (Sq > 0) last_pos = q;
+          if (owner < 0 && cum + Sq > target) {
             owner = q;
-            P = prev;
+            P = cum;
           }
+          cum += Sq;
         }
-        sm.no_cross = 0;
-        if (owner < 0) {
+        sm.fallback = (res_pass && S == 0) ? 1 : 0;
+        sm.y_min = INT_MAX;
+        sm.y_last = -1;
+        if (owner < 0) {  // u' outside [0, 1): the last token with mass
           owner = last_pos;
-          sm.no_cross = 1;
+          P = -1;
         }
         sm.owner = owner;
         sm.P_owner = P;
         sm.target = target;
-        sm.fallback = (resid && !(S > 0.f)) ? 1 : 0;
-        sm.y_min = INT_MAX;
-        sm.y_last = -1;
       }
       __syncthreads();
       if (sm.fallback) continue;  // residual without mass: draw from p_a instead
       if (rank == sm.owner) {
-        const float P = sm.P_owner, target = sm.target;
-        float carry2 = 0.f;
+        // ---- pass C: exact prefix sums over this chunk, segment by segment ----
+        const long long P = sm.P_owner, target = sm.target;
+        long long carry = 0;
         for (int s0 = lo; s0 < hi; s0 += kSeg) {
-          float w[kSegPer];
-          float local = 0.f;
+          long long w[kSegPer];
+          long long local = 0;
           const int e = s0 + tid * kSegPer;
 #pragma unroll
           for (int k = 0; k < kSegPer; ++k) {
-            w[k] = (e + k < hi) ? weight(e + k) : 0.f;
+            w[k] = (e + k < hi) ? to_fix(weight(e + k)) : 0;
             local += w[k];
           }
-          float seg_total;
-          const float excl = block_excl_scan_f(local, sm.warp_buf, &seg_total);
-          float inc = 0.f;
+          long long seg_total;
+          const long long excl = block_excl_scan_ll(local, sm.ll_buf, &seg_total);
+          long long inc = P + carry + excl;
 #pragma unroll
           for (int k = 0; k < kSegPer; ++k) {
             inc += w[k];
-            if (w[k] > 0.f) {
-              if (!sm.no_cross && P + (carry2 + (excl + inc)) > target) atomicMin(&sm.y_min, e + k);
+            if (w[k] > 0) {
+              if (P >= 0 && inc > target) atomicMin(&sm.y_min, e + k);
               atomicMax(&sm.y_last, e + k);
             }
           }
-          carry2 = carry2 + seg_total;
+          carry += seg_total;
         }
         __syncthreads();
         if (tid == 0) {

@@ -54,6 +54,7 @@ namespace {
 
 constexpr int kMaxQ = 64;
 constexpr int kGranule = 64;
+int g_attn_path = SV_ATTN_AUTO;
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -103,6 +104,14 @@ const char *sv_status_string(int32_t status) {
 }
 
 int32_t sv_version(void) { return 10000; }
+
+sv_status sv_set_option(int32_t option, int32_t value) {
+  if (option == SV_OPT_ATTN_PATH && value >= SV_ATTN_AUTO && value <= SV_ATTN_TENSOR_CORES) {
+    g_attn_path = value;
+    return SV_OK;
+  }
+  return SV_ERR_INVALID_ARG;
+}
 
 sv_status sv_kv_append(const sv_paged_kv *kv, const void *new_k, const void *new_v, const int32_t *cu_q,
                        int32_t total_q, int32_t *status_dev, void *stream) {
@@ -161,9 +170,10 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
   a.mask_kind = mask_kind;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e;
-  if (kv->dtype == SV_DTYPE_BF16 && attn_tc_supported(a.kv, num_q_heads, max_q_per_seq)) e = launch_attn_tc(a, st);
-  else e = launch_attn_simt(a, kv->dtype, st);
+  const bool tc_ok = kv->dtype == SV_DTYPE_BF16 && attn_tc_supported(a.kv, num_q_heads, max_q_per_seq);
+  if (g_attn_path == SV_ATTN_TENSOR_CORES && !tc_ok) return SV_ERR_UNSUPPORTED;
+  const bool use_tc = tc_ok && g_attn_path != SV_ATTN_CUDA_CORES;
+  cudaError_t e = use_tc ? launch_attn_tc(a, st) : launch_attn_simt(a, kv->dtype, st);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   return cuda_status(launch_attn_combine(a, kv->dtype, st));
 }
@@ -202,7 +212,11 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
   a.batch = batch;
   a.max_q = max_q_per_seq;
   a.total_q = total_q;
-  a.coef = greedy ? 0.f : 1.4426950408889634f / temperature;
+  if (!greedy) {
+    const double c = 1.4426950408889634 / (double)temperature;
+    a.coef = (float)c;
+    a.coef_lo = (float)(c - (double)a.coef);
+  }
   return cuda_status(launch_sampler(a, logits_dtype, greedy ? kGreedy : kStochastic, (cudaStream_t)stream));
 }
 

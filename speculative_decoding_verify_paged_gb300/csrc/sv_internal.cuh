@@ -109,7 +109,8 @@ struct SamplerArgs {
   int32_t *path;
   int32_t *status;
   int vocab, batch, max_q, chunk, total_q;
-  float coef;  // log2(e) / temperature
+  float coef;     // log2(e) / temperature, rounded to fp32
+  float coef_lo;  // log2(e) / temperature - coef
 };
 enum SamplerMode { kStochastic = 0, kGreedy = 1, kTree = 2 };
 cudaError_t launch_sampler(const SamplerArgs &a, int dtype, int mode, cudaStream_t st);

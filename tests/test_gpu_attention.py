@@ -20,7 +20,15 @@ from _helpers import assert_attn_close, attn_as_f64, max_seq_len, rows_of, statu
 pytestmark = pytest.mark.gpu
 
 
-def _run(case, seqs=None, rel=None, slack=0):
+def _run(case, seqs=None, rel=None, slack=0, path="auto"):
+    L.set_attn_path(path)
+    try:
+        return _run_path(case, seqs, rel, slack)
+    finally:
+        L.set_attn_path("auto")
+
+
+def _run_path(case, seqs, rel, slack):
     kv, d, buf = upload(case)
     okv = oracle.OracleKV(case.state)
     assert okv.append(case.step) is None
@@ -57,12 +65,26 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("path", ["auto", "cuda_cores"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_small_cases(name):
+def test_small_cases(name, path):
     seed, ctx, nq, hq, hkv, d, bs, dt = SMALL[name]
     case = W.custom(seed, batch=len(ctx), ctx_lens=ctx, n_q=nq, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                     block_size=bs, vocab=16, dtype=dt, use_bank=False)
-    _run(case)
+    _run(case, path=path)
+
+
+def test_tensor_core_path_refuses_unsupported_shapes():
+    case = W.custom(26, batch=2, ctx_lens=[30, 40], n_q=[3, 3], num_q_heads=8, num_kv_heads=2, head_dim=64,
+                    block_size=16, vocab=16, use_bank=False)
+    kv, d, buf = upload(case)
+    L.set_attn_path("tensor_cores")
+    try:
+        with pytest.raises(L.SVError) as e:
+            S.attention(kv, d, buf, max_seq_len(case.state, case.step))
+        assert e.value.code == 2
+    finally:
+        L.set_attn_path("auto")
 
 
 def test_small_case_with_loose_length_bound():
@@ -89,14 +111,17 @@ def test_chain_tree_mask_equals_causal():
     assert torch.equal(causal, buf.attn_out)
 
 
-def test_tree_small():
+@pytest.mark.parametrize("path", ["auto", "cuda_cores"])
+def test_tree_small(path):
     case = W.tree(batch=2, ctx=333, vocab=256)
-    _run(case)
+    _run(case, path=path)
 
 
-@pytest.mark.parametrize("name,seqs", [("llama8b", [0, 5, 17, 31]), ("llama70b", [0, 63, 127])])
-def test_full_size_sampled(name, seqs):
-    _run(W.CONFIGS[name](), seqs=seqs)
+@pytest.mark.parametrize("name,seqs,path", [("llama8b", [0, 5, 17, 31], "auto"),
+                                            ("llama8b", [3, 30], "cuda_cores"),
+                                            ("llama70b", [0, 63, 127], "auto")])
+def test_full_size_sampled(name, seqs, path):
+    _run(W.CONFIGS[name](), seqs=seqs, path=path)
 
 
 def test_contbatch_sampled():

@@ -64,7 +64,7 @@ def test_contbatch_ten_iterations():
 
 def test_llama8b_three_steps_with_pools():
     """Pools bit-exact after three full steps (only the rows the steps wrote can differ)."""
-    case = W.llama8b(batch=6, ctx_range=(100, 900), vocab=4096)
+    case = W.llama8b(batch=6, ctx_range=(100, 900), vocab=4096, growth_tokens=24)
     kv, okv, _ = _loop(case, 3, lambda it: case.step if it == 0 else W.make_chain_step(
         case.seed, case.step.n_q, num_q_heads=32, num_kv_heads=8, head_dim=128, qkv_dtype="bf16", vocab=4096,
         logits_dtype="bf16", target_sigma=3.0, draft_coef=0.8, draft_sigma=1.5, temperature=1.0, stream=it),
