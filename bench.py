@@ -214,6 +214,20 @@ def attn_traffic_record():
     return rec if rec.get("sources_sha256") == h.hexdigest() else None
 
 
+def aggregate(elapsed_ms: float, seqs_local: int, world: int, device=None):
+    """Whole-job throughput over the ranks of the default process group: the
+    slowest rank's time, the sum of the sequences every rank verified."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    n = torch.tensor([seqs_local], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    ms = float(t.item())
+    return float(n.item()) / (ms / 1e3), ms
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
@@ -292,13 +306,8 @@ def run_native(args):
     attn_ms_avg = float(np.mean(attn_ms))
     samp_ms_avg = float(np.mean(samp_ms))
 
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
     B = st.batch
-    seqs_total = B * args.steps * world
-    value = seqs_total / (elapsed_ms / 1e3)
+    value, elapsed_ms = aggregate(elapsed_ms, B * args.steps, world, dev)
 
     paths = attn_path_times(kv, d, buf, msl, stream)
     e2e = None if args.no_e2e else run_e2e(args, kv, d, buf, msl, sp, dev, stream, world)

@@ -173,34 +173,50 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
 
   if (warp == kConsumerWarps) {
     // ================= producer: TMA K/V tiles into the ring =================
-    if (lane == 0) {
-      const int bs = kv.block_size, box = P.box_rows;
-      const uint32_t box_bytes = static_cast<uint32_t>(box) * 128;
-      const int last_block = (L - 1) / bs;
-      for (int t = 0; t < ntiles; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages && !mbar_wait(smem_u32(&empty[s]), ((t / kStages) - 1) & 1)) {
-          record(a.status, SV_ERR_TIMEOUT);
-          break;
-        }
-        const int kt = kb + t * kTile;
-        // boxes of this tile: `box` rows each, covering keys kt .. kt+63
-        int ids[kTile / 16];
-        int nbox = 0;
-        for (int r = 0; r < kTile; r += box) {
-          const int tok = kt + r;
+    // The split's physical block ids are read 32 at a time (one per lane) into
+    // registers, with the next window in flight while the current one is used;
+    // lane 0 picks ids by shuffle and issues the copies.
+    const int bs = kv.block_size, box = P.box_rows;
+    const uint32_t box_bytes = static_cast<uint32_t>(box) * 128;
+    const int lb_first = kb / bs, lb_last = (ke - 1) / bs;
+    const int32_t *bt = kv.block_table + (size_t)b * kv.max_blocks;
+    auto load_id = [&](int lb) -> int {
+      if (lb > lb_last) return -1;
+      const int id = bt[lb];
+      if (id < 0 || id >= kv.num_blocks) {
+        record(a.status, SV_ERR_BAD_BLOCK_ID);
+        return -1;
+      }
+      return id;
+    };
+    int wbase = lb_first;
+    int cur = load_id(wbase + lane);
+    int nxt = load_id(wbase + 32 + lane);
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t % kStages;
+      if (t >= kStages && !mbar_wait(smem_u32(&empty[s]), ((t / kStages) - 1) & 1)) {
+        if (lane == 0) record(a.status, SV_ERR_TIMEOUT);
+        break;
+      }
+      const int kt = kb + t * kTile;
+      int ids[kTile / 16];
+      int nbox = 0;
+      for (int r = 0; r < kTile; r += box) {
+        const int tok = kt + r;
+        int id = -1;
+        if (tok < ke) {
           const int lb = tok / bs;
-          int id = -1;
-          if (lb <= last_block && tok < ke) {
-            id = kv.block_table[(size_t)b * kv.max_blocks + lb];
-            if (id < 0 || id >= kv.num_blocks) {
-              record(a.status, SV_ERR_BAD_BLOCK_ID);
-              id = -1;
-            }
+          while (lb >= wbase + 32) {  // warp-uniform
+            wbase += 32;
+            cur = nxt;
+            nxt = load_id(wbase + 32 + lane);
           }
-          ids[r / box] = id;
-          nbox += id >= 0;
+          id = __shfl_sync(0xffffffffu, cur, lb - wbase);
         }
+        ids[r / box] = id;
+        nbox += id >= 0;
+      }
+      if (lane == 0) {
         const uint32_t fb = smem_u32(&full[s]);
         mbar_expect_tx(fb, static_cast<uint32_t>(nbox) * 4u * box_bytes);
         const uint32_t kdst = smem_u32(stages + s * kStageBytes);
@@ -217,6 +233,7 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
           tma_load_2d(vdst + kHalfBytes + off, &tmap_v, 64, y, fb);
         }
       }
+      __syncwarp();
     }
     return;
   }

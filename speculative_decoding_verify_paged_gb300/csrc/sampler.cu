@@ -14,9 +14,9 @@
 //
 // How: the vocabulary is cut into C equal chunks, one per CTA of the cluster.
 //   phase 1  every CTA streams its chunk of every row of the sequence (target
-//            rows and draft rows) once with 16-byte loads and keeps a running
-//            (max, sum of exp2) per row (argmax for greedy modes); work items
-//            are (row, 1024-element sub-chunk) pairs spread over the warps.
+//            rows and draft rows) once; a work item is 4 KB of one row for
+//            one warp (eight 16-byte loads in flight per lane), reduced to a
+//            (max, sum of 2^((l - max) log2(e)/T)) pair, or to an argmax.
 //   phase 2  cluster barrier; every CTA combines the C partial results of
 //            every row through distributed shared memory in rank order, so all
 //            CTAs hold identical row statistics and take identical decisions.
@@ -43,51 +43,46 @@ namespace cg = cooperative_groups;
 namespace sv {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxQ = 64;
 constexpr int kMaxRows = 2 * kMaxQ;  // target + draft rows of one sequence
-constexpr int kSub = 1024;           // elements per work item
-constexpr int kMaxSub = 16;          // => at most 16384 elements per CTA chunk
-constexpr int kSegPer = 8;           // phase 3: elements per thread per segment
-constexpr int kSeg = kThreads * kSegPer;
+constexpr int kMaxSub = 16;          // work items per row per CTA
+constexpr int kMaxChunk = 16384;     // vocabulary elements per CTA
+constexpr int kGroup = 8;            // phase 3: consecutive elements per thread
+constexpr int kSeg = kThreads * kGroup;
 
-template <typename T> struct VecTraits;
-template <> struct VecTraits<__nv_bfloat16> { static constexpr int N = 8; };
-template <> struct VecTraits<float> { static constexpr int N = 4; };
+// Work-item geometry: LOADS loads of N elements per lane.
+template <typename T, bool VEC> struct ItemCfg;
+template <> struct ItemCfg<__nv_bfloat16, true> { static constexpr int N = 8, LOADS = 8; };
+template <> struct ItemCfg<float, true> { static constexpr int N = 4, LOADS = 8; };
+template <typename T> struct ItemCfg<T, false> { static constexpr int N = 1, LOADS = 32; };
+template <typename T, bool VEC> __host__ __device__ constexpr int item_elems() { return 32 * ItemCfg<T, VEC>::N * ItemCfg<T, VEC>::LOADS; }
 
-// Load the 32 values a lane owns in [e0, e1) of a row (1024-element item).
-// Vector layout: vector u of the lane covers e0 + (u*32 + lane)*N .. +N.
-// Scalar layout: value k of the lane is e0 + k*32 + lane.
+template <typename T, bool VEC> struct Raw;
+template <typename T> struct Raw<T, true> { uint4 v; };
+template <typename T> struct Raw<T, false> { T v; };
+
 template <typename T, bool VEC>
-__device__ __forceinline__ void load_item(const T *__restrict__ row, int e0, int e1, int lane, float (&v)[32],
-                                          int (&idx)[32]) {
-  if constexpr (VEC) {
-    constexpr int N = VecTraits<T>::N;
-    constexpr int U = 32 / N;
-    uint4 raw[U];
+__device__ __forceinline__ float elem(const Raw<T, VEC> &r, int k) {
+  if constexpr (VEC) return to_f32(reinterpret_cast<const T *>(&r.v)[k]);
+  else return to_f32(r.v);
+}
+
+// The lane's loads of one item: load u covers e0 + (u*32 + lane)*N .. +N.
+// Chunks are multiples of N, so a load is wholly inside or outside [e0, e1).
+template <typename T, bool VEC>
+__device__ __forceinline__ void load_item(const T *__restrict__ row, int e0, int e1, int lane,
+                                          Raw<T, VEC> (&raw)[ItemCfg<T, VEC>::LOADS], int &nvalid) {
+  constexpr int N = ItemCfg<T, VEC>::N, LOADS = ItemCfg<T, VEC>::LOADS;
+  nvalid = 0;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int e = e0 + (u * 32 + lane) * N;
-      if (e < e1) raw[u] = __ldg(reinterpret_cast<const uint4 *>(row + e));
-      else raw[u] = make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int e = e0 + (u * 32 + lane) * N;
-      const T *t = reinterpret_cast<const T *>(&raw[u]);
-#pragma unroll
-      for (int k = 0; k < N; ++k) {
-        v[u * N + k] = to_f32(t[k]);
-        idx[u * N + k] = (e + k < e1) ? e + k : -1;  // chunks are multiples of N: all or none valid
-      }
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int e = e0 + k * 32 + lane;
-      v[k] = e < e1 ? to_f32(row[e]) : 0.f;
-      idx[k] = e < e1 ? e : -1;
+  for (int u = 0; u < LOADS; ++u) {
+    const int e = e0 + (u * 32 + lane) * N;
+    if (e < e1) {
+      if constexpr (VEC) raw[u].v = __ldg(reinterpret_cast<const uint4 *>(row + e));
+      else raw[u].v = row[e];
+      nvalid = u + 1;
     }
   }
 }
@@ -161,8 +156,33 @@ __device__ long long block_excl_scan_ll(long long x, long long *buf, long long *
   return before + inc - x;
 }
 
+// Eight consecutive logits e .. e+7 of a row as floats; -inf past `hi`.
+template <typename T, bool VEC>
+__device__ __forceinline__ void load8(const T *__restrict__ row, int e, int hi, float (&x)[kGroup]) {
+  if (VEC && e + kGroup <= hi) {
+    if constexpr (sizeof(T) == 2) {
+      const uint4 r = __ldg(reinterpret_cast<const uint4 *>(row + e));
+      const T *t = reinterpret_cast<const T *>(&r);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = to_f32(t[k]);
+    } else {
+      const uint4 r0 = __ldg(reinterpret_cast<const uint4 *>(row + e));
+      const uint4 r1 = __ldg(reinterpret_cast<const uint4 *>(row + e + 4));
+      const float *f0 = reinterpret_cast<const float *>(&r0), *f1 = reinterpret_cast<const float *>(&r1);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        x[k] = f0[k];
+        x[k + 4] = f1[k];
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) x[k] = (e + k < hi) ? to_f32(row[e + k]) : -INFINITY;
+  }
+}
+
 struct Smem {
-  float pm[kMaxRows][kMaxSub];  // per item: max (z domain) or best value
+  float pm[kMaxRows][kMaxSub];  // per item: raw max, or best value
   float ps[kMaxRows][kMaxSub];  // per item: sum of exp2, or best index (as int bits)
   float rm[kMaxRows];           // per row, this CTA's chunk (cluster-visible)
   float rs[kMaxRows];
@@ -173,8 +193,8 @@ struct Smem {
   float Z[kMaxRows];
   int am[kMaxRows];
   float gtl[kMaxQ], gdl[kMaxQ];
-  long long zt, zd;     // phase 3: this CTA's fixed-point normalisers (cluster-visible)
-  long long S[2];       // phase 3: this CTA's fixed-point weight sum per pass (cluster-visible)
+  long long zt, zd;  // phase 3: this CTA's fixed-point normalisers (cluster-visible)
+  long long S[2];    // phase 3: this CTA's fixed-point weight sum per pass (cluster-visible)
   long long ll_buf[kWarps];
   long long P_owner, target;
   float rho_hi, rho_lo;
@@ -186,6 +206,8 @@ struct Smem {
 
 template <typename T, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
+  constexpr int IE = item_elems<T, VEC>();
+  constexpr int LOADS = ItemCfg<T, VEC>::LOADS, N = ItemCfg<T, VEC>::N;
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -200,7 +222,7 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
   const int d0 = t0 - b;
   const int lo = min(V, rank * args.chunk), hi = min(V, lo + args.chunk);
   const int len = hi - lo;
-  const int nsub = (len + kSub - 1) / kSub;
+  const int nsub = (len + IE - 1) / IE;
   const int rows = (MODE == kStochastic) ? n + K : n;
   const T *tgt = reinterpret_cast<const T *>(args.tgt);
   const T *drf = reinterpret_cast<const T *>(args.drf);
@@ -221,23 +243,28 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
   for (int it = warp; it < items; it += kWarps) {
     const int r = it / nsub, s = it % nsub;
     const T *row = (r < n) ? tgt + (size_t)(t0 + r) * V : drf + (size_t)(d0 + (r - n)) * V;
-    const int e0 = lo + s * kSub, e1 = min(hi, e0 + kSub);
-    float v[32];
-    int idx[32];
-    load_item<T, VEC>(row, e0, e1, lane, v, idx);
+    const int e0 = lo + s * IE, e1 = min(hi, e0 + IE);
+    Raw<T, VEC> raw[LOADS];
+    int nv;
+    load_item<T, VEC>(row, e0, e1, lane, raw, nv);
     if constexpr (MODE == kStochastic) {
       float m = -INFINITY;  // raw logit maximum (exact)
 #pragma unroll
-      for (int k = 0; k < 32; ++k)
-        if (idx[k] >= 0) {
-          bad |= (v[k] != v[k]) | (v[k] == INFINITY);
-          m = fmaxf(m, v[k]);
-        }
+      for (int u = 0; u < LOADS; ++u)
+        if (u < nv)
+#pragma unroll
+          for (int k = 0; k < N; ++k) {
+            const float x = elem<T, VEC>(raw[u], k);
+            bad |= (x != x) | (x == INFINITY);
+            m = fmaxf(m, x);
+          }
       float sum = 0.f;
       if (m != -INFINITY) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (idx[k] >= 0) sum += exp2f((v[k] - m) * coef);
+        for (int u = 0; u < LOADS; ++u)
+          if (u < nv)
+#pragma unroll
+            for (int k = 0; k < N; ++k) sum += exp2f((elem<T, VEC>(raw[u], k) - m) * coef);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -253,11 +280,14 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
       float best = 0.f;
       int bi = -1;
 #pragma unroll
-      for (int k = 0; k < 32; ++k)
-        if (idx[k] >= 0) {
-          bad |= (v[k] != v[k]);
-          am_combine(best, bi, v[k], idx[k]);
-        }
+      for (int u = 0; u < LOADS; ++u)
+        if (u < nv)
+#pragma unroll
+          for (int k = 0; k < N; ++k) {
+            const float x = elem<T, VEC>(raw[u], k);
+            bad |= (x != x);
+            am_combine(best, bi, x, e0 + (u * 32 + lane) * N + k);
+          }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
@@ -409,9 +439,15 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
     // ---- pass A: fixed-point normalisers of the row pair (residual draws) ----
     if (resid) {
       long long zt = 0, zd = 0;
-      for (int e = lo + tid; e < hi; e += kThreads) {
-        zt += to_fix(exp2_acc(to_f32(trow[e]) - Mt, chi, clo));
-        zd += to_fix(exp2_acc(to_f32(drow[e]) - Md, chi, clo));
+      for (int e = lo + tid * kGroup; e < hi; e += kSeg) {
+        float xt[kGroup], xd[kGroup];
+        load8<T, VEC>(trow, e, hi, xt);
+        load8<T, VEC>(drow, e, hi, xd);
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+          zt += to_fix(exp2_acc(xt[k] - Mt, chi, clo));
+          zd += to_fix(exp2_acc(xd[k] - Md, chi, clo));
+        }
       }
       zt = block_sum_ll(zt, sm.ll_buf);
       zd = block_sum_ll(zd, sm.ll_buf);
@@ -437,16 +473,33 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
 
     for (int pass = 0; pass < 2; ++pass) {
       const bool res_pass = resid && pass == 0;
-      // w_v proportional to max(0, p_v - q_v) (or to p_v), scaled by Z_t, in [0, 1]
-      auto weight = [&](int e) -> float {
-        const float et = exp2_acc(to_f32(trow[e]) - Mt, chi, clo);
-        if (!res_pass) return et;
-        const float ed = exp2_acc(to_f32(drow[e]) - Md, chi, clo);
-        return fmaxf(et - fmaf(ed, rho_hi, ed * rho_lo), 0.f);
+      // the eight weights of elements e .. e+7, in [0, 1]: proportional to
+      // max(0, p_v - q_v) (scaled by Z_t), or to p_v
+      auto weights8 = [&](int e, long long (&w)[kGroup]) {
+        float xt[kGroup];
+        load8<T, VEC>(trow, e, hi, xt);
+        if (res_pass) {
+          float xd[kGroup];
+          load8<T, VEC>(drow, e, hi, xd);
+#pragma unroll
+          for (int k = 0; k < kGroup; ++k) {
+            const float et = exp2_acc(xt[k] - Mt, chi, clo);
+            const float ed = exp2_acc(xd[k] - Md, chi, clo);
+            w[k] = to_fix(fmaxf(et - fmaf(ed, rho_hi, ed * rho_lo), 0.f));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kGroup; ++k) w[k] = to_fix(exp2_acc(xt[k] - Mt, chi, clo));
+        }
       };
       // ---- pass B: this CTA's fixed-point mass ----
       long long mass = 0;
-      for (int e = lo + tid; e < hi; e += kThreads) mass += to_fix(weight(e));
+      for (int e = lo + tid * kGroup; e < hi; e += kSeg) {
+        long long w[kGroup];
+        weights8(e, w);
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) mass += w[k];
+      }
       mass = block_sum_ll(mass, sm.ll_buf);
       if (tid == 0) sm.S[pass] = mass;
       cluster.sync();
@@ -484,19 +537,22 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
         const long long P = sm.P_owner, target = sm.target;
         long long carry = 0;
         for (int s0 = lo; s0 < hi; s0 += kSeg) {
-          long long w[kSegPer];
-          long long local = 0;
-          const int e = s0 + tid * kSegPer;
+          const int e = s0 + tid * kGroup;
+          long long w[kGroup];
+          if (e < hi) {
+            weights8(e, w);
+          } else {
 #pragma unroll
-          for (int k = 0; k < kSegPer; ++k) {
-            w[k] = (e + k < hi) ? to_fix(weight(e + k)) : 0;
-            local += w[k];
+            for (int k = 0; k < kGroup; ++k) w[k] = 0;
           }
+          long long local = 0;
+#pragma unroll
+          for (int k = 0; k < kGroup; ++k) local += w[k];
           long long seg_total;
           const long long excl = block_excl_scan_ll(local, sm.ll_buf, &seg_total);
           long long inc = P + carry + excl;
 #pragma unroll
-          for (int k = 0; k < kSegPer; ++k) {
+          for (int k = 0; k < kGroup; ++k) {
             inc += w[k];
             if (w[k] > 0) {
               if (P >= 0 && inc > target) atomicMin(&sm.y_min, e + k);
@@ -521,16 +577,17 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
   cluster.sync();  // keep this CTA's shared memory alive until every peer is done reading it
 }
 
+// Cluster size: enough CTAs to cover the SMs a few times over, and chunks of at
+// most kMaxChunk elements.
 int pick_cluster(int batch, int vocab) {
   const int sms = num_sms();
   int C = (batch * 8 < 3 * sms) ? 16 : 8;
-  if ((vocab + 7) / 8 * 8 > 8 * kSub * kMaxSub) C = 16;
+  while (C < 16 && (vocab + C - 1) / C > kMaxChunk) C *= 2;
   return C;
 }
 
 template <typename T, bool VEC, int MODE>
-cudaError_t launch_t(const SamplerArgs &a0, int C, cudaStream_t st) {
-  SamplerArgs a = a0;
+cudaError_t launch_t(const SamplerArgs &a, int C, cudaStream_t st) {
   auto kern = sampler_kernel<T, VEC, MODE>;
   if (C > 8) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -577,6 +634,8 @@ cudaError_t launch_sampler(const SamplerArgs &a0, int dtype, int mode, cudaStrea
   return dtype == SV_DTYPE_BF16 ? launch_d<__nv_bfloat16>(a, mode, C, st) : launch_d<float>(a, mode, C, st);
 }
 
-bool sampler_supports(int vocab) { return vocab <= 16 * kSub * kMaxSub; }
+// Largest vocabulary: 16 chunks of kMaxChunk elements (a chunk is at most
+// kMaxSub work items of 1024 or 2048 elements).
+bool sampler_supports(int vocab) { return vocab <= 16 * kMaxChunk; }
 
 }  // namespace sv

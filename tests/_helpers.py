@@ -51,6 +51,7 @@ def compare_samples(step, gpu, ref, *, tree=False):
     acc, tok, num = gpu
     B = step.n_q.shape[0]
     diverged = 0
+    details = []
     for b in range(B):
         same = (acc[b] == ref.accept_cnt[b] and num[b] == ref.num_out[b]
                 and np.array_equal(tok[b], ref.out_tok[b]))
