@@ -17,10 +17,11 @@
 //    128-byte swizzle, one box per (physical block, half of head_dim));
 //    mbarriers with transaction counts signal "full", consumer arrivals
 //    signal "empty"; every wait is bounded;
-//  * four consumer warps: S = Q K^T with bf16 mma.sync m16n8k16 (warp w takes
-//    keys 16w..16w+15 of the tile for all rows), online softmax in base 2
-//    with the running max shared through shared memory, P (bf16) to shared
-//    memory, then O += P V with warp w taking output columns 32w..32w+31;
+//  * consumer warps (4 by default): S = Q K^T with bf16 mma.sync m16n8k16
+//    (warp w takes an equal slice of the tile's keys for all rows), online
+//    softmax in base 2 with the running max shared through shared memory,
+//    P (bf16) to shared memory, then O += P V with warp w taking an equal
+//    slice of the output columns;
 //  * the final tile of a split zeroes the V rows past the split's end before
 //    P V (pool slots past a sequence's length hold arbitrary bytes).
 // Partial results of multi-split sequences go to the workspace in the same
@@ -34,9 +35,21 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTile = 64;  // keys per tile
-constexpr int kStages = 3;
-constexpr int kConsumerWarps = 4;
+// Ring depth and consumer warps are build-time constants (defaults below).
+#ifndef SV_ATTN_STAGES
+#define SV_ATTN_STAGES 3
+#endif
+#ifndef SV_ATTN_CONSUMER_WARPS
+#define SV_ATTN_CONSUMER_WARPS 4
+#endif
+constexpr int kStages = SV_ATTN_STAGES;
+constexpr int kConsumerWarps = SV_ATTN_CONSUMER_WARPS;  // 4 or 8
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kKeysPerWarp = kTile / kConsumerWarps;  // S = Q K^T: keys per warp
+constexpr int kNtS = kKeysPerWarp / 8;                // n8 tiles of keys per warp
+constexpr int kColsPerWarp = kD / kConsumerWarps;      // O += P V: output columns per warp
+constexpr int kNtO = kColsPerWarp / 8;                 // n8 tiles of columns per warp
+static_assert(kConsumerWarps == 4 || kConsumerWarps == 8, "4 or 8 consumer warps");
 constexpr int kStageBytes = 2 * kTile * kD * 2;  // K and V
 constexpr int kHalfBytes = kTile * 128;          // 64 rows x 128 bytes (half of head_dim)
 constexpr long long kSpinLimit = 1LL << 24;  // try_wait polls before a wait gives up
@@ -91,6 +104,9 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -270,11 +286,11 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
       pos_of[mt][h] = r < R ? r / G : -1;
       tmask_of[mt][h] = (r < R && a.mask_kind == SV_MASK_TREE) ? a.tree_mask[row0 + r / G] : 0ull;
     }
-  float o_acc[RG][4][4];
+  float o_acc[RG][kNtO][4];
 #pragma unroll
   for (int mt = 0; mt < RG; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < kNtO; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o_acc[mt][nt][e] = 0.f;
 
@@ -297,23 +313,24 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
     }
     const uint32_t k_base = smem_u32(kst), v_base = smem_u32(vst);
 
-    // ---- S = Q K^T for keys 16w .. 16w+15 of the tile ----
-    float sfr[RG][2][4];
+    // ---- S = Q K^T for keys kKeysPerWarp*w .. of the tile ----
+    float sfr[RG][kNtS][4];
 #pragma unroll
     for (int mt = 0; mt < RG; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < kNtS; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sfr[mt][nt][e] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < kD / 16; ++kk) {
-      // B fragments: keys (16w + 8*nt + lane%8), head_dim chunk 2kk + (lane/8)%2
-      uint32_t b00, b01, b10, b11;
+      // B fragments: keys (kKeysPerWarp*w + 8*nt + lane%8), head_dim chunk 2kk + (lane/8)%2
+      uint32_t b00, b01, b10 = 0, b11 = 0;
       {
         const int mi = lane >> 3;
-        const int key = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+        const int key = warp * kKeysPerWarp + (kNtS == 2 ? (mi >> 1) : 0) * 8 + (lane & 7);
         const int ch = 2 * kk + (mi & 1);
-        ldsm_x4(k_base + (ch >> 3) * kHalfBytes + swz(key, ch & 7), b00, b01, b10, b11);
+        if constexpr (kNtS == 2) ldsm_x4(k_base + (ch >> 3) * kHalfBytes + swz(key, ch & 7), b00, b01, b10, b11);
+        else ldsm_x2(k_base + (ch >> 3) * kHalfBytes + swz(key, ch & 7), b00, b01);
       }
 #pragma unroll
       for (int mt = 0; mt < RG; ++mt) {
@@ -323,7 +340,7 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
         const int ch = 2 * kk + (mi >> 1);
         ldsm_x4(q_base + (ch >> 3) * (kRows * 128) + swz(row, ch & 7), a0, a1, a2, a3);
         mma16816(sfr[mt][0], a0, a1, a2, a3, b00, b01);
-        mma16816(sfr[mt][1], a0, a1, a2, a3, b10, b11);
+        if constexpr (kNtS == 2) mma16816(sfr[mt][kNtS - 1], a0, a1, a2, a3, b10, b11);
       }
     }
     // ---- scale, mask, per-warp row max ----
@@ -334,10 +351,10 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
         float mx = -INFINITY;
         const int i = pos_of[mt][h];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < kNtS; ++nt)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int key = kt + warp * 16 + nt * 8 + 2 * qc + e;
+            const int key = kt + warp * kKeysPerWarp + nt * 8 + 2 * qc + e;
             bool vis = i >= 0 && key < ke;
             if (vis && key >= c) {
               const int j = key - c;
@@ -373,21 +390,21 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
         m_run[mt][h] = mn;
         float ls = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < kNtS; ++nt) {
           const float p0 = exp2f(sfr[mt][nt][2 * h] - ref);
           const float p1 = exp2f(sfr[mt][nt][2 * h + 1] - ref);
           ls += p0 + p1;
-          const int chunk = warp * 2 + nt;
+          const int chunk = warp * kNtS + nt;
           *reinterpret_cast<uint32_t *>(p_s + swz(row, chunk) + qc * 4) = pack_bf16(p0, p1);
         }
         l_run[mt][h] = l_run[mt][h] * alpha[mt][h] + ls;
       }
     consumers_sync();
-    // ---- O = alpha * O + P V for output columns 32w .. 32w+31 ----
+    // ---- O = alpha * O + P V for output columns kColsPerWarp*w .. ----
 #pragma unroll
     for (int mt = 0; mt < RG; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
+      for (int nt = 0; nt < kNtO; ++nt) {
         o_acc[mt][nt][0] *= alpha[mt][0];
         o_acc[mt][nt][1] *= alpha[mt][0];
         o_acc[mt][nt][2] *= alpha[mt][1];
@@ -395,12 +412,12 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
       }
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk) {
-      uint32_t bv[4][2];
+      uint32_t bv[kNtO][2];
 #pragma unroll
-      for (int np = 0; np < 2; ++np) {
+      for (int np = 0; np < kNtO / 2; ++np) {
         const int mi = lane >> 3;
         const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
-        const int ch = warp * 4 + np * 2 + (mi >> 1);  // 16-byte chunk along head_dim (0..15)
+        const int ch = warp * kNtO + np * 2 + (mi >> 1);  // 16-byte chunk along head_dim (0..15)
         ldsm_x4_t(v_base + (ch >> 3) * kHalfBytes + swz(key, ch & 7), bv[2 * np][0], bv[2 * np][1], bv[2 * np + 1][0],
                   bv[2 * np + 1][1]);
       }
@@ -412,7 +429,7 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
         const int ch = 2 * kk + (mi >> 1);
         ldsm_x4(p_base + swz(row, ch), a0, a1, a2, a3);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mma16816(o_acc[mt][nt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+        for (int nt = 0; nt < kNtO; ++nt) mma16816(o_acc[mt][nt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
       }
     }
     __syncwarp();
@@ -447,15 +464,15 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
       if (nsplit == 1) {
         __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(a.out) + qrow * kD;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const int col = warp * 32 + nt * 8 + 2 * qc;
+        for (int nt = 0; nt < kNtO; ++nt) {
+          const int col = warp * kColsPerWarp + nt * 8 + 2 * qc;
           *reinterpret_cast<uint32_t *>(op + col) = pack_bf16(o_acc[mt][nt][2 * h] * inv, o_acc[mt][nt][2 * h + 1] * inv);
         }
       } else {
         const size_t prow = (size_t)split * a.total_q * a.num_q_heads + qrow;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const int col = warp * 32 + nt * 8 + 2 * qc;
+        for (int nt = 0; nt < kNtO; ++nt) {
+          const int col = warp * kColsPerWarp + nt * 8 + 2 * qc;
           *reinterpret_cast<float2 *>(a.ws_o + prow * kD + col) =
               make_float2(o_acc[mt][nt][2 * h] * inv, o_acc[mt][nt][2 * h + 1] * inv);
         }

@@ -3,7 +3,13 @@ workload (256 sequences, lognormal contexts, K_b ~ U{2..8} redrawn every
 iteration, 128-token blocks from a fragmented free list) runs 10 iterations of
 append -> attention -> rejection sample -> rollback on the GPU and in the
 oracle. Block tables, seq_lens, the free list and every emitted token must be
-bit-exact at every iteration; attention is compared on sampled sequences."""
+bit-exact at every iteration; attention is compared on sampled sequences.
+
+A decision may differ from the oracle only at an oracle-flagged near-tie, and
+such divergences, counted over the whole run, must stay below 0.01% of the
+verified positions. After one, the GPU rollback is given the oracle's accept
+counts for that step (oracle output into the GPU, never the reverse), so the
+caches stay comparable in the iterations that follow."""
 import numpy as np
 import pytest
 import torch
@@ -12,8 +18,8 @@ import oracle
 from speculative_decoding_verify_paged_gb300 import step as S
 from speculative_decoding_verify_paged_gb300 import workloads as W
 
-from _helpers import (assert_attn_close, assert_kv_equal, attn_as_f64, compare_samples, gpu_sample_result,
-                      rows_of, status_of)
+from _helpers import (MAX_TIE_FRACTION, assert_attn_close, assert_kv_equal, attn_as_f64, compare_samples,
+                      gpu_sample_result, rows_of, status_of)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +30,7 @@ def _loop(case, iterations, steps_of, attn_check_iters, attn_seqs, with_pools):
     okv = oracle.OracleKV(st, with_pools=with_pools)
     msl = int(st.seq_lens.max()) + 9 * iterations + 16
     accepted = []
+    diverged, positions = 0, 0
     for it in range(iterations):
         step = steps_of(it)
         d = S.DeviceStep.from_host(step)
@@ -38,14 +45,17 @@ def _loop(case, iterations, steps_of, attn_check_iters, attn_seqs, with_pools):
             assert_attn_close(attn_as_f64(buf.attn_out), ref, rows_of(step, attn_seqs))
         ref = oracle.rejection_sample(step)
         got = gpu_sample_result(buf)
-        diverged = compare_samples(step, got, ref)
-        assert diverged == 0, "a near-tie diverged: later iterations are not comparable"
+        diverged += compare_samples(step, got, ref, max_fraction=None)
+        positions += int(step.n_q.sum())
+        if not np.array_equal(got[0], ref.accept_cnt):
+            buf.accept.copy_(torch.from_numpy(ref.accept_cnt))
         S.rollback(kv, d, buf)
         okv.rollback(step, ref.accept_cnt)
         torch.cuda.synchronize()
         assert status_of(buf) == 0
         assert_kv_equal(kv, okv, pools=False)
         accepted.append(ref.accept_cnt)
+    assert diverged <= MAX_TIE_FRACTION * positions, f"{diverged} near-tie divergences in {positions} positions"
     return kv, okv, accepted
 
 
