@@ -33,7 +33,7 @@ METRIC = "spec-verify seqs/s & tokens/s; achieved HBM TB/s vs 8 TB/s (1 GB300)"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILES = os.path.join(ROOT, "profiles")
-ATTN_SOURCES = ["attn_tc.cu", "attn_simt.cu"]
+ATTN_SOURCES = ["attn_umma.cu", "attn_simt.cu"]
 
 
 def parse():
@@ -325,7 +325,7 @@ def run_native(args):
         "tokens_per_s": emitted * world / (elapsed_ms / 1e3),
         "scored_tokens_per_s": sp.total_q * args.steps * world / (elapsed_ms / 1e3),
         "mean_tokens_per_seq_step": emitted / (B * args.steps),
-        "roofline": {"kernel": "spec_verify_attn (split-KV attention + combine)", "bound": "hbm",
+        "roofline": {"kernel": "spec_verify_attn (tcgen05 split-KV attention + combine)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS, "peak_source": peak_kind,
                      "traffic": (traffic["bytes_per_launch_scaled"] if traffic else None),
@@ -363,7 +363,7 @@ def attn_path_times(kv, d, buf, msl, stream, reps=10):
     from speculative_decoding_verify_paged_gb300 import step as S
     out = {}
     S.append(kv, d, buf, stream)
-    for path in ("tensor_cores", "cuda_cores"):
+    for path in ("tensor_cores", "warp_mma", "cuda_cores"):
         try:
             L.set_attn_path(path)
             for _ in range(2):

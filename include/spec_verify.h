@@ -237,17 +237,27 @@ sv_status sv_kv_rollback(const sv_paged_kv *kv, const int32_t *cu_q, const int32
                          const int32_t *path_nodes, int32_t max_q_per_seq, int32_t *status_dev, void *stream);
 
 /*
- * Process-wide options (no counterpart on the pages; they select between two
+ * Process-wide options (no counterpart on the pages; they select between
  * complete implementations of the same operation, for measurement).
- *   SV_OPT_ATTN_PATH: SV_ATTN_AUTO (default: tensor cores for bf16 caches with
- *   head_dim 128 and blocks of at least 16 tokens, CUDA cores otherwise),
- *   SV_ATTN_CUDA_CORES, or SV_ATTN_TENSOR_CORES (an unsupported shape then
- *   returns SV_ERR_UNSUPPORTED from sv_spec_verify_attn).
+ *   SV_OPT_ATTN_PATH:
+ *     SV_ATTN_AUTO (default): 5th-generation tensor cores (tcgen05, TMEM) for
+ *       bf16 caches with head_dim 128 and blocks of 16..256 tokens, CUDA cores
+ *       otherwise;
+ *     SV_ATTN_CUDA_CORES: the CUDA-core kernel for every shape;
+ *     SV_ATTN_TENSOR_CORES: tcgen05 (an unsupported shape then returns
+ *       SV_ERR_UNSUPPORTED from sv_spec_verify_attn);
+ *     SV_ATTN_WARP_MMA: warp-level mma.sync tensor-core kernel (same shapes as
+ *       tcgen05).
  * Returns SV_ERR_INVALID_ARG for an unknown option or value. Not thread-safe
  * with respect to calls in flight on other host threads.
  */
 typedef enum sv_option { SV_OPT_ATTN_PATH = 1 } sv_option;
-typedef enum sv_attn_path { SV_ATTN_AUTO = 0, SV_ATTN_CUDA_CORES = 1, SV_ATTN_TENSOR_CORES = 2 } sv_attn_path;
+typedef enum sv_attn_path {
+  SV_ATTN_AUTO = 0,
+  SV_ATTN_CUDA_CORES = 1,
+  SV_ATTN_TENSOR_CORES = 2,
+  SV_ATTN_WARP_MMA = 3
+} sv_attn_path;
 sv_status sv_set_option(int32_t option, int32_t value);
 
 /* A static, human-readable name of a status code. */

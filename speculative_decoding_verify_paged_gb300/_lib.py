@@ -32,7 +32,7 @@ EXPORTS = ("sv_kv_append", "sv_spec_verify_attn_workspace_bytes", "sv_spec_verif
            "sv_spec_rejection_sample", "sv_tree_greedy_accept", "sv_kv_rollback", "sv_status_string",
            "sv_version", "sv_set_option")
 SV_OPT_ATTN_PATH = 1
-ATTN_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
+ATTN_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "warp_mma": 3}
 
 
 class SVError(RuntimeError):
@@ -92,7 +92,8 @@ def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CD
 
 
 def set_attn_path(path: str) -> None:
-    """Select the attention implementation: "auto", "cuda_cores" or "tensor_cores"."""
+    """Select the attention implementation: "auto", "cuda_cores", "tensor_cores"
+    (tcgen05) or "warp_mma" (mma.sync)."""
     _check(load().sv_set_option(SV_OPT_ATTN_PATH, ATTN_PATHS[path]), "sv_set_option")
 
 

@@ -106,7 +106,7 @@ const char *sv_status_string(int32_t status) {
 int32_t sv_version(void) { return 10000; }
 
 sv_status sv_set_option(int32_t option, int32_t value) {
-  if (option == SV_OPT_ATTN_PATH && value >= SV_ATTN_AUTO && value <= SV_ATTN_TENSOR_CORES) {
+  if (option == SV_OPT_ATTN_PATH && value >= SV_ATTN_AUTO && value <= SV_ATTN_WARP_MMA) {
     g_attn_path = value;
     return SV_OK;
   }
@@ -170,10 +170,21 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
   a.mask_kind = mask_kind;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = (cudaStream_t)stream;
-  const bool tc_ok = kv->dtype == SV_DTYPE_BF16 && attn_tc_supported(a.kv, num_q_heads, max_q_per_seq);
-  if (g_attn_path == SV_ATTN_TENSOR_CORES && !tc_ok) return SV_ERR_UNSUPPORTED;
-  const bool use_tc = tc_ok && g_attn_path != SV_ATTN_CUDA_CORES;
-  cudaError_t e = use_tc ? launch_attn_tc(a, st) : launch_attn_simt(a, kv->dtype, st);
+  const bool umma_ok = kv->dtype == SV_DTYPE_BF16 && attn_umma_supported(a.kv);
+  const bool mma_ok = kv->dtype == SV_DTYPE_BF16 && attn_tc_supported(a.kv, num_q_heads, max_q_per_seq);
+  cudaError_t e;
+  switch (g_attn_path) {
+    case SV_ATTN_CUDA_CORES: e = launch_attn_simt(a, kv->dtype, st); break;
+    case SV_ATTN_TENSOR_CORES:
+      if (!umma_ok) return SV_ERR_UNSUPPORTED;
+      e = launch_attn_umma(a, st);
+      break;
+    case SV_ATTN_WARP_MMA:
+      if (!mma_ok) return SV_ERR_UNSUPPORTED;
+      e = launch_attn_tc(a, st);
+      break;
+    default: e = umma_ok ? launch_attn_umma(a, st) : launch_attn_simt(a, kv->dtype, st);
+  }
   if (e != cudaSuccess) return SV_ERR_CUDA;
   return cuda_status(launch_attn_combine(a, kv->dtype, st));
 }

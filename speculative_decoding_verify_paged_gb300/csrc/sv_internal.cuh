@@ -94,6 +94,8 @@ cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnArgs &a, int dtype, cudaStream_t st);
 bool attn_tc_supported(const KV &kv, int num_q_heads, int max_q);
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
+bool attn_umma_supported(const KV &kv);
+cudaError_t launch_attn_umma(const AttnArgs &a, cudaStream_t st);
 
 struct SamplerArgs {
   const void *tgt;
