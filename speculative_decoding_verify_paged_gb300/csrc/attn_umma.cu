@@ -13,11 +13,14 @@
 // One CTA = one sequence x one KV head x one split of its keys x up to 128
 // query rows (the G query heads of the KV head times the sequence's rows, one
 // row per TMEM lane). Six warps:
-//  * warp 0, producer: TMA (cp.async.bulk.tensor.2d, 128-byte swizzle) of
-//    32-key K and V tiles into a 4-stage ring; block ids read 32 at a time;
+//  * warp 0, producer: TMA of 32-key K and V tiles into a 4-stage ring. The
+//    pool is viewed as a 3-D tensor (64 elements, rows, 2 halves of
+//    head_dim) so that one 128-byte-swizzled box brings both halves of a
+//    group of R = min(block_size, 32) rows: a tile is 32/R groups, each
+//    stored [half 0 | half 1]; block ids are read 32 at a time;
 //  * warp 1, MMA issuer (one lane) and TMEM owner: S(t) = Q K(t)^T with
-//    tcgen05.mma kind::f16 (M = 128 rows, N = 32 keys, K = 128; A and B
-//    K-major in shared memory) into one of two TMEM S buffers, then
+//    tcgen05.mma kind::f16 (M = 128 rows, N = R keys per group, K = 128; A and
+//    B K-major in shared memory) into one of two TMEM S buffers, then
 //    O += P(t-1) V(t-1) (A = P in TMEM, B = V MN-major in shared memory,
 //    N = 128); tcgen05.commit frees the K/V stage and signals the softmax;
 //  * warps 2-5, softmax and epilogue: thread = query row = TMEM lane. Each
@@ -72,11 +75,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
   return false;
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+// One box of the (64 elements, rows, 2 halves) view: R rows, both halves.
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap *map, int y, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
           dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(0), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -156,7 +160,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 struct UmmaParams {
   AttnArgs a;
-  int box_rows;    // rows per TMA box: min(block_size, 32)
+  int box_rows;    // rows per TMA box (a group): min(block_size, 32), 16 or 32
   int row_blocks;  // CTAs per (sequence, KV head, split) along the query rows
 };
 
@@ -239,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
   if (warp == 0) {
     // ================= producer =================
     const int bs = kv.block_size, box = P.box_rows;
-    const uint32_t box_bytes = static_cast<uint32_t>(box) * 128;
+    const uint32_t box_bytes = static_cast<uint32_t>(box) * 256;
     const int lb_first = kb / bs, lb_last = (ke - 1) / bs;
     const int32_t *bt = kv.block_table + (size_t)b * kv.max_blocks;
     auto load_id = [&](int lb) -> int {
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
       }
       if (lane == 0) {
         const uint32_t fb = smem_u32(&full[s]);
-        mbar_expect_tx(fb, static_cast<uint32_t>(nbox) * 4u * box_bytes);
+        mbar_expect_tx(fb, static_cast<uint32_t>(nbox) * 2u * box_bytes);
         const uint32_t kdst = smem_u32(stages + s * kStageBytes);
         const uint32_t vdst = kdst + 2 * kHalfBytes;
         for (int r = 0; r < kTile; r += box) {
@@ -288,28 +292,30 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
           if (id < 0) continue;
           const int tok = kt + r;
           const int y = (id * kv.num_kv_heads + kvh) * bs + (tok % bs);
-          const uint32_t off = static_cast<uint32_t>(r) * 128;
-          tma_load_2d(kdst + off, &tmap_k, 0, y, fb);
-          tma_load_2d(kdst + kHalfBytes + off, &tmap_k, 64, y, fb);
-          tma_load_2d(vdst + off, &tmap_v, 0, y, fb);
-          tma_load_2d(vdst + kHalfBytes + off, &tmap_v, 64, y, fb);
+          const uint32_t off = static_cast<uint32_t>(r) * 256;  // group of `box` rows, both halves
+          tma_load_rows(kdst + off, &tmap_k, y, fb);
+          tma_load_rows(vdst + off, &tmap_v, y, fb);
         }
       }
       __syncwarp();
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
-    constexpr uint32_t idesc_s = mma_idesc(128, kTile, 0);
+    const int R = P.box_rows;            // rows per group: 16 or 32
+    const uint32_t idesc_s = mma_idesc(128, R, 0);
     constexpr uint32_t idesc_o = mma_idesc(128, kD, 1);
     const uint32_t q_base = smem_u32(q_s);
-    auto issue_pv = [&](int u) {  // O += P(u) V(u)
+    const uint32_t half_bytes = static_cast<uint32_t>(R) * 128;  // one half of a group
+    auto issue_pv = [&](int u) {  // O += P(u) V(u), 16 keys per MMA
       const int su = u % kStages;
       const uint32_t v_base = smem_u32(stages + su * kStageBytes) + 2 * kHalfBytes;
       const uint32_t p_col = tmem + (u & 1) * kTile;
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk)
-        mma_ts(tmem + kColO, p_col + kk * 8, smem_desc(v_base + kk * 2048, kHalfBytes, 1024), idesc_o,
-               (u > 0 || kk > 0) ? 1 : 0);
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const int grp = (kk * 16) / R, sub = ((kk * 16) % R) / 16;
+        const uint32_t start = v_base + grp * 2 * half_bytes + sub * 2048;
+        mma_ts(tmem + kColO, p_col + kk * 8, smem_desc(start, half_bytes, 1024), idesc_o, (u > 0 || kk > 0) ? 1 : 0);
+      }
       mma_commit(smem_u32(&empty[su]));
       mma_commit(smem_u32(o_bar));
     };
@@ -321,11 +327,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
         tc_fence_after();
         if (lane == 0) {
           const uint32_t k_base = smem_u32(stages + s * kStageBytes);
+          for (int grp = 0; grp < kTile / R; ++grp) {
+            const uint32_t kg = k_base + grp * 2 * half_bytes;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_ss(tmem + (t & 1) * kTile,
-                   smem_desc(q_base + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
-                   smem_desc(k_base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024), idesc_s, kk > 0 ? 1 : 0);
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ss(tmem + (t & 1) * kTile + grp * R,
+                     smem_desc(q_base + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
+                     smem_desc(kg + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024), idesc_s, kk > 0 ? 1 : 0);
+          }
           mma_commit(smem_u32(&s_full[t & 1]));
         }
         __syncwarp();
@@ -360,9 +369,11 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
       if (valid < kTile) {
         // zero this tile's V rows past the split's end before P V reads them
         uint8_t *vst = stages + (t % kStages) * kStageBytes + 2 * kHalfBytes;
+        const int R = P.box_rows;
         for (int x = (warp - 2) * 32 + lane; x < (kTile - valid) * 16; x += kSoftWarps * 32) {
           const int rr = valid + (x >> 4), ch = x & 15;
-          *reinterpret_cast<uint4 *>(vst + (ch >> 3) * kHalfBytes + rr * 128 + (ch & 7) * 16) =
+          const int grp = rr / R, rin = rr % R;
+          *reinterpret_cast<uint4 *>(vst + grp * 2 * R * 128 + (ch >> 3) * R * 128 + rin * 128 + (ch & 7) * 16) =
               make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async();
@@ -491,15 +502,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// The pool as a 3-D tensor: (64 elements of a half row, rows, 2 halves) with
+// strides (256 B per row, 128 B per half); a box of R rows lands as
+// [half 0: R rows x 128 B][half 1: R rows x 128 B], 128-byte swizzled.
 bool make_map(CUtensorMap *map, void *pool, const KV &kv, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t rows = (cuuint64_t)kv.num_blocks * kv.num_kv_heads * kv.block_size;
-  const cuuint64_t gdim[2] = {(cuuint64_t)kD, rows};
-  const cuuint64_t gstride[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  const cuuint32_t estride[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool, gdim, gstride, box, estride,
+  const cuuint64_t gdim[3] = {64, rows, 2};
+  const cuuint64_t gstride[2] = {(cuuint64_t)kD * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool, gdim, gstride, box, estride,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
