@@ -13,18 +13,21 @@
 // One CTA = one sequence x one KV head x one split of its keys x up to 128
 // query rows (the G query heads of the KV head times the sequence's rows, one
 // row per TMEM lane). Six warps:
-//  * warp 0, producer: TMA of 32-key K and V tiles into a 4-stage ring. The
+//  * warp 0, producer: TMA of 32-key K and V tiles into a 6-stage ring. The
 //    pool is viewed as a 3-D tensor (64 elements, rows, 2 halves of
 //    head_dim) so that one 128-byte-swizzled box brings both halves of a
 //    group of R = min(block_size, 32) rows: a tile is 32/R groups, each
 //    stored [half 0 | half 1]; block ids are read 32 at a time;
 //  * warp 1, MMA issuer (one lane) and TMEM owner: S(t) = Q K(t)^T with
-//    tcgen05.mma kind::f16 (M = 128 rows, N = R keys per group, K = 128; A and
-//    B K-major in shared memory) into one of two TMEM S buffers, then
+//    tcgen05.mma kind::f16 (M = 128 rows, N = R keys per group, K = 128; A = Q
+//    in TMEM, B = K K-major in shared memory) into one of two TMEM S buffers,
+//    then
 //    O += P(t-1) V(t-1) (A = P in TMEM, B = V MN-major in shared memory,
 //    N = 128); tcgen05.commit frees the K/V stage and signals the softmax;
 //  * warps 2-5, softmax and epilogue: thread = query row = TMEM lane. Each
-//    reads its row of S(t) (tcgen05.ld), masks edge tiles, keeps a running
+//    first stores its row of Q into TMEM (the tensor core then reads Q from
+//    TMEM instead of shared memory), reads its row of S(t) (tcgen05.ld),
+//    masks edge tiles, keeps a running
 //    maximum that moves only when the tile maximum exceeds it by more than
 //    2^8 (then O is rescaled in TMEM), writes P = 2^(s - m) as bf16 over S
 //    (tcgen05.st), and at the end reads O, divides by the row sum and stores
@@ -39,15 +42,15 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTile = 32;                       // keys per tile
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kRowsMax = 128;                   // query rows per CTA (TMEM lanes)
 constexpr int kSoftWarps = 4;
 constexpr int kThreads = (2 + kSoftWarps) * 32;
 constexpr int kHalfBytes = kTile * 128;         // 32 keys x 128 bytes (half of head_dim)
 constexpr int kStageBytes = 4 * kHalfBytes;     // K and V, two halves each
-constexpr int kQHalf = kRowsMax * 128;          // 128 rows x 128 bytes
-constexpr int kTmemCols = 256;                  // S0 [0,32) S1 [32,64) O [64,192)
+constexpr int kTmemCols = 256;                  // S0 [0,32) S1 [32,64) O [64,192) Q [192,256)
 constexpr int kColO = 64;
+constexpr int kColQ = 192;
 constexpr float kRescaleThreshold = 8.f;        // log2 units
 constexpr long long kSpinLimit = 1LL << 24;
 
@@ -104,12 +107,6 @@ __host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
-          d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accum));
-}
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, int accum) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
@@ -140,6 +137,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       SV_W8(r, 0), SV_W8(r, 8), SV_W8(r, 16), SV_W8(r, 24)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,"
+      "%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};" ::"r"(taddr),
+      SV_W8(r, 0), SV_W8(r, 8), SV_W8(r, 16), SV_W8(r, 24), SV_W8(r, 32), SV_W8(r, 40), SV_W8(r, 48), SV_W8(r, 56)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -154,10 +159,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
 }
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
 struct UmmaParams {
   AttnArgs a;
   int box_rows;    // rows per TMA box (a group): min(block_size, 32), 16 or 32
@@ -193,29 +194,15 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *stages = base;                              // kStages x (K 8 KB | V 8 KB)
-  uint8_t *q_s = stages + kStages * kStageBytes;       // 2 halves x 128 rows x 128 B
-  uint64_t *full = reinterpret_cast<uint64_t *>(q_s + 2 * kQHalf);
+  uint8_t *stages = base;  // kStages x (K 8 KB | V 8 KB)
+  uint64_t *full = reinterpret_cast<uint64_t *>(stages + kStages * kStageBytes);
   uint64_t *empty = full + kStages;
   uint64_t *s_full = empty + kStages;  // [2] S(t) in TMEM buffer t % 2
   uint64_t *p_ready = s_full + 2;      // [2] P(t) written over buffer t % 2
   uint64_t *o_bar = p_ready + 2;       // one phase per finished P V
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_bar + 1);
+  uint64_t *q_ready = o_bar + 1;       // Q rows stored in TMEM
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_ready + 1);
 
-  // ---- Q rows into shared memory (K-major, 128-byte swizzle); padding rows are zero ----
-  {
-    const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q);
-    for (int x = tid; x < kRowsMax * 16; x += kThreads) {
-      const int rr = x >> 4, ch = x & 15, r = rbase + rr;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < R) {
-        const int i = r / G, g = r % G;
-        v = *reinterpret_cast<const uint4 *>(qp + ((size_t)(row0 + i) * a.num_q_heads + kvh * G + g) * kD + ch * 8);
-      }
-      *reinterpret_cast<uint4 *>(q_s + (ch >> 3) * kQHalf + swz(rr, ch & 7)) = v;
-    }
-  }
-  fence_proxy_async();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -226,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
       mbar_init(smem_u32(&p_ready[s]), kSoftWarps);
     }
     mbar_init(smem_u32(o_bar), 1);
+    mbar_init(smem_u32(q_ready), kSoftWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -304,7 +292,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
     const int R = P.box_rows;            // rows per group: 16 or 32
     const uint32_t idesc_s = mma_idesc(128, R, 0);
     constexpr uint32_t idesc_o = mma_idesc(128, kD, 1);
-    const uint32_t q_base = smem_u32(q_s);
     const uint32_t half_bytes = static_cast<uint32_t>(R) * 128;  // one half of a group
     auto issue_pv = [&](int u) {  // O += P(u) V(u), 16 keys per MMA
       const int su = u % kStages;
@@ -319,6 +306,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
       mma_commit(smem_u32(&empty[su]));
       mma_commit(smem_u32(o_bar));
     };
+    ok = mbar_wait(smem_u32(q_ready), 0);
+    tc_fence_after();
     for (int t = 0; t <= ntiles && ok; ++t) {
       if (t < ntiles) {
         const int s = t % kStages;
@@ -331,8 +320,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
             const uint32_t kg = k_base + grp * 2 * half_bytes;
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-              mma_ss(tmem + (t & 1) * kTile + grp * R,
-                     smem_desc(q_base + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
+              mma_ts(tmem + (t & 1) * kTile + grp * R, tmem + kColQ + kk * 8,
                      smem_desc(kg + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024), idesc_s, kk > 0 ? 1 : 0);
           }
           mma_commit(smem_u32(&s_full[t & 1]));
@@ -358,6 +346,30 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
     const uint64_t tm = (live && a.mask_kind == SV_MASK_TREE) ? a.tree_mask[row0 + i] : 0ull;
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
     const bool warp_live = __any_sync(0xffffffffu, live);
+    if (warp_live) {
+      // this lane's query row into TMEM columns [kColQ, kColQ + 64): bf16 pairs, zeros for padding rows
+      uint32_t qr[64];
+      if (live) {
+        const uint4 *qp = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.q) +
+                                                          ((size_t)(row0 + i) * a.num_q_heads + kvh * G + r % G) * kD);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          const uint4 x = qp[v];
+          qr[4 * v] = x.x;
+          qr[4 * v + 1] = x.y;
+          qr[4 * v + 2] = x.z;
+          qr[4 * v + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 64; ++v) qr[v] = 0u;
+      }
+      tmem_st64(lane_addr + kColQ, qr);
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(q_ready));
     float m_run = -INFINITY, l_run = 0.f;
     for (int t = 0; t < ntiles; ++t) {
       const int kt = kb + t * kTile;
@@ -384,7 +396,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
         tmem_wait_ld();
         const bool edge = (kt + kTile > c) || (valid < kTile);
         float sv[32];
-        float mx = -INFINITY;
 #pragma unroll
         for (int k = 0; k < kTile; ++k) {
           float v = __uint_as_float(sr[k]) * a.scale_log2;
@@ -399,7 +410,17 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
           }
           if (!live) v = -INFINITY;
           sv[k] = v;
-          mx = fmaxf(mx, v);
+        }
+        float mx;
+        {
+          float t16[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) t16[k] = fmaxf(sv[k], sv[k + 16]);
+#pragma unroll
+          for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) t16[k] = fmaxf(t16[k], t16[k + w]);
+          mx = t16[0];
         }
         // move the running maximum only when the tile's exceeds it by the threshold
         const bool move = mx > m_run + kRescaleThreshold || (m_run == -INFINITY && mx != -INFINITY);
@@ -425,14 +446,18 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
         }
         const float ref = (m_run == -INFINITY) ? 0.f : m_run;
         uint32_t pr[kTile / 2];
-        float ls = 0.f;
+        float ps[kTile / 2];
 #pragma unroll
         for (int k = 0; k < kTile / 2; ++k) {
           const float p0 = exp2f(sv[2 * k] - ref), p1 = exp2f(sv[2 * k + 1] - ref);
-          ls += p0 + p1;
+          ps[k] = p0 + p1;
           pr[k] = pack_bf16(p0, p1);
         }
-        l_run += ls;
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int k = 0; k < w; ++k) ps[k] += ps[k + w];
+        l_run += ps[0];
         tmem_st16(lane_addr + (t & 1) * kTile, pr);
         tmem_wait_st();
       }
@@ -518,7 +543,9 @@ bool make_map(CUtensorMap *map, void *pool, const KV &kv, int box_rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 2 * kQHalf + 16 * 8 + 16;
+// 6 stages of 16 KB; at most two CTAs fit an SM, which is what TMEM allows (2 x 256 columns)
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 32 * 8;
+static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "a third CTA per SM would wait for TMEM");
 
 }  // namespace
 
