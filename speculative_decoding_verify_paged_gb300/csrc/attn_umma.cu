@@ -466,6 +466,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
       if (lane == 0) mbar_arrive(smem_u32(&p_ready[t & 1]));
     }
     // ---- epilogue: wait for the last P V, then write the row ----
+    // S(t) is issued before P(t-1) V(t-1), so seeing S(ntiles-1) proves only
+    // that P V up to ntiles-3 finished: o_bar may still be in the phase of
+    // ntiles-2, and a parity wait for ntiles-1 alone would pass early there.
+    if (ok && ntiles > 1) ok = mbar_wait(smem_u32(o_bar), (ntiles - 2) & 1);
     if (ok && ntiles > 0) ok = mbar_wait(smem_u32(o_bar), (ntiles - 1) & 1);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
