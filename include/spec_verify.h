@@ -163,6 +163,35 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
                               void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /*
+ * sv_spec_verify_attn_no_alloc -- sv_spec_verify_attn without a caller
+ * workspace. The pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory around the attention call: an
+ * engine that hands all free HBM to its KV block pool at start-up and has none
+ * left to lend, or a host framework that owns the device allocator and
+ * forbids a plug-in from calling cudaMalloc (which may also synchronise the
+ * device in the middle of a step).
+ *
+ * Same arguments, semantics and status codes as sv_spec_verify_attn, minus
+ * the workspace. The scratch is a static device array of
+ * SV_ATTN_NO_ALLOC_SCRATCH_BYTES that every device loading the library holds
+ * until the process exits. Sizes whose sv_spec_verify_attn_workspace_bytes
+ * exceeds it return SV_ERR_WORKSPACE and launch nothing.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device uses the same array and leaves its contents
+ *     behind; nothing in it needs to start at zero, since each value the
+ *     kernels read was written earlier in the same call.
+ *   - Calls whose kernels overlap on the GPU (other streams, other host
+ *     threads) race on the array: order them on one stream or with events.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ */
+#define SV_ATTN_NO_ALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+sv_status sv_spec_verify_attn_no_alloc(const sv_paged_kv *kv, const void *q, void *out, const int32_t *cu_q,
+                                       int32_t num_q_heads, int32_t total_q, int32_t max_q_per_seq,
+                                       int32_t max_seq_len, float scale, int32_t mask_kind,
+                                       const uint64_t *tree_mask, int32_t *status_dev, void *stream);
+
+/*
  * sv_spec_rejection_sample -- lossless verification of chain drafts.
  *
  * Target row cu_q[b] + i holds the logits of the position that draft token

@@ -20,6 +20,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
 SV_OK = 0
+SV_ERR_WORKSPACE = 10
 SV_DTYPE_BF16, SV_DTYPE_F32 = 0, 1
 SV_MASK_CAUSAL, SV_MASK_TREE = 0, 1
 STATUS_NAMES = {
@@ -29,8 +30,8 @@ STATUS_NAMES = {
 }
 
 EXPORTS = ("sv_kv_append", "sv_spec_verify_attn_workspace_bytes", "sv_spec_verify_attn",
-           "sv_spec_rejection_sample", "sv_tree_greedy_accept", "sv_kv_rollback", "sv_status_string",
-           "sv_version", "sv_set_option")
+           "sv_spec_verify_attn_no_alloc", "sv_spec_rejection_sample", "sv_tree_greedy_accept", "sv_kv_rollback",
+           "sv_status_string", "sv_version", "sv_set_option")
 SV_OPT_ATTN_PATH = 1
 ATTN_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "warp_mma": 3}
 
@@ -75,6 +76,7 @@ def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CD
             "sv_kv_append": (I, [KVP, P, P, P, I, P, P]),
             "sv_spec_verify_attn_workspace_bytes": (S, [KVP, I, I, I, I]),
             "sv_spec_verify_attn": (I, [KVP, P, P, P, I, I, I, I, F, I, P, P, S, P, P]),
+            "sv_spec_verify_attn_no_alloc": (I, [KVP, P, P, P, I, I, I, I, F, I, P, P, P]),
             "sv_spec_rejection_sample": (I, [P, P, I, I, I, P, I, I, P, P, P, F, P, P, P, P, P]),
             "sv_tree_greedy_accept": (I, [P, I, I, I, P, I, I, P, P, P, P, P, P, P, P]),
             "sv_kv_rollback": (I, [KVP, P, P, P, I, P, P]),
@@ -180,6 +182,24 @@ def spec_verify_attn(kv: PagedKV, q: torch.Tensor, out: torch.Tensor, cu_q: torc
                                       int(q.shape[0]), int(max_q), int(max_seq_len), float(scale), int(mask_kind),
                                       _ptr(tree_mask), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)),
            "sv_spec_verify_attn")
+
+
+# size of the static scratch behind spec_verify_attn_no_alloc (SV_ATTN_NO_ALLOC_SCRATCH_BYTES)
+ATTN_NO_ALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def spec_verify_attn_no_alloc(kv: PagedKV, q: torch.Tensor, out: torch.Tensor, cu_q: torch.Tensor, *, max_q: int,
+                              max_seq_len: int, scale: float, mask_kind: int = SV_MASK_CAUSAL,
+                              tree_mask: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                              stream=None) -> None:
+    """spec_verify_attn for callers that cannot allocate device memory: the
+    split-KV scratch is a static array inside the library, shared by every
+    call on a device (calls that overlap on the GPU race on it)."""
+    s = kv.struct()
+    _check(load().sv_spec_verify_attn_no_alloc(ctypes.byref(s), _ptr(q), _ptr(out), _ptr(cu_q), int(q.shape[1]),
+                                               int(q.shape[0]), int(max_q), int(max_seq_len), float(scale),
+                                               int(mask_kind), _ptr(tree_mask), _ptr(status), _stream(stream)),
+           "sv_spec_verify_attn_no_alloc")
 
 
 def spec_rejection_sample(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor], cu_q: torch.Tensor,
