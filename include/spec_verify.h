@@ -129,9 +129,11 @@ sv_status sv_kv_append(const sv_paged_kv *kv, const void *new_k, const void *new
                        int32_t total_q, int32_t *status_dev, void *stream);
 
 /*
- * Workspace bytes sv_spec_verify_attn needs for these sizes (split-KV partial
- * results: per split, query row and query head, head_dim floats plus one
- * log-sum-exp). max_seq_len bounds c_b + n_b over the batch.
+ * Workspace bytes sv_spec_verify_attn needs for these sizes: the split-KV
+ * partial results (head_dim floats plus one log-sum-exp per partial row) of
+ * whichever kernel the call may select, and for the tcgen05 kernel the
+ * per-sequence tile prefix. max_seq_len bounds c_b + n_b over the batch;
+ * max_q_per_seq bounds n_b. Returns 0 for invalid sizes.
  */
 size_t sv_spec_verify_attn_workspace_bytes(const sv_paged_kv *kv, int32_t num_q_heads, int32_t total_q,
                                            int32_t max_q_per_seq, int32_t max_seq_len);
@@ -152,7 +154,8 @@ size_t sv_spec_verify_attn_workspace_bytes(const sv_paged_kv *kv, int32_t num_q_
  *   tree_mask   uint64 [total_q] for SV_MASK_TREE, else NULL
  *   max_seq_len an upper bound of c_b + n_b (sizes the launch; a longer
  *               sequence sets SV_ERR_BAD_LENGTH and its rows are not written)
- *   workspace   device scratch of at least sv_spec_verify_attn_workspace_bytes
+ *   workspace   device scratch of at least sv_spec_verify_attn_workspace_bytes,
+ *               256-byte aligned; its contents need no initialisation
  *   status_dev  int32 [1] or NULL
  * Block ids outside [0, num_blocks) set SV_ERR_BAD_BLOCK_ID; the rows of that
  * sequence are then undefined, no out-of-bounds memory is touched.

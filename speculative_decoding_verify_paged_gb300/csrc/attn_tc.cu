@@ -52,7 +52,6 @@ constexpr int kNtO = kColsPerWarp / 8;                 // n8 tiles of columns pe
 static_assert(kConsumerWarps == 4 || kConsumerWarps == 8, "4 or 8 consumer warps");
 constexpr int kStageBytes = 2 * kTile * kD * 2;  // K and V
 constexpr int kHalfBytes = kTile * 128;          // 64 rows x 128 bytes (half of head_dim)
-constexpr long long kSpinLimit = 1LL << 24;  // try_wait polls before a wait gives up
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -68,18 +67,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 // Bounded wait for the phase with the given parity; false after the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kSpinLimit; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(

@@ -1,5 +1,5 @@
-// Split-KV paged attention on the 5th-generation tensor cores (tcgen05 + TMEM)
-// for bf16 caches with head_dim 128.
+// Persistent split-KV paged attention on the 5th-generation tensor cores
+// (tcgen05 + TMEM) for bf16 caches with head_dim 128.
 //
 // What it computes is the attention of the verify pass ("Speculative decoding
 // and continuous batching in practice", sec. 1.2: the target scores all K+1
@@ -10,30 +10,45 @@
 // committed tokens, key t is visible if t < c, or if new row j = t - c is
 // visible to row i (j <= i causal; bit j of the row's tree mask).
 //
-// One CTA = one sequence x one KV head x one split of its keys x up to 128
-// query rows (the G query heads of the KV head times the sequence's rows, one
-// row per TMEM lane). Six warps:
-//  * warp 0, producer: TMA of 32-key K and V tiles into a 6-stage ring. The
-//    pool is viewed as a 3-D tensor (64 elements, rows, 2 halves of
-//    head_dim) so that one 128-byte-swizzled box brings both halves of a
-//    group of R = min(block_size, 32) rows: a tile is 32/R groups, each
-//    stored [half 0 | half 1]; block ids are read 32 at a time;
+// Work. A unit is one sequence x one KV head x one block of up to 128 query
+// rows (the G query heads of the KV head times the sequence's rows; one row
+// per TMEM lane); its keys form ceil(L / 32) tiles. Two CTAs run per SM. The
+// tiles of all units, laid end to end (sequence, KV head, row block order),
+// are cut into equal contiguous ranges, one per CTA, so that every CTA
+// streams the same number of tiles within one. A range holds whole units,
+// whose rows the CTA writes itself, and at its two ends pieces of units it
+// shares with its neighbours: such a piece leaves its normalised partial
+// output and log-sum-exp in one of the CTA's two workspace slots (slot 0 for
+// the range's first piece, slot 1 for its last), and attn_umma_combine merges
+// them. Each CTA finds its range with a block scan over the sequences; CTA 0
+// also stores the per-sequence tile prefix for the combine.
+//
+// Six warps per CTA, each walking the same pieces in the same order:
+//  * warp 0, producer: TMA of 32-key K and V tiles into a 6-stage ring that
+//    runs on across unit boundaries. The pool is viewed as a 3-D tensor (64
+//    elements, rows, 2 halves of head_dim) so that one 128-byte-swizzled box
+//    brings both halves of a group of R = min(block_size, 32) rows: a tile is
+//    32/R groups, each stored [half 0 | half 1]; block ids are read 32 at a
+//    time;
 //  * warp 1, MMA issuer (one lane) and TMEM owner: S(t) = Q K(t)^T with
 //    tcgen05.mma kind::f16 (M = 128 rows, N = R keys per group, K = 128; A = Q
 //    in TMEM, B = K K-major in shared memory) into one of two TMEM S buffers,
-//    then
-//    O += P(t-1) V(t-1) (A = P in TMEM, B = V MN-major in shared memory,
-//    N = 128); tcgen05.commit frees the K/V stage and signals the softmax;
-//  * warps 2-5, softmax and epilogue: thread = query row = TMEM lane. Each
-//    first stores its row of Q into TMEM (the tensor core then reads Q from
-//    TMEM instead of shared memory), reads its row of S(t) (tcgen05.ld),
-//    masks edge tiles, keeps a running
-//    maximum that moves only when the tile maximum exceeds it by more than
-//    2^8 (then O is rescaled in TMEM), writes P = 2^(s - m) as bf16 over S
-//    (tcgen05.st), and at the end reads O, divides by the row sum and stores
-//    the row (or the split's partial result and log-sum-exp).
+//    then O += P(t-1) V(t-1) (A = P in TMEM, B = V MN-major in shared memory,
+//    N = 128; the first tile of a piece overwrites O); tcgen05.commit frees
+//    the K/V stage and signals the softmax. Before the first S of a piece it
+//    waits for that unit's Q;
+//  * warps 2-5, softmax and epilogue: thread = query row = TMEM lane. They
+//    store the unit's Q rows into TMEM (the next unit's as soon as the last S
+//    of the current one has landed, its loads issued one tile earlier), read
+//    S(t) (tcgen05.ld), mask edge tiles, keep a running maximum that moves
+//    only when the tile maximum exceeds it by more than 2^8 (then O is
+//    rescaled in TMEM), write P = 2^(s - m) as bf16 over S (tcgen05.st), and
+//    at the end of a piece read O, divide by the row sum and store the rows or
+//    the partial result.
 // All mbarrier waits are bounded; a wait that gives up records SV_ERR_TIMEOUT.
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "sv_internal.cuh"
 
@@ -43,7 +58,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kTile = 32;                       // keys per tile
 constexpr int kStages = 6;
-constexpr int kRowsMax = 128;                   // query rows per CTA (TMEM lanes)
+constexpr int kRowsMax = 128;                   // query rows per unit (TMEM lanes)
 constexpr int kSoftWarps = 4;
 constexpr int kThreads = (2 + kSoftWarps) * 32;
 constexpr int kHalfBytes = kTile * 128;         // 32 keys x 128 bytes (half of head_dim)
@@ -52,7 +67,7 @@ constexpr int kTmemCols = 256;                  // S0 [0,32) S1 [32,64) O [64,19
 constexpr int kColO = 64;
 constexpr int kColQ = 192;
 constexpr float kRescaleThreshold = 8.f;        // log2 units
-constexpr long long kSpinLimit = 1LL << 24;
+constexpr int kCtasPerSm = 2;                   // TMEM: 2 x 256 columns; shared memory: 2 x ~100 KB
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -66,24 +81,15 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kSpinLimit; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
-// One box of the (64 elements, rows, 2 halves) view: R rows, both halves.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
+// One box of the (64 elements, 8 rows, 2 halves, row groups) view: R rows
+// starting at row y (a multiple of 8), both halves, as R/8 groups of
+// [half 0: 8 rows x 128 B][half 1: 8 rows x 128 B].
 __device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap *map, int y, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
           dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(0), "r"(bar)
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(y >> 3), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -155,42 +161,129 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 2^x by the MUFU approximation (flush-to-zero): softmax weights only, rounded to bf16 next
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
 }
 struct UmmaParams {
   AttnArgs a;
-  int box_rows;    // rows per TMA box (a group): min(block_size, 32), 16 or 32
-  int row_blocks;  // CTAs per (sequence, KV head, split) along the query rows
+  int box_rows;     // rows per TMA box (a group): min(block_size, 32), 16 or 32
+  int G;            // query heads per KV head
+  int rows_cap;     // rows of a workspace slot: min(128, G * max_q)
+  int rb_max;       // row blocks of the longest sequence: ceil(G * max_q / 128)
+  int ctas;         // CTAs of the launch
+  float *part_o;    // [ctas][2][rows_cap][128] normalised partial outputs
+  float *part_lse;  // [ctas][2][rows_cap] their log-sum-exp (base 2)
+  int *prefix;      // [batch + 1]: first tile of each sequence's units; [batch] = all tiles
 };
 
-__global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                                                                const __grid_constant__ CUtensorMap tmap_v,
-                                                                const UmmaParams P) {
+// One sequence as the work decomposition sees it; tiles == 0: nothing to do.
+struct Seq {
+  int c, row0, n, L;
+  int rbs;    // row blocks: ceil(G n / 128)
+  int tiles;  // key tiles of each of its units: ceil(L / 32)
+};
+
+__device__ __forceinline__ Seq load_seq(const UmmaParams &P, int b, bool *bad) {
   const AttnArgs &a = P.a;
   const KV &kv = a.kv;
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / P.row_blocks, rb = blockIdx.y % P.row_blocks;
-  const int b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  Seq s;
+  s.c = kv.seq_lens[b];
+  s.row0 = a.cu_q[b];
+  s.n = a.cu_q[b + 1] - s.row0;
+  const long long L = (long long)s.c + s.n;
+  const bool ok = s.c >= 0 && s.n >= 0 && s.n <= a.max_q && s.row0 >= 0 &&
+                  (long long)s.row0 + s.n <= a.total_q && L <= a.max_seq_len &&
+                  L <= (long long)kv.max_blocks * kv.block_size;
+  *bad = !ok;
+  s.L = ok ? (int)L : 0;
+  s.rbs = ok ? (P.G * s.n + kRowsMax - 1) / kRowsMax : 0;
+  s.tiles = (ok && s.rbs > 0) ? (s.L + kTile - 1) / kTile : 0;
+  return s;
+}
+__device__ __forceinline__ int seq_work(const UmmaParams &P, const Seq &s) {
+  return P.a.kv.num_kv_heads * s.rbs * s.tiles;
+}
 
-  const int c = kv.seq_lens[b];
-  const int row0 = a.cu_q[b];
-  const int n = a.cu_q[b + 1] - row0;
-  const int L = c + n;
-  if (L > a.max_seq_len || c < 0 || n < 0 || row0 + n > a.total_q || L > kv.max_blocks * kv.block_size) {
-    if (split == 0 && blockIdx.y == 0 && tid == 0) record(a.status, SV_ERR_BAD_LENGTH);
-    return;
+// Inclusive sum over the CTA's threads; *total gets the sum over all of them.
+__device__ __forceinline__ int block_scan(int v, int *sh, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  const int nsplit = (L + a.chunk - 1) / a.chunk;
-  if (split >= nsplit) return;
-  const int G = a.num_q_heads / kv.num_kv_heads;
-  const int R = G * n;
-  const int rbase = rb * kRowsMax;
-  if (rbase >= R) return;
-  const int kb = split * a.chunk, ke = min(L, kb + a.chunk);
-  const int ntiles = (ke - kb + kTile - 1) / kTile;
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int t = sh[w];
+    before += w < warp ? t : 0;
+    all += t;
+  }
+  __syncthreads();
+  *total = all;
+  return x + before;
+}
+
+// The part of one unit that lies in a CTA's tile range.
+struct Piece {
+  int b, kvh, rb, c, row0, n, L;
+  int kt0, kt1;  // key tiles [kt0, kt1) of the unit
+  bool whole;    // the piece is the whole unit
+};
+
+// Walks the tile range [g, end) piece by piece, sequence b starting at global tile `base`.
+struct Walker {
+  int b, base, g, end;
+  Seq s;
+  __device__ __forceinline__ bool next(const UmmaParams &P, Piece &p) {
+    if (g >= end) return false;
+    int work = seq_work(P, s);
+    while (g - base >= work) {
+      if (b + 1 >= P.a.kv.batch) {  // cannot happen while the lengths stay put; never read past the batch
+        g = end;
+        return false;
+      }
+      base += work;
+      ++b;
+      bool bad;
+      s = load_seq(P, b, &bad);
+      work = seq_work(P, s);
+    }
+    const int local = g - base;
+    const int j = local / s.tiles, off = local - j * s.tiles;
+    const int len = min(s.tiles - off, end - g);
+    p.b = b;
+    p.kvh = j / s.rbs;
+    p.rb = j - p.kvh * s.rbs;
+    p.c = s.c;
+    p.row0 = s.row0;
+    p.n = s.n;
+    p.L = s.L;
+    p.kt0 = off;
+    p.kt1 = off + len;
+    p.whole = off == 0 && len == s.tiles;
+    g += len;
+    return true;
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                                                         const __grid_constant__ CUtensorMap tmap_v,
+                                                                         const UmmaParams P) {
+  const AttnArgs &a = P.a;
+  const KV &kv = a.kv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = kv.batch;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -200,8 +293,11 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
   uint64_t *s_full = empty + kStages;  // [2] S(t) in TMEM buffer t % 2
   uint64_t *p_ready = s_full + 2;      // [2] P(t) written over buffer t % 2
   uint64_t *o_bar = p_ready + 2;       // one phase per finished P V
-  uint64_t *q_ready = o_bar + 1;       // Q rows stored in TMEM
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_ready + 1);
+  uint64_t *q_ready = o_bar + 1;       // one phase per unit whose Q rows are in TMEM
+  uint64_t *mma_done = q_ready + 1;    // every MMA issued has finished
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  __shared__ int sh_scan[kThreads / 32];
+  __shared__ int sh_first_b, sh_first_base, sh_err;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -214,7 +310,11 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
     }
     mbar_init(smem_u32(o_bar), 1);
     mbar_init(smem_u32(q_ready), kSoftWarps);
+    mbar_init(smem_u32(mma_done), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    sh_first_b = 0;
+    sh_first_base = 0;
+    sh_err = 0;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -222,136 +322,197 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+
+  // ---- this CTA's tile range [g0, g1) of the W tiles of the launch ----
+  int mine = 0;
+  for (int b = tid; b < B; b += kThreads) {
+    bool bad;
+    const Seq s = load_seq(P, b, &bad);
+    if (bad && blockIdx.x == 0) record(a.status, SV_ERR_BAD_LENGTH);
+    mine += seq_work(P, s);
+  }
+  int W;
+  block_scan(mine, sh_scan, &W);
+  const int per = max(1, (W + P.ctas - 1) / P.ctas);
+  const int g0 = min(W, (int)blockIdx.x * per), g1 = min(W, g0 + per);
+  int run = 0;
+  for (int b0 = 0; b0 < B; b0 += kThreads) {  // the sequence holding tile g0; CTA 0 also stores the prefix
+    const int b = b0 + tid;
+    int v = 0;
+    if (b < B) {
+      bool bad;
+      v = seq_work(P, load_seq(P, b, &bad));
+    }
+    int tot;
+    const int excl = run + block_scan(v, sh_scan, &tot) - v;
+    if (blockIdx.x == 0 && b < B) P.prefix[b] = excl;
+    if (v > 0 && excl <= g0 && g0 < excl + v) {
+      sh_first_b = b;
+      sh_first_base = excl;
+    }
+    run += tot;
+    if (blockIdx.x != 0 && run > g0) break;  // uniform: run and g0 are the same in every thread
+  }
+  if (blockIdx.x == 0 && tid == 0) P.prefix[B] = W;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  Walker walker;
+  walker.b = sh_first_b;
+  walker.base = sh_first_base;
+  walker.g = g0;
+  walker.end = g1;
+  {
+    bool bad;
+    walker.s = load_seq(P, walker.b, &bad);
+  }
   bool ok = true;
+  int issued = 0;  // producer: tiles whose loads were issued
 
   if (warp == 0) {
     // ================= producer =================
     const int bs = kv.block_size, box = P.box_rows;
     const uint32_t box_bytes = static_cast<uint32_t>(box) * 256;
-    const int lb_first = kb / bs, lb_last = (ke - 1) / bs;
-    const int32_t *bt = kv.block_table + (size_t)b * kv.max_blocks;
-    auto load_id = [&](int lb) -> int {
-      if (lb > lb_last) return -1;
-      const int id = bt[lb];
-      if (id < 0 || id >= kv.num_blocks) {
-        record(a.status, SV_ERR_BAD_BLOCK_ID);
-        return -1;
-      }
-      return id;
-    };
-    int wbase = lb_first;
-    int cur = load_id(wbase + lane);
-    int nxt = load_id(wbase + 32 + lane);
-    for (int t = 0; t < ntiles && ok; ++t) {
-      const int s = t % kStages;
-      if (t >= kStages && !mbar_wait(smem_u32(&empty[s]), ((t / kStages) - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      const int kt = kb + t * kTile;
-      int ids[kTile / 16];
-      int nbox = 0;
-      for (int r = 0; r < kTile; r += box) {
-        const int tok = kt + r;
-        int id = -1;
-        if (tok < ke) {
-          const int lb = tok / bs;
-          while (lb >= wbase + 32) {  // warp-uniform
-            wbase += 32;
-            cur = nxt;
-            nxt = load_id(wbase + 32 + lane);
-          }
-          id = __shfl_sync(0xffffffffu, cur, lb - wbase);
+    Piece p;
+    while (ok && walker.next(P, p)) {
+      const int kb = p.kt0 * kTile, ke = min(p.L, p.kt1 * kTile);
+      const int lb_last = (ke - 1) / bs;
+      const int32_t *bt = kv.block_table + (size_t)p.b * kv.max_blocks;
+      auto load_id = [&](int lb) -> int {
+        if (lb > lb_last) return -1;
+        const int id = bt[lb];
+        if (id < 0 || id >= kv.num_blocks) {
+          record(a.status, SV_ERR_BAD_BLOCK_ID);
+          return -1;
         }
-        ids[r / box] = id;
-        nbox += id >= 0;
-      }
-      if (lane == 0) {
-        const uint32_t fb = smem_u32(&full[s]);
-        mbar_expect_tx(fb, static_cast<uint32_t>(nbox) * 2u * box_bytes);
-        const uint32_t kdst = smem_u32(stages + s * kStageBytes);
-        const uint32_t vdst = kdst + 2 * kHalfBytes;
+        return id;
+      };
+      int wbase = kb / bs;
+      int cur = load_id(wbase + lane);
+      int nxt = load_id(wbase + 32 + lane);
+      for (int kt = p.kt0; kt < p.kt1; ++kt, ++issued) {
+        const int s = issued % kStages;
+        if (issued >= kStages) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), ((issued / kStages) - 1) & 1));
+        if (!ok) break;
+        const int k0 = kt * kTile;
+        int ids[kTile / 16];
+        int nbox = 0;
         for (int r = 0; r < kTile; r += box) {
-          const int id = ids[r / box];
-          if (id < 0) continue;
-          const int tok = kt + r;
-          const int y = (id * kv.num_kv_heads + kvh) * bs + (tok % bs);
-          const uint32_t off = static_cast<uint32_t>(r) * 256;  // group of `box` rows, both halves
-          tma_load_rows(kdst + off, &tmap_k, y, fb);
-          tma_load_rows(vdst + off, &tmap_v, y, fb);
+          const int tok = k0 + r;
+          int id = -1;
+          if (tok < ke) {
+            const int lb = tok / bs;
+            while (lb >= wbase + 32) {  // warp-uniform
+              wbase += 32;
+              cur = nxt;
+              nxt = load_id(wbase + 32 + lane);
+            }
+            id = __shfl_sync(0xffffffffu, cur, lb - wbase);
+          }
+          ids[r / box] = id;
+          nbox += id >= 0;
         }
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_expect_tx(fb, static_cast<uint32_t>(nbox) * 2u * box_bytes);
+          const uint32_t kdst = smem_u32(stages + s * kStageBytes);
+          const uint32_t vdst = kdst + 2 * kHalfBytes;
+          for (int r = 0; r < kTile; r += box) {
+            const int id = ids[r / box];
+            if (id < 0) continue;
+            const int tok = k0 + r;
+            const int y = (id * kv.num_kv_heads + p.kvh) * bs + (tok % bs);
+            const uint32_t off = static_cast<uint32_t>(r) * 256;  // group of `box` rows, both halves
+            tma_load_rows(kdst + off, &tmap_k, y, fb);
+            tma_load_rows(vdst + off, &tmap_v, y, fb);
+          }
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
-    const int R = P.box_rows;            // rows per group: 16 or 32
-    const uint32_t idesc_s = mma_idesc(128, R, 0);
+    const int R = P.box_rows;  // rows per group: 16 or 32
+    const uint32_t idesc_s = mma_idesc(128, kTile, 0);
     constexpr uint32_t idesc_o = mma_idesc(128, kD, 1);
-    const uint32_t half_bytes = static_cast<uint32_t>(R) * 128;  // one half of a group
-    auto issue_pv = [&](int u) {  // O += P(u) V(u), 16 keys per MMA
+    (void)R;
+    auto issue_pv = [&](int u, bool accumulate) {  // O (+)= P(u) V(u), 16 keys per MMA
       const int su = u % kStages;
       const uint32_t v_base = smem_u32(stages + su * kStageBytes) + 2 * kHalfBytes;
       const uint32_t p_col = tmem + (u & 1) * kTile;
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const int grp = (kk * 16) / R, sub = ((kk * 16) % R) / 16;
-        const uint32_t start = v_base + grp * 2 * half_bytes + sub * 2048;
-        mma_ts(tmem + kColO, p_col + kk * 8, smem_desc(start, half_bytes, 1024), idesc_o, (u > 0 || kk > 0) ? 1 : 0);
-      }
+      for (int kk = 0; kk < kTile / 16; ++kk)  // keys 16 kk .. 16 kk + 15: two 8-key groups of 2 KB
+        mma_ts(tmem + kColO, p_col + kk * 8, smem_desc(v_base + kk * 4096, 1024, 2048), idesc_o,
+               (accumulate || kk > 0) ? 1 : 0);
       mma_commit(smem_u32(&empty[su]));
       mma_commit(smem_u32(o_bar));
     };
-    ok = mbar_wait(smem_u32(q_ready), 0);
-    tc_fence_after();
-    for (int t = 0; t <= ntiles && ok; ++t) {
-      if (t < ntiles) {
+    int t = 0, piece = 0;
+    int pend = -1;  // P V of tile t - 1 still to issue: -1 none, 0 overwrite O, 1 accumulate
+    Piece p;
+    while (ok && walker.next(P, p)) {
+      for (int kt = p.kt0; kt < p.kt1; ++kt, ++t) {
         const int s = t % kStages;
-        ok = mbar_wait(smem_u32(&full[s]), (t / kStages) & 1);
+        bool w = mbar_wait(smem_u32(&full[s]), (t / kStages) & 1);
+        if (w && kt == p.kt0) w = mbar_wait(smem_u32(q_ready), piece & 1);
+        ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t k_base = smem_u32(stages + s * kStageBytes);
-          for (int grp = 0; grp < kTile / R; ++grp) {
-            const uint32_t kg = k_base + grp * 2 * half_bytes;
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
-              mma_ts(tmem + (t & 1) * kTile + grp * R, tmem + kColQ + kk * 8,
-                     smem_desc(kg + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024), idesc_s, kk > 0 ? 1 : 0);
-          }
+          for (int kk = 0; kk < kD / 16; ++kk)  // 8-key groups 2 KB apart, half kk / 4 at +1 KB
+            mma_ts(tmem + (t & 1) * kTile, tmem + kColQ + kk * 8,
+                   smem_desc(k_base + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048), idesc_s, kk > 0 ? 1 : 0);
           mma_commit(smem_u32(&s_full[t & 1]));
         }
         __syncwarp();
+        if (pend >= 0) {
+          const int u = t - 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_ready[u & 1]), (u >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) issue_pv(u, pend == 1);
+          __syncwarp();
+        }
+        pend = kt != p.kt0 ? 1 : 0;
       }
-      if (t > 0) {
-        const int u = t - 1;
-        ok = mbar_wait(smem_u32(&p_ready[u & 1]), (u >> 1) & 1);
-        if (!ok) break;
+      ++piece;
+    }
+    if (ok && pend >= 0) {
+      const int u = t - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_ready[u & 1]), (u >> 1) & 1));
+      if (ok) {
         tc_fence_after();
-        if (lane == 0) issue_pv(u);
+        if (lane == 0) issue_pv(u, pend == 1);
         __syncwarp();
       }
     }
+    // every MMA issued finishes before TMEM is released
+    if (lane == 0) mma_commit(smem_u32(mma_done));
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(mma_done), 0))) ok = false;
   } else {
     // ================= softmax, one query row per thread =================
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
-    const int row = q4 * 32 + lane;          // row within the CTA = TMEM lane
-    const int r = rbase + row;
-    const bool live = r < R;
-    const int i = live ? r / G : 0;
-    const uint64_t tm = (live && a.mask_kind == SV_MASK_TREE) ? a.tree_mask[row0 + i] : 0ull;
+    const int row = q4 * 32 + lane;          // row within the unit's row block = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
-    const bool warp_live = __any_sync(0xffffffffu, live);
-    if (warp_live) {
-      // this lane's query row into TMEM columns [kColQ, kColQ + 64): bf16 pairs, zeros for padding rows
-      uint32_t qr[64];
+    const __nv_bfloat16 *qsrc = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+    // query row (i, head g) of this lane in piece p; false for a padding lane
+    auto row_of = [&](const Piece &p, int &i, int &g) -> bool {
+      const int r = p.rb * kRowsMax + row;
+      const bool live = r < P.G * p.n;
+      i = live ? r / P.G : 0;
+      g = live ? r - i * P.G : 0;
+      return live;
+    };
+    // this lane's Q row of piece p as bf16 pairs (zeros for a padding lane)
+    auto load_q = [&](const Piece &p, uint32_t (&qr)[64]) -> bool {
+      int i, g;
+      const bool live = row_of(p, i, g);
       if (live) {
-        const uint4 *qp = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.q) +
-                                                          ((size_t)(row0 + i) * a.num_q_heads + kvh * G + r % G) * kD);
+        const uint4 *qp = reinterpret_cast<const uint4 *>(qsrc + ((size_t)(p.row0 + i) * a.num_q_heads + p.kvh * P.G + g) * kD);
 #pragma unroll
         for (int v = 0; v < 16; ++v) {
           const uint4 x = qp[v];
@@ -364,150 +525,247 @@ __global__ void __launch_bounds__(kThreads, 2) attn_umma_kernel(const __grid_con
 #pragma unroll
         for (int v = 0; v < 64; ++v) qr[v] = 0u;
       }
-      tmem_st64(lane_addr + kColQ, qr);
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(q_ready));
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int t = 0; t < ntiles; ++t) {
-      const int kt = kb + t * kTile;
-      const int valid = min(kTile, ke - kt);
-      ok = mbar_wait(smem_u32(&s_full[t & 1]), (t >> 1) & 1);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      if (valid < kTile) {
-        // zero this tile's V rows past the split's end before P V reads them
-        uint8_t *vst = stages + (t % kStages) * kStageBytes + 2 * kHalfBytes;
-        const int R = P.box_rows;
-        for (int x = (warp - 2) * 32 + lane; x < (kTile - valid) * 16; x += kSoftWarps * 32) {
-          const int rr = valid + (x >> 4), ch = x & 15;
-          const int grp = rr / R, rin = rr % R;
-          *reinterpret_cast<uint4 *>(vst + grp * 2 * R * 128 + (ch >> 3) * R * 128 + rin * 128 + (ch & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async();
+      return live;
+    };
+    // the next unit's Q row into L2 while this unit's last S is awaited
+    auto prefetch_q = [&](const Piece &p) {
+      int i, g;
+      if (row_of(p, i, g)) {
+        const char *qp = reinterpret_cast<const char *>(qsrc + ((size_t)(p.row0 + i) * a.num_q_heads + p.kvh * P.G + g) * kD);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qp));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qp + 128));
       }
-      if (warp_live) {
-        uint32_t sr[32];
-        tmem_ld32(lane_addr + (t & 1) * kTile, sr);
-        tmem_wait_ld();
-        const bool edge = (kt + kTile > c) || (valid < kTile);
-        float sv[32];
-#pragma unroll
-        for (int k = 0; k < kTile; ++k) {
-          float v = __uint_as_float(sr[k]) * a.scale_log2;
-          if (edge) {
-            const int key = kt + k;
-            bool vis = live && key < ke;
-            if (vis && key >= c) {
-              const int j = key - c;
-              vis = (a.mask_kind == SV_MASK_CAUSAL) ? (j <= i) : (j < 64 && ((tm >> j) & 1ull));
-            }
-            if (!vis) v = -INFINITY;
-          }
-          if (!live) v = -INFINITY;
-          sv[k] = v;
-        }
-        float mx;
-        {
-          float t16[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) t16[k] = fmaxf(sv[k], sv[k + 16]);
-#pragma unroll
-          for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) t16[k] = fmaxf(t16[k], t16[k + w]);
-          mx = t16[0];
-        }
-        // move the running maximum only when the tile's exceeds it by the threshold
-        const bool move = mx > m_run + kRescaleThreshold || (m_run == -INFINITY && mx != -INFINITY);
-        if (__any_sync(0xffffffffu, move && l_run > 0.f)) {
-          // O must be rescaled: wait for P(t-1) V(t-1), then scale this lane's row
-          if (t > 0 && !mbar_wait(smem_u32(o_bar), (t - 1) & 1)) ok = false;
-          tc_fence_after();
-          const float f = (move && l_run > 0.f) ? exp2f(m_run - mx) : 1.f;
-#pragma unroll
-          for (int cb = 0; cb < kD / 32; ++cb) {
-            uint32_t o[32];
-            tmem_ld32(lane_addr + kColO + cb * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-            tmem_st32(lane_addr + kColO + cb * 32, o);
-          }
-          tmem_wait_st();
-        }
-        if (move) {
-          l_run = (l_run > 0.f) ? l_run * exp2f(m_run - mx) : l_run;
-          m_run = mx;
-        }
-        const float ref = (m_run == -INFINITY) ? 0.f : m_run;
-        uint32_t pr[kTile / 2];
-        float ps[kTile / 2];
-#pragma unroll
-        for (int k = 0; k < kTile / 2; ++k) {
-          const float p0 = exp2f(sv[2 * k] - ref), p1 = exp2f(sv[2 * k + 1] - ref);
-          ps[k] = p0 + p1;
-          pr[k] = pack_bf16(p0, p1);
-        }
-#pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-          for (int k = 0; k < w; ++k) ps[k] += ps[k + w];
-        l_run += ps[0];
-        tmem_st16(lane_addr + (t & 1) * kTile, pr);
+    };
+    auto store_q = [&](const uint32_t (&qr)[64], bool live) {
+      if (__any_sync(0xffffffffu, live)) {
+        tmem_st64(lane_addr + kColQ, qr);
         tmem_wait_st();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_ready[t & 1]));
+      if (lane == 0) mbar_arrive(smem_u32(q_ready));
+    };
+    Piece cur, nxt;
+    bool has_cur = walker.next(P, cur);
+    bool has_nxt = has_cur && walker.next(P, nxt);
+    if (has_cur) {
+      uint32_t qr[64];
+      store_q(qr, load_q(cur, qr));
     }
-    // ---- epilogue: wait for the last P V, then write the row ----
-    // S(t) is issued before P(t-1) V(t-1), so seeing S(ntiles-1) proves only
-    // that P V up to ntiles-3 finished: o_bar may still be in the phase of
-    // ntiles-2, and a parity wait for ntiles-1 alone would pass early there.
-    if (ok && ntiles > 1) ok = mbar_wait(smem_u32(o_bar), (ntiles - 2) & 1);
-    if (ok && ntiles > 0) ok = mbar_wait(smem_u32(o_bar), (ntiles - 1) & 1);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
-    if (ok && warp_live) {
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const int g = live ? r % G : 0;
-      const size_t qrow = (size_t)(row0 + i) * a.num_q_heads + kvh * G + g;
+    int t = 0;
+    bool first_piece = true;
+    while (has_cur && ok) {
+      int i, g;
+      const bool live = row_of(cur, i, g);
+      const uint64_t tm = (live && a.mask_kind == SV_MASK_TREE) ? a.tree_mask[cur.row0 + i] : 0ull;
+      const bool warp_live = __any_sync(0xffffffffu, live);
+      const int c = cur.c, ke = min(cur.L, cur.kt1 * kTile);
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int kt = cur.kt0; kt < cur.kt1; ++kt, ++t) {
+        const bool handoff = kt == cur.kt1 - 1 && has_nxt;
+        if (handoff) prefetch_q(nxt);
+        const int k0 = kt * kTile;
+        const int valid = min(kTile, ke - k0);
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t & 1]), (t >> 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        // S(t) was this unit's last product with its Q: the next unit's rows can take its place
+        if (handoff) {
+          uint32_t qr[64];
+          store_q(qr, load_q(nxt, qr));
+        }
+        if (valid < kTile) {
+          // zero this tile's V rows past the unit's end before P V reads them
+          uint8_t *vst = stages + (t % kStages) * kStageBytes + 2 * kHalfBytes;
+          for (int x = (warp - 2) * 32 + lane; x < (kTile - valid) * 16; x += kSoftWarps * 32) {
+            const int rr = valid + (x >> 4), ch = x & 15;
+            *reinterpret_cast<uint4 *>(vst + (rr >> 3) * 2048 + (ch >> 3) * 1024 + (rr & 7) * 128 + (ch & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+        if (warp_live) {
+          uint32_t sr[32];
+          tmem_ld32(lane_addr + (t & 1) * kTile, sr);
+          tmem_wait_ld();
+          // scores in log2 units; only the last tiles of a unit (new rows, ragged end) need
+          // the mask. Padding lanes (no query row) score against a zero Q row: finite values
+          // whose P V rows are never stored.
+          const bool edge = (k0 + kTile > c) || (valid < kTile);  // warp-uniform
+          float sv[32];
+          if (!edge) {
 #pragma unroll
-      for (int cb = 0; cb < kD / 32; ++cb) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + kColO + cb * 32, o);
-        tmem_wait_ld();
-        if (!live) continue;
-        if (nsplit == 1) {
-          uint4 *op = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + qrow * kD + cb * 32);
+            for (int k = 0; k < kTile; ++k) sv[k] = __uint_as_float(sr[k]) * a.scale_log2;
+          } else {
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            op[v] = make_uint4(pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
-                               pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
-                               pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
-                               pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
-        } else {
-          const size_t prow = (size_t)split * a.total_q * a.num_q_heads + qrow;
-          float4 *op = reinterpret_cast<float4 *>(a.ws_o + prow * kD + cb * 32);
+            for (int k = 0; k < kTile; ++k) {
+              const int key = k0 + k;
+              bool vis = key < ke;
+              if (vis && key >= c) {
+                const int j = key - c;
+                vis = (a.mask_kind == SV_MASK_CAUSAL) ? (j <= i) : (j < 64 && ((tm >> j) & 1ull));
+              }
+              sv[k] = vis ? __uint_as_float(sr[k]) * a.scale_log2 : -INFINITY;
+            }
+          }
+          float mx;
+          {
+            float t16[16];
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            op[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
-          if (cb == 0) a.ws_lse[prow] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+            for (int k = 0; k < 16; ++k) t16[k] = fmaxf(sv[k], sv[k + 16]);
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+              for (int k = 0; k < w; ++k) t16[k] = fmaxf(t16[k], t16[k + w]);
+            mx = t16[0];
+          }
+          // move the running maximum only when the tile's exceeds it by the threshold
+          const bool move = mx > m_run + kRescaleThreshold || (m_run == -INFINITY && mx != -INFINITY);
+          if (__any_sync(0xffffffffu, move && l_run > 0.f)) {
+            // O must be rescaled: wait for P(t-1) V(t-1) (S(t) done means P V up to t-2 is),
+            // then scale this lane's row
+            if (!mbar_wait(smem_u32(o_bar), (t - 1) & 1)) ok = false;
+            tc_fence_after();
+            const float f = (move && l_run > 0.f) ? exp2f(m_run - mx) : 1.f;
+#pragma unroll
+            for (int cb = 0; cb < kD / 32; ++cb) {
+              uint32_t o[32];
+              tmem_ld32(lane_addr + kColO + cb * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+              tmem_st32(lane_addr + kColO + cb * 32, o);
+            }
+            tmem_wait_st();
+          }
+          if (move) {
+            l_run = (l_run > 0.f) ? l_run * exp2f(m_run - mx) : l_run;
+            m_run = mx;
+          }
+          const float ref = (m_run == -INFINITY) ? 0.f : m_run;
+          uint32_t pr[kTile / 2];
+          float ps[kTile / 2];
+#pragma unroll
+          for (int k = 0; k < kTile / 2; ++k) {
+            const float p0 = fast_exp2(sv[2 * k] - ref), p1 = fast_exp2(sv[2 * k + 1] - ref);
+            ps[k] = p0 + p1;
+            pr[k] = pack_bf16(p0, p1);
+          }
+#pragma unroll
+          for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) ps[k] += ps[k + w];
+          l_run += ps[0];
+          tmem_st16(lane_addr + (t & 1) * kTile, pr);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_ready[t & 1]));
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      // ---- end of the piece: wait for its last P V, then write ----
+      // S(tl) is issued before P(tl-1) V(tl-1), so seeing S(tl) proves only that
+      // P V up to tl-2 finished: o_bar may still be in the phase of tl-1, where a
+      // parity wait for tl alone would pass early.
+      const int tl = t - 1;
+      bool w = tl < 1 || mbar_wait(smem_u32(o_bar), (tl - 1) & 1);
+      if (w) w = mbar_wait(smem_u32(o_bar), tl & 1);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      if (warp_live) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const size_t qrow = (size_t)(cur.row0 + i) * a.num_q_heads + cur.kvh * P.G + g;
+        const size_t slot = ((size_t)blockIdx.x * 2 + (first_piece ? 0 : 1)) * P.rows_cap + row;
+#pragma unroll
+        for (int cb = 0; cb < kD / 32; ++cb) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + kColO + cb * 32, o);
+          tmem_wait_ld();
+          if (!live) continue;
+          if (cur.whole) {
+            uint4 *op = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + qrow * kD + cb * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              op[v] = make_uint4(pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
+                                 pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
+                                 pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
+                                 pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
+          } else {
+            float4 *op = reinterpret_cast<float4 *>(P.part_o + slot * kD + cb * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              op[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                  __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+            if (cb == 0) P.part_lse[slot] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+          }
         }
       }
+      first_piece = false;
+      cur = nxt;
+      has_cur = has_nxt;
+      has_nxt = has_cur && walker.next(P, nxt);
     }
   }
-  if (!ok && lane == 0) record(a.status, SV_ERR_TIMEOUT);
+  if (!ok) {
+    if (lane == 0) record(a.status, SV_ERR_TIMEOUT);
+    sh_err = 1;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (sh_err != 0 && warp == 0 && lane == 0) {
+    // after a failed wait, let this CTA's copies in flight land before its shared memory is released
+    for (int k = max(0, issued - kStages); k < issued; ++k) mbar_wait(smem_u32(&full[k % kStages]), (k / kStages) & 1);
+  }
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+// Merges the partial results of every unit that two or more CTAs shared; one
+// warp per query row, four head_dim elements per lane.
+__global__ void __launch_bounds__(128) attn_umma_combine(const UmmaParams P) {
+  const AttnArgs &a = P.a;
+  const int b = blockIdx.x, kvh = blockIdx.y / P.rb_max, rb = blockIdx.y % P.rb_max;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool bad;
+  const Seq s = load_seq(P, b, &bad);
+  if (s.tiles == 0 || rb >= s.rbs) return;
+  const int W = P.prefix[a.kv.batch];
+  const int per = max(1, (W + P.ctas - 1) / P.ctas);
+  const int T0 = P.prefix[b] + (kvh * s.rbs + rb) * s.tiles, T1 = T0 + s.tiles;
+  const int c0 = T0 / per, c1 = (T1 - 1) / per;
+  if (c0 == c1) return;  // one CTA held the whole unit and wrote its rows
+  // CTA c0 holds the unit as its first piece (slot 0) only when the unit starts its range
+  const int slot0 = T0 == c0 * per ? 0 : 1;
+  const int rows = min(kRowsMax, P.G * s.n - rb * kRowsMax);
+  for (int row = warp; row < rows; row += 4) {
+    float M = -INFINITY;
+    for (int cc = c0; cc <= c1; ++cc) {
+      const size_t slot = ((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * P.rows_cap + row;
+      M = fmaxf(M, P.part_lse[slot]);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    if (M != -INFINITY) {
+      for (int cc = c0; cc <= c1; ++cc) {
+        const size_t slot = ((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * P.rows_cap + row;
+        const float w = exp2f(P.part_lse[slot] - M);
+        const float4 o = *reinterpret_cast<const float4 *>(P.part_o + slot * kD + lane * 4);
+        den += w;
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int r = rb * kRowsMax + row, i = r / P.G, g = r - i * P.G;
+    const size_t qrow = (size_t)(s.row0 + i) * a.num_q_heads + kvh * P.G + g;
+    *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + qrow * kD + lane * 4) =
+        make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+  }
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -531,18 +789,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// The pool as a 3-D tensor: (64 elements of a half row, rows, 2 halves) with
-// strides (256 B per row, 128 B per half); a box of R rows lands as
-// [half 0: R rows x 128 B][half 1: R rows x 128 B], 128-byte swizzled.
+// The pool as a 4-D tensor: (64 elements of a half row, 8 rows, 2 halves,
+// groups of 8 rows) with strides (256 B per row, 128 B per half, 2 KB per
+// group); a box of R rows lands as R/8 groups of [half 0: 8 rows x 128 B]
+// [half 1: 8 rows x 128 B], 128-byte swizzled: every 1 KB is one swizzle
+// atom, and the atoms of one half are 2 KB apart across the whole tile.
 bool make_map(CUtensorMap *map, void *pool, const KV &kv, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t rows = (cuuint64_t)kv.num_blocks * kv.num_kv_heads * kv.block_size;
-  const cuuint64_t gdim[3] = {64, rows, 2};
-  const cuuint64_t gstride[2] = {(cuuint64_t)kD * 2, 128};
-  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
-  const cuuint32_t estride[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool, gdim, gstride, box, estride,
+  const cuuint64_t gdim[4] = {64, 8, 2, rows / 8};
+  const cuuint64_t gstride[3] = {(cuuint64_t)kD * 2, 128, (cuuint64_t)kD * 2 * 8};
+  const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)box_rows / 8};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pool, gdim, gstride, box, estride,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -551,6 +811,26 @@ bool make_map(CUtensorMap *map, void *pool, const KV &kv, int box_rows) {
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 32 * 8;
 static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "a third CTA per SM would wait for TMEM");
 
+struct UmmaLayout {
+  int ctas, rows_cap, rb_max;
+  size_t lse_offset, prefix_offset, bytes;  // byte offsets in the workspace, and its size
+};
+
+UmmaLayout umma_layout(const KV &kv, int num_q_heads, int max_q, int max_seq_len) {
+  UmmaLayout l;
+  const int G = num_q_heads / kv.num_kv_heads;
+  const long long max_tiles =
+      (long long)kv.batch * kv.num_kv_heads * ((G * max_q + kRowsMax - 1) / kRowsMax) * ((max_seq_len + kTile - 1) / kTile);
+  l.ctas = (int)std::max(1LL, std::min<long long>((long long)kCtasPerSm * num_sms(), max_tiles));
+  l.rows_cap = std::min(kRowsMax, G * max_q);
+  l.rb_max = (G * max_q + kRowsMax - 1) / kRowsMax;
+  const size_t slots = (size_t)l.ctas * 2 * l.rows_cap;
+  l.lse_offset = slots * kD * sizeof(float);
+  l.prefix_offset = (l.lse_offset + slots * sizeof(float) + 255) / 256 * 256;
+  l.bytes = l.prefix_offset + ((size_t)kv.batch + 1) * sizeof(int);
+  return l;
+}
+
 }  // namespace
 
 bool attn_umma_supported(const KV &kv) {
@@ -558,20 +838,41 @@ bool attn_umma_supported(const KV &kv) {
          encode_fn() != nullptr && ((uintptr_t)kv.k_pool % 16 == 0) && ((uintptr_t)kv.v_pool % 16 == 0);
 }
 
-cudaError_t launch_attn_umma(const AttnArgs &a, cudaStream_t st) {
+bool attn_umma_fits(const KV &kv, int num_q_heads, int max_q, int max_seq_len) {
+  const int G = num_q_heads / kv.num_kv_heads;
+  const long long max_tiles =
+      (long long)kv.batch * kv.num_kv_heads * ((G * max_q + kRowsMax - 1) / kRowsMax) * ((max_seq_len + kTile - 1) / kTile);
+  return max_tiles < (1LL << 30);
+}
+
+size_t attn_umma_workspace_bytes(const KV &kv, int num_q_heads, int max_q, int max_seq_len) {
+  return umma_layout(kv, num_q_heads, max_q, max_seq_len).bytes;
+}
+
+cudaError_t launch_attn_umma(const AttnArgs &a, void *workspace, size_t workspace_bytes, cudaStream_t st) {
   if (a.kv.batch == 0) return cudaSuccess;
+  const UmmaLayout l = umma_layout(a.kv, a.num_q_heads, a.max_q, a.max_seq_len);
+  if (workspace == nullptr || workspace_bytes < l.bytes || (uintptr_t)workspace % 256 != 0)
+    return cudaErrorInvalidValue;
   UmmaParams p;
   p.a = a;
   p.box_rows = a.kv.block_size < kTile ? a.kv.block_size : kTile;
-  const int G = a.num_q_heads / a.kv.num_kv_heads;
-  p.row_blocks = (G * a.max_q + kRowsMax - 1) / kRowsMax;
+  p.G = a.num_q_heads / a.kv.num_kv_heads;
+  p.rows_cap = l.rows_cap;
+  p.rb_max = l.rb_max;
+  p.ctas = l.ctas;
+  p.part_o = reinterpret_cast<float *>(workspace);
+  p.part_lse = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + l.lse_offset);
+  p.prefix = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(workspace) + l.prefix_offset);
   CUtensorMap mk, mv;
   if (!make_map(&mk, a.kv.k_pool, a.kv, p.box_rows) || !make_map(&mv, a.kv.v_pool, a.kv, p.box_rows))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.max_splits, a.kv.num_kv_heads * p.row_blocks, a.kv.batch);
-  attn_umma_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, p);
+  attn_umma_kernel<<<p.ctas, kThreads, kSmemBytes, st>>>(mk, mv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_umma_combine<<<dim3(a.kv.batch, a.kv.num_kv_heads * p.rb_max), 128, 0, st>>>(p);
   return cudaGetLastError();
 }
 

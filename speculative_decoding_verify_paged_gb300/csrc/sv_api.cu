@@ -1,5 +1,6 @@
 // extern "C" entry points of libspecverify: argument checks, launch planning
 // and dispatch. Nothing here allocates device memory or synchronises.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -75,11 +76,25 @@ sv_status check_kv(const sv_paged_kv *kv, bool need_free) {
 
 sv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
 
-size_t attn_workspace(const sv_paged_kv *kv, int32_t num_q_heads, int32_t total_q, int32_t max_seq_len) {
+// Whether the tcgen05 kernel can take these sizes.
+bool umma_usable(const sv_paged_kv *kv, int32_t num_q_heads, int32_t max_q, int32_t max_seq_len) {
+  return kv->dtype == SV_DTYPE_BF16 && attn_umma_supported(make_kv(*kv)) &&
+         attn_umma_fits(make_kv(*kv), num_q_heads, max_q, max_seq_len);
+}
+
+// Workspace of whichever kernel a call may select: the split-KV partials of the
+// CUDA-core and mma.sync kernels, or the tcgen05 kernel's slots and tile prefix.
+size_t attn_workspace(const sv_paged_kv *kv, int32_t num_q_heads, int32_t total_q, int32_t max_q,
+                      int32_t max_seq_len) {
   const SplitPlan p = plan_splits(kv->batch, kv->num_kv_heads, max_seq_len, kGranule);
-  if (p.max_splits <= 1) return 0;
-  const size_t rows = (size_t)p.max_splits * total_q * num_q_heads;
-  return rows * (size_t)kv->head_dim * sizeof(float) + rows * sizeof(float) + 256;
+  size_t need = 0;
+  if (p.max_splits > 1) {
+    const size_t rows = (size_t)p.max_splits * total_q * num_q_heads;
+    need = rows * (size_t)kv->head_dim * sizeof(float) + rows * sizeof(float) + 256;
+  }
+  if (kv->batch > 0 && umma_usable(kv, num_q_heads, max_q, max_seq_len))
+    need = std::max(need, attn_umma_workspace_bytes(make_kv(*kv), num_q_heads, max_q, max_seq_len));
+  return need;
 }
 
 }  // namespace
@@ -127,9 +142,10 @@ sv_status sv_kv_append(const sv_paged_kv *kv, const void *new_k, const void *new
 
 size_t sv_spec_verify_attn_workspace_bytes(const sv_paged_kv *kv, int32_t num_q_heads, int32_t total_q,
                                            int32_t max_q_per_seq, int32_t max_seq_len) {
-  (void)max_q_per_seq;
-  if (kv == nullptr || num_q_heads <= 0 || total_q < 0 || max_seq_len <= 0) return 0;
-  return attn_workspace(kv, num_q_heads, total_q, max_seq_len);
+  if (kv == nullptr || num_q_heads <= 0 || kv->num_kv_heads <= 0 || num_q_heads % kv->num_kv_heads != 0 ||
+      total_q < 0 || max_q_per_seq < 1 || max_q_per_seq > kMaxQ || max_seq_len <= 0)
+    return 0;
+  return attn_workspace(kv, num_q_heads, total_q, max_q_per_seq, max_seq_len);
 }
 
 sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, const int32_t *cu_q,
@@ -147,8 +163,9 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
   if (q == nullptr || out == nullptr || cu_q == nullptr || !aligned16(q) || !aligned16(out))
     return SV_ERR_INVALID_ARG;
   if (kv->head_dim % 32 != 0) return SV_ERR_UNSUPPORTED;
-  const size_t need = attn_workspace(kv, num_q_heads, total_q, max_seq_len);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))) return SV_ERR_WORKSPACE;
+  const size_t need = attn_workspace(kv, num_q_heads, total_q, max_q_per_seq, max_seq_len);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || ((uintptr_t)workspace & 255u) != 0))
+    return SV_ERR_WORKSPACE;
 
   const SplitPlan p = plan_splits(kv->batch, kv->num_kv_heads, max_seq_len, kGranule);
   AttnArgs a;
@@ -170,20 +187,21 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
   a.mask_kind = mask_kind;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = (cudaStream_t)stream;
-  const bool umma_ok = kv->dtype == SV_DTYPE_BF16 && attn_umma_supported(a.kv);
+  const bool umma_ok = umma_usable(kv, num_q_heads, max_q_per_seq, max_seq_len);
   const bool mma_ok = kv->dtype == SV_DTYPE_BF16 && attn_tc_supported(a.kv, num_q_heads, max_q_per_seq);
   cudaError_t e;
   switch (g_attn_path) {
     case SV_ATTN_CUDA_CORES: e = launch_attn_simt(a, kv->dtype, st); break;
     case SV_ATTN_TENSOR_CORES:
       if (!umma_ok) return SV_ERR_UNSUPPORTED;
-      e = launch_attn_umma(a, st);
-      break;
+      return cuda_status(launch_attn_umma(a, workspace, workspace_bytes, st));
     case SV_ATTN_WARP_MMA:
       if (!mma_ok) return SV_ERR_UNSUPPORTED;
       e = launch_attn_tc(a, st);
       break;
-    default: e = umma_ok ? launch_attn_umma(a, st) : launch_attn_simt(a, kv->dtype, st);
+    default:
+      if (umma_ok) return cuda_status(launch_attn_umma(a, workspace, workspace_bytes, st));
+      e = launch_attn_simt(a, kv->dtype, st);
   }
   if (e != cudaSuccess) return SV_ERR_CUDA;
   return cuda_status(launch_attn_combine(a, kv->dtype, st));

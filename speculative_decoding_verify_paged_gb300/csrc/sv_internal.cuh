@@ -32,6 +32,38 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------------------
+// bounded mbarrier wait: gives up (returns false) once it has waited about
+// kWaitBudgetNs of wall-clock time (globaltimer), so that a kernel whose
+// barrier phase never completes ends within a second instead of spinning on
+// ---------------------------------------------------------------------------
+constexpr unsigned long long kWaitBudgetNs = 500ull * 1000 * 1000;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  unsigned long long deadline = 0;
+  for (uint32_t i = 0; i < (1u << 30); ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 63u) == 63u) {
+      const unsigned long long now = global_ns();
+      if (deadline == 0) deadline = now + kWaitBudgetNs;
+      else if (now > deadline) return false;
+    }
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------------------
 // plain-data views of the ABI struct, passed by value to kernels
 // ---------------------------------------------------------------------------
 struct KV {
@@ -95,7 +127,10 @@ cudaError_t launch_attn_combine(const AttnArgs &a, int dtype, cudaStream_t st);
 bool attn_tc_supported(const KV &kv, int num_q_heads, int max_q);
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
 bool attn_umma_supported(const KV &kv);
-cudaError_t launch_attn_umma(const AttnArgs &a, cudaStream_t st);
+bool attn_umma_fits(const KV &kv, int num_q_heads, int max_q, int max_seq_len);
+size_t attn_umma_workspace_bytes(const KV &kv, int num_q_heads, int max_q, int max_seq_len);
+// launches the persistent tcgen05 kernel and its combine (workspace: attn_umma_workspace_bytes, 256-aligned)
+cudaError_t launch_attn_umma(const AttnArgs &a, void *workspace, size_t workspace_bytes, cudaStream_t st);
 
 struct SamplerArgs {
   const void *tgt;
