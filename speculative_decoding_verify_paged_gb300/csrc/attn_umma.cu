@@ -372,60 +372,63 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
 
   if (warp == 0) {
     // ================= producer =================
+    // block_size is a power of two: logical blocks and row offsets by shift and mask
     const int bs = kv.block_size, box = P.box_rows;
+    const int bs_shift = __ffs(bs) - 1;
     const uint32_t box_bytes = static_cast<uint32_t>(box) * 256;
     Piece p;
     while (ok && walker.next(P, p)) {
       const int kb = p.kt0 * kTile, ke = min(p.L, p.kt1 * kTile);
-      const int lb_last = (ke - 1) / bs;
+      const int lb_last = (ke - 1) >> bs_shift;
       const int32_t *bt = kv.block_table + (size_t)p.b * kv.max_blocks;
-      auto load_id = [&](int lb) -> int {
+      // first pool row of logical block lb for this KV head; -1 past the piece or for a bad id
+      auto load_y = [&](int lb) -> int {
         if (lb > lb_last) return -1;
         const int id = bt[lb];
         if (id < 0 || id >= kv.num_blocks) {
           record(a.status, SV_ERR_BAD_BLOCK_ID);
           return -1;
         }
-        return id;
+        return (id * kv.num_kv_heads + p.kvh) << bs_shift;
       };
-      int wbase = kb / bs;
-      int cur = load_id(wbase + lane);
-      int nxt = load_id(wbase + 32 + lane);
+      int wbase = kb >> bs_shift;  // lane l holds logical block wbase + l (cur) and wbase + 32 + l (nxt)
+      int cur = load_y(wbase + lane);
+      int nxt = load_y(wbase + 32 + lane);
       for (int kt = p.kt0; kt < p.kt1; ++kt, ++issued) {
         const int s = issued % kStages;
         if (issued >= kStages) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), ((issued / kStages) - 1) & 1));
         if (!ok) break;
         const int k0 = kt * kTile;
-        int ids[kTile / 16];
+        int ys[kTile / 16];
         int nbox = 0;
-        for (int r = 0; r < kTile; r += box) {
-          const int tok = k0 + r;
-          int id = -1;
-          if (tok < ke) {
-            const int lb = tok / bs;
+#pragma unroll
+        for (int j = 0; j < kTile / 16; ++j) {
+          const int tok = k0 + j * box;
+          int y = -1;
+          if (j * box < kTile && tok < ke) {
+            const int lb = tok >> bs_shift;
             while (lb >= wbase + 32) {  // warp-uniform
               wbase += 32;
               cur = nxt;
-              nxt = load_id(wbase + 32 + lane);
+              nxt = load_y(wbase + 32 + lane);
             }
-            id = __shfl_sync(0xffffffffu, cur, lb - wbase);
+            const int yb = __shfl_sync(0xffffffffu, cur, lb - wbase);
+            y = yb < 0 ? -1 : yb + (tok & (bs - 1));
           }
-          ids[r / box] = id;
-          nbox += id >= 0;
+          ys[j] = y;
+          nbox += y >= 0;
         }
         if (lane == 0) {
           const uint32_t fb = smem_u32(&full[s]);
           mbar_expect_tx(fb, static_cast<uint32_t>(nbox) * 2u * box_bytes);
           const uint32_t kdst = smem_u32(stages + s * kStageBytes);
           const uint32_t vdst = kdst + 2 * kHalfBytes;
-          for (int r = 0; r < kTile; r += box) {
-            const int id = ids[r / box];
-            if (id < 0) continue;
-            const int tok = k0 + r;
-            const int y = (id * kv.num_kv_heads + p.kvh) * bs + (tok % bs);
-            const uint32_t off = static_cast<uint32_t>(r) * 256;  // group of `box` rows, both halves
-            tma_load_rows(kdst + off, &tmap_k, y, fb);
-            tma_load_rows(vdst + off, &tmap_v, y, fb);
+#pragma unroll
+          for (int j = 0; j < kTile / 16; ++j) {
+            if (ys[j] < 0) continue;
+            const uint32_t off = static_cast<uint32_t>(j * box) * 256;  // group of `box` rows, both halves
+            tma_load_rows(kdst + off, &tmap_k, ys[j], fb);
+            tma_load_rows(vdst + off, &tmap_v, ys[j], fb);
           }
         }
         __syncwarp();
@@ -834,7 +837,10 @@ UmmaLayout umma_layout(const KV &kv, int num_q_heads, int max_q, int max_seq_len
 }  // namespace
 
 bool attn_umma_supported(const KV &kv) {
+  // TMA row coordinates are 32-bit: the pool's rows (blocks x KV heads x block_size) must fit
+  const long long rows = (long long)kv.num_blocks * kv.num_kv_heads * kv.block_size;
   return kv.elem_bytes == 2 && kv.head_dim == kD && kv.block_size >= 16 && kv.block_size <= 256 &&
+         (kv.block_size & (kv.block_size - 1)) == 0 && rows < (1LL << 31) &&
          encode_fn() != nullptr && ((uintptr_t)kv.k_pool % 16 == 0) && ((uintptr_t)kv.v_pool % 16 == 0);
 }
 
