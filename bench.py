@@ -325,10 +325,10 @@ def run_native(args):
         "tokens_per_s": emitted * world / (elapsed_ms / 1e3),
         "scored_tokens_per_s": sp.total_q * args.steps * world / (elapsed_ms / 1e3),
         "mean_tokens_per_seq_step": emitted / (B * args.steps),
-        "roofline": {"kernel": "spec_verify_attn (tcgen05 split-KV attention + combine)", "bound": "hbm",
+        "roofline": {"kernel": "spec_verify_attn (persistent tcgen05 attention + combine)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS, "peak_source": peak_kind,
-                     "traffic": (traffic["bytes_per_launch_scaled"] if traffic else None),
+                     "traffic": (traffic["traffic_per_algorithmic_byte"] * attn_bytes_avg if traffic else None),
                      "algorithmic_bytes_per_launch": attn_bytes_avg, "avg_launch_ms": attn_ms_avg,
                      "tflops": fl / args.steps / (attn_ms_avg / 1e3) / 1e12},
         "sampler_roofline": {"kernel": "spec_rejection_sample", "bound": "hbm",
