@@ -14,25 +14,30 @@
 //
 // How: the vocabulary is cut into C equal chunks, one per CTA of the cluster.
 //   phase 1  every CTA streams its chunk of every row of the sequence (target
-//            rows and draft rows) once; a work item is 4 KB of one row for
-//            one warp (eight 16-byte loads in flight per lane), reduced to a
-//            (max, sum of 2^((l - max) log2(e)/T)) pair, or to an argmax.
+//            rows and draft rows) once; a work item is 2 KB of one row for one
+//            warp, and each warp has its next item's loads in flight while it
+//            reduces the current one to a (max, sum of 2^((l - max) log2(e)/T))
+//            pair, or to an argmax.
 //   phase 2  cluster barrier; every CTA combines the C partial results of
-//            every row through distributed shared memory in rank order, so all
-//            CTAs hold identical row statistics and take identical decisions.
+//            every row through distributed shared memory with a fixed shuffle
+//            tree (one lane per rank), so all CTAs hold identical row
+//            statistics and take identical decisions.
 //   phase 3  (T > 0) the row pair of the draw (target and draft row a, or the
-//            bonus row) is re-read. With a 128K vocabulary the residual CDF
-//            has intervals of ~1e-5, so this phase is exact where fp32 would
-//            not be: exponents carry log2(e)/T as a hi+lo pair, the weights
-//            are summed in 64-bit fixed point (2^-40 units, order-free and
-//            exact), the draft normaliser enters as the ratio Z_t/Z_d in
-//            hi+lo form, and the target is the integer floor(u' * S). Pass A
-//            sums the two normalisers, pass B each CTA's residual mass, and
-//            after a cluster barrier the prefix over ranks picks the CTA
-//            holding the crossing, which rescans its chunk (pass C).
+//            bonus row) is copied once into shared memory. With a 128K
+//            vocabulary the residual CDF has intervals of ~1e-5, so this phase
+//            is exact where fp32 would not be: exponents carry log2(e)/T as a
+//            hi+lo pair, the weights are summed in 64-bit fixed point (2^-40
+//            units, order-free and exact), the draft normaliser enters as the
+//            ratio Z_t/Z_d in hi+lo form, and the target is the integer
+//            floor(u' * S). Pass A sums the two normalisers, pass B each
+//            8-element group's residual mass (kept in shared memory) and each
+//            CTA's total; after a cluster barrier the prefix over ranks picks
+//            the CTA holding the crossing, which scans its group masses and
+//            recomputes the one group that holds it.
 // All reductions run in a fixed order, so results are deterministic.
 #include <cooperative_groups.h>
 
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 
@@ -47,17 +52,19 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxQ = 64;
 constexpr int kMaxRows = 2 * kMaxQ;  // target + draft rows of one sequence
-constexpr int kMaxSub = 16;          // work items per row per CTA
 constexpr int kMaxChunk = 16384;     // vocabulary elements per CTA
-constexpr int kGroup = 8;            // phase 3: consecutive elements per thread
-constexpr int kSeg = kThreads * kGroup;
+constexpr int kGroup = 8;            // consecutive elements of a group
+constexpr int kMaxSub = 32;          // phase 1 work items per row per CTA
 
-// Work-item geometry: LOADS loads of N elements per lane.
+// Phase 1 work item: one warp, LOADS loads of N elements per lane (2 KB).
 template <typename T, bool VEC> struct ItemCfg;
-template <> struct ItemCfg<__nv_bfloat16, true> { static constexpr int N = 8, LOADS = 8; };
-template <> struct ItemCfg<float, true> { static constexpr int N = 4, LOADS = 8; };
-template <typename T> struct ItemCfg<T, false> { static constexpr int N = 1, LOADS = 32; };
-template <typename T, bool VEC> __host__ __device__ constexpr int item_elems() { return 32 * ItemCfg<T, VEC>::N * ItemCfg<T, VEC>::LOADS; }
+template <> struct ItemCfg<__nv_bfloat16, true> { static constexpr int N = 8, LOADS = 4; };
+template <> struct ItemCfg<float, true> { static constexpr int N = 4, LOADS = 4; };
+template <typename T> struct ItemCfg<T, false> { static constexpr int N = 1, LOADS = 16; };
+template <typename T, bool VEC> __host__ __device__ constexpr int item_elems() {
+  return 32 * ItemCfg<T, VEC>::N * ItemCfg<T, VEC>::LOADS;
+}
+static_assert(kMaxChunk / item_elems<float, true>() <= kMaxSub, "phase 1 items per row");
 
 template <typename T, bool VEC> struct Raw;
 template <typename T> struct Raw<T, true> { uint4 v; };
@@ -87,6 +94,13 @@ __device__ __forceinline__ void load_item(const T *__restrict__ row, int e0, int
   }
 }
 
+// 2^x by the MUFU approximation (flush-to-zero; relative error about 2^-22)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // (max, sum) pair combine: m is a raw logit maximum, s = sum 2^((l - m) * coef);
 // m == -inf means "empty".
 __device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2, float coef) {
@@ -96,7 +110,7 @@ __device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s
     s = 0.f;
     return;
   }
-  s = s * exp2f((m - mn) * coef) + s2 * exp2f((m2 - mn) * coef);
+  s = s * fast_exp2((m - mn) * coef) + s2 * fast_exp2((m2 - mn) * coef);
   m = mn;
 }
 
@@ -115,7 +129,7 @@ __device__ __forceinline__ float exp2_acc(float d, float c_hi, float c_lo) {
   const float xh = d * c_hi;
   if (!(xh > -160.f)) return 0.f;  // -inf logits and underflow
   const float xe = fmaf(d, c_hi, -xh) + d * c_lo;
-  return exp2f(xh) * fmaf(xe, 0.69314718055994531f, 1.0f);
+  return fast_exp2(xh) * fmaf(xe, 0.69314718055994531f, 1.0f);
 }
 
 // Weights in [0, 1] as 64-bit fixed point with 40 fractional bits: sums of up
@@ -156,35 +170,35 @@ __device__ long long block_excl_scan_ll(long long x, long long *buf, long long *
   return before + inc - x;
 }
 
-// Eight consecutive logits e .. e+7 of a row as floats; -inf past `hi`.
-template <typename T, bool VEC>
-__device__ __forceinline__ void load8(const T *__restrict__ row, int e, int hi, float (&x)[kGroup]) {
-  if (VEC && e + kGroup <= hi) {
-    if constexpr (sizeof(T) == 2) {
-      const uint4 r = __ldg(reinterpret_cast<const uint4 *>(row + e));
-      const T *t = reinterpret_cast<const T *>(&r);
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// The eight elements of group g of a shared-memory copy of a chunk, as floats;
+// -inf at and past element n.
+template <typename T>
+__device__ __forceinline__ void group8(const T *buf, int g, int n, float (&x)[kGroup]) {
+  const int e = g * kGroup;
+  if constexpr (sizeof(T) == 2) {
+    const uint4 r = *reinterpret_cast<const uint4 *>(buf + e);
+    const T *t = reinterpret_cast<const T *>(&r);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] = to_f32(t[k]);
-    } else {
-      const uint4 r0 = __ldg(reinterpret_cast<const uint4 *>(row + e));
-      const uint4 r1 = __ldg(reinterpret_cast<const uint4 *>(row + e + 4));
-      const float *f0 = reinterpret_cast<const float *>(&r0), *f1 = reinterpret_cast<const float *>(&r1);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        x[k] = f0[k];
-        x[k + 4] = f1[k];
-      }
-    }
+    for (int k = 0; k < kGroup; ++k) x[k] = (e + k < n) ? to_f32(t[k]) : -INFINITY;
   } else {
+    const uint4 r0 = *reinterpret_cast<const uint4 *>(buf + e);
+    const uint4 r1 = *reinterpret_cast<const uint4 *>(buf + e + 4);
+    const float *f0 = reinterpret_cast<const float *>(&r0), *f1 = reinterpret_cast<const float *>(&r1);
 #pragma unroll
-    for (int k = 0; k < kGroup; ++k) x[k] = (e + k < hi) ? to_f32(row[e + k]) : -INFINITY;
+    for (int k = 0; k < 4; ++k) {
+      x[k] = (e + k < n) ? f0[k] : -INFINITY;
+      x[k + 4] = (e + k + 4 < n) ? f1[k] : -INFINITY;
+    }
   }
 }
 
 struct Smem {
-  float pm[kMaxRows][kMaxSub];  // per item: raw max, or best value
-  float ps[kMaxRows][kMaxSub];  // per item: sum of exp2, or best index (as int bits)
-  float rm[kMaxRows];           // per row, this CTA's chunk (cluster-visible)
+  uint64_t pair;  // phase 3 row pair
+  float rm[kMaxRows];  // per row, this CTA's chunk (cluster-visible)
   float rs[kMaxRows];
   int ri[kMaxRows];
   float tl[kMaxQ];  // target logit of the draft token, if this CTA owns it (cluster-visible)
@@ -200,12 +214,12 @@ struct Smem {
   float rho_hi, rho_lo;
   int a;
   int bad;
-  int y_min, y_last;
   int owner, fallback;
+  int y_hit, y_last;
 };
 
 template <typename T, bool VEC, int MODE>
-__global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
+__global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int ring_bytes) {
   constexpr int IE = item_elems<T, VEC>();
   constexpr int LOADS = ItemCfg<T, VEC>::LOADS, N = ItemCfg<T, VEC>::N;
   cg::cluster_group cluster = cg::this_cluster();
@@ -214,6 +228,12 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
   const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ Smem sm;
+  extern __shared__ __align__(128) uint8_t dyn[];
+  // phase 1: per-item partials [kMaxRows][kMaxSub] x 2; phase 3: the row pair (same bytes)
+  uint8_t *ring = dyn;
+  float *pm = reinterpret_cast<float *>(dyn);
+  float *ps = pm + kMaxRows * kMaxSub;
+  long long *gmass = reinterpret_cast<long long *>(dyn + ring_bytes);  // phase 3: per-group mass
 
   const int V = args.vocab;
   const int t0 = args.cu_q[b];
@@ -222,7 +242,6 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
   const int d0 = t0 - b;
   const int lo = min(V, rank * args.chunk), hi = min(V, lo + args.chunk);
   const int len = hi - lo;
-  const int nsub = (len + IE - 1) / IE;
   const int rows = (MODE == kStochastic) ? n + K : n;
   const T *tgt = reinterpret_cast<const T *>(args.tgt);
   const T *drf = reinterpret_cast<const T *>(args.drf);
@@ -234,20 +253,63 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
     if (rank == 0 && tid == 0) record(args.status, SV_ERR_BAD_LENGTH);
     return;
   }
-  if (tid == 0) sm.bad = 0;
+  if (tid == 0) {
+    sm.bad = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pair)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   __syncthreads();
+  bool ok = true;  // false after a bounded wait gave up: the remaining work is skipped, barriers are kept
 
   // ---------------- phase 1: per-item partial statistics ----------------
-  int bad = 0;
+  // warp w takes items w, w + 8, ...; the next item's loads are in flight while
+  // the current one is reduced
+  const int nsub = (len + IE - 1) / IE;
   const int items = rows * nsub;
-  for (int it = warp; it < items; it += kWarps) {
-    const int r = it / nsub, s = it % nsub;
-    const T *row = (r < n) ? tgt + (size_t)(t0 + r) * V : drf + (size_t)(d0 + (r - n)) * V;
-    const int e0 = lo + s * IE, e1 = min(hi, e0 + IE);
-    Raw<T, VEC> raw[LOADS];
-    int nv;
-    load_item<T, VEC>(row, e0, e1, lane, raw, nv);
-    if constexpr (MODE == kStochastic) {
+  int bad = 0;
+  auto reduce_item = [&](int it, const Raw<T, VEC> (&raw)[LOADS], int nv) {
+    const int r = it / nsub, sub = it % nsub;
+    const int e0 = lo + sub * IE;
+    if constexpr (MODE == kStochastic && VEC && sizeof(T) == 2) {
+      // bf16 pairs: the maximum on packed pairs (NaN propagates, so one test of the
+      // item maximum catches NaN and +inf), then sum 2^(x c - m c) with one unpack per half
+      const __nv_bfloat162 ninf2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+      __nv_bfloat162 mx2 = ninf2;
+#pragma unroll
+      for (int u = 0; u < LOADS; ++u)
+        if (u < nv) {
+          const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw[u].v);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mx2 = __hmax2_nan(mx2, h[k]);
+        }
+      float m = fmaxf(__low2float(mx2), __high2float(mx2));
+      if (__low2float(mx2) != __low2float(mx2) || __high2float(mx2) != __high2float(mx2)) m = NAN;
+      bad |= (m != m) | (m == INFINITY);
+      float sum = 0.f;
+      if (m != -INFINITY && m == m) {
+        const float nmc = -m * coef;
+#pragma unroll
+        for (int u = 0; u < LOADS; ++u)
+          if (u < nv) {
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(&raw[u].v);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              sum += fast_exp2(fmaf(__uint_as_float(w[k] << 16), coef, nmc));
+              sum += fast_exp2(fmaf(__uint_as_float(w[k] & 0xffff0000u), coef, nmc));
+            }
+          }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+        ms_combine(m, sum, m2, s2, coef);
+      }
+      if (lane == 0) {
+        pm[r * kMaxSub + sub] = m;
+        ps[r * kMaxSub + sub] = sum;
+      }
+    } else if constexpr (MODE == kStochastic) {
       float m = -INFINITY;  // raw logit maximum (exact)
 #pragma unroll
       for (int u = 0; u < LOADS; ++u)
@@ -260,11 +322,12 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
           }
       float sum = 0.f;
       if (m != -INFINITY) {
+        const float nmc = -m * coef;
 #pragma unroll
         for (int u = 0; u < LOADS; ++u)
           if (u < nv)
 #pragma unroll
-            for (int k = 0; k < N; ++k) sum += exp2f((elem<T, VEC>(raw[u], k) - m) * coef);
+            for (int k = 0; k < N; ++k) sum += fast_exp2(fmaf(elem<T, VEC>(raw[u], k), coef, nmc));
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -273,8 +336,8 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
         ms_combine(m, sum, m2, s2, coef);
       }
       if (lane == 0) {
-        sm.pm[r][s] = m;
-        sm.ps[r][s] = sum;
+        pm[r * kMaxSub + sub] = m;
+        ps[r * kMaxSub + sub] = sum;
       }
     } else {
       float best = 0.f;
@@ -295,9 +358,47 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
         am_combine(best, bi, v2, i2);
       }
       if (lane == 0) {
-        sm.pm[r][s] = best;
-        sm.ps[r][s] = __int_as_float(bi);
+        pm[r * kMaxSub + sub] = best;
+        ps[r * kMaxSub + sub] = __int_as_float(bi);
       }
+    }
+  };
+  auto fetch = [&](int it, Raw<T, VEC> (&raw)[LOADS], int &nv) {
+    const int r = it / nsub, sub = it % nsub;
+    const T *row = (r < n) ? tgt + (size_t)(t0 + r) * V : drf + (size_t)(d0 + (r - n)) * V;
+    const int e0 = lo + sub * IE;
+    load_item<T, VEC>(row, e0, min(hi, e0 + IE), lane, raw, nv);
+  };
+  {
+    Raw<T, VEC> ra[LOADS], rb[LOADS];
+    int na = 0, nb = 0;
+    int it = warp;
+    if (it < items) fetch(it, ra, na);
+    while (it < items) {
+      const int i2 = it + kWarps;
+      if (i2 < items) fetch(i2, rb, nb);
+      reduce_item(it, ra, na);
+      it = i2;
+      if (it >= items) break;
+      const int i3 = it + kWarps;
+      if (i3 < items) fetch(i3, ra, na);
+      reduce_item(it, rb, nb);
+      it = i3;
+    }
+  }
+  __syncthreads();
+  for (int r = tid; r < rows; r += kThreads) {
+    if constexpr (MODE == kStochastic) {
+      float m = -INFINITY, sum = 0.f;
+      for (int k = 0; k < nsub; ++k) ms_combine(m, sum, pm[r * kMaxSub + k], ps[r * kMaxSub + k], coef);
+      sm.rm[r] = m;
+      sm.rs[r] = sum;
+    } else {
+      float best = 0.f;
+      int bi = -1;
+      for (int k = 0; k < nsub; ++k) am_combine(best, bi, pm[r * kMaxSub + k], __float_as_int(ps[r * kMaxSub + k]));
+      sm.rm[r] = best;
+      sm.ri[r] = bi;
     }
   }
   // token logits of the draft tokens this CTA owns
@@ -314,40 +415,43 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
   }
   if (bad) atomicOr(&sm.bad, 1);
   __syncthreads();
-  if (tid < rows) {
-    if constexpr (MODE == kStochastic) {
-      float m = -INFINITY, s = 0.f;
-      for (int k = 0; k < nsub; ++k) ms_combine(m, s, sm.pm[tid][k], sm.ps[tid][k], coef);
-      sm.rm[tid] = m;
-      sm.rs[tid] = s;
-    } else {
-      float best = 0.f;
-      int bi = -1;
-      for (int k = 0; k < nsub; ++k) am_combine(best, bi, sm.pm[tid][k], __float_as_int(sm.ps[tid][k]));
-      sm.rm[tid] = best;
-      sm.ri[tid] = bi;
-    }
-  }
   if (tid == 0 && sm.bad) record(args.status, SV_ERR_NONFINITE);
   cluster.sync();
 
-  // ---------------- phase 2: combine across the cluster ----------------
-  if (tid < rows) {
+  // ---------------- phase 2: combine across the cluster, one lane per rank ----------------
+  for (int base = 0; base < rows * 16; base += kThreads) {
+    const int x = base + tid, r = x >> 4, q = x & 15;
+    const bool valid = x < rows * 16 && q < C;
     if constexpr (MODE == kStochastic) {
       float m = -INFINITY, s = 0.f;
-      for (int q = 0; q < C; ++q) {
-        const float m2 = *cluster.map_shared_rank(&sm.rm[tid], q);
-        const float s2 = *cluster.map_shared_rank(&sm.rs[tid], q);
+      if (valid) {
+        m = *cluster.map_shared_rank(&sm.rm[r], q);
+        s = *cluster.map_shared_rank(&sm.rs[r], q);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
         ms_combine(m, s, m2, s2, coef);
       }
-      sm.M[tid] = m;
-      sm.Z[tid] = s;
+      if (x < rows * 16 && q == 0) {
+        sm.M[r] = m;
+        sm.Z[r] = s;
+      }
     } else {
       float best = 0.f;
       int bi = -1;
-      for (int q = 0; q < C; ++q)
-        am_combine(best, bi, *cluster.map_shared_rank(&sm.rm[tid], q), *cluster.map_shared_rank(&sm.ri[tid], q));
-      sm.am[tid] = bi;
+      if (valid) {
+        best = *cluster.map_shared_rank(&sm.rm[r], q);
+        bi = *cluster.map_shared_rank(&sm.ri[r], q);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        am_combine(best, bi, v2, i2);
+      }
+      if (x < rows * 16 && q == 0) sm.am[r] = bi;
     }
   }
   if constexpr (MODE == kStochastic) {
@@ -383,13 +487,13 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
         path[j] = -1;
       }
       int cur = 0, a = 0, am = sm.am[0];
-      bool ok = true;
+      bool good = true;
       for (int j = 1; j < n; ++j) {
         const int p = args.parent[t0 + j];
-        ok &= (p >= 0 && p < n && p != j);
+        good &= (p >= 0 && p < n && p != j);
       }
-      if (!ok) record(args.status, SV_ERR_BAD_LENGTH);
-      while (ok && a < n - 1) {
+      if (!good) record(args.status, SV_ERR_BAD_LENGTH);
+      while (good && a < n - 1) {
         am = sm.am[cur];
         int next = -1;
         for (int j = 1; j < n; ++j)
@@ -435,18 +539,59 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
     const float Mt = sm.M[a], Md = resid ? sm.M[n + a] : 0.f;
     const float chi = args.coef, clo = args.coef_lo;
     const float ur = args.u_res[b];
+    const int pair_off = ((len * (int)sizeof(T) + 127) / 128) * 128;
+    const T *bt = reinterpret_cast<const T *>(ring);
+    const T *bd = reinterpret_cast<const T *>(ring + pair_off);
+    const int ngroups = (len + kGroup - 1) / kGroup;
+
+    // ---- the row pair of the draw into shared memory ----
+    if (len > 0) {
+      if (VEC) {
+        if (tid == 0) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          const uint32_t bytes = static_cast<uint32_t>(len * sizeof(T));
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&sm.pair)),
+                       "r"(resid ? 2 * bytes : bytes)
+                       : "memory");
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                           smem_addr(ring)),
+                       "l"(trow + lo), "r"(bytes), "r"(smem_addr(&sm.pair))
+                       : "memory");
+          if (resid)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_addr(ring + pair_off)),
+                "l"(drow + lo), "r"(bytes), "r"(smem_addr(&sm.pair))
+                : "memory");
+        }
+        if (ok && !mbar_wait_bounded(smem_addr(&sm.pair), 0)) {
+          ok = false;
+          record(args.status, SV_ERR_TIMEOUT);
+        }
+      } else {
+        T *wt = reinterpret_cast<T *>(ring);
+        T *wd = reinterpret_cast<T *>(ring + pair_off);
+        for (int k = tid; k < len; k += kThreads) {
+          wt[k] = trow[lo + k];
+          if (resid) wd[k] = drow[lo + k];
+        }
+      }
+    }
+    __syncthreads();
 
     // ---- pass A: fixed-point normalisers of the row pair (residual draws) ----
     if (resid) {
       long long zt = 0, zd = 0;
-      for (int e = lo + tid * kGroup; e < hi; e += kSeg) {
-        float xt[kGroup], xd[kGroup];
-        load8<T, VEC>(trow, e, hi, xt);
-        load8<T, VEC>(drow, e, hi, xd);
+      if (ok) {
+        for (int g = tid; g < ngroups; g += kThreads) {
+          float xt[kGroup], xd[kGroup];
+          group8<T>(bt, g, len, xt);
+          group8<T>(bd, g, len, xd);
 #pragma unroll
-        for (int k = 0; k < kGroup; ++k) {
-          zt += to_fix(exp2_acc(xt[k] - Mt, chi, clo));
-          zd += to_fix(exp2_acc(xd[k] - Md, chi, clo));
+          for (int k = 0; k < kGroup; ++k) {
+            zt += to_fix(exp2_acc(xt[k] - Mt, chi, clo));
+            zd += to_fix(exp2_acc(xd[k] - Md, chi, clo));
+          }
         }
       }
       zt = block_sum_ll(zt, sm.ll_buf);
@@ -457,30 +602,37 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
       }
     }
     cluster.sync();
-    if (resid && tid == 0) {
+    if (resid && warp == 0) {
       long long Zt = 0, Zd = 0;
-      for (int q = 0; q < C; ++q) {
-        Zt += *cluster.map_shared_rank(&sm.zt, q);
-        Zd += *cluster.map_shared_rank(&sm.zd, q);
+      if (lane < C) {
+        Zt = *cluster.map_shared_rank(&sm.zt, lane);
+        Zd = *cluster.map_shared_rank(&sm.zd, lane);
       }
-      // q_v enters as e_d * (Z_t / Z_d), carried as hi + lo
-      const double rho = Zd > 0 ? (double)Zt / (double)Zd : 0.0;
-      sm.rho_hi = (float)rho;
-      sm.rho_lo = (float)(rho - (double)sm.rho_hi);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        Zt += __shfl_xor_sync(0xffffffffu, Zt, o);
+        Zd += __shfl_xor_sync(0xffffffffu, Zd, o);
+      }
+      if (lane == 0) {
+        // q_v enters as e_d * (Z_t / Z_d), carried as hi + lo
+        const double rho = Zd > 0 ? (double)Zt / (double)Zd : 0.0;
+        sm.rho_hi = (float)rho;
+        sm.rho_lo = (float)(rho - (double)sm.rho_hi);
+      }
     }
     __syncthreads();
     const float rho_hi = sm.rho_hi, rho_lo = sm.rho_lo;
 
     for (int pass = 0; pass < 2; ++pass) {
       const bool res_pass = resid && pass == 0;
-      // the eight weights of elements e .. e+7, in [0, 1]: proportional to
-      // max(0, p_v - q_v) (scaled by Z_t), or to p_v
-      auto weights8 = [&](int e, long long (&w)[kGroup]) {
+      // the eight weights of group g, in [0, 1]: proportional to max(0, p_v - q_v)
+      // (scaled by Z_t), or to p_v
+      auto weights8 = [&](int g, long long (&w)[kGroup]) {
         float xt[kGroup];
-        load8<T, VEC>(trow, e, hi, xt);
+        group8<T>(bt, g, len, xt);
         if (res_pass) {
           float xd[kGroup];
-          load8<T, VEC>(drow, e, hi, xd);
+          group8<T>(bd, g, len, xd);
 #pragma unroll
           for (int k = 0; k < kGroup; ++k) {
             const float et = exp2_acc(xt[k] - Mt, chi, clo);
@@ -492,78 +644,101 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args) {
           for (int k = 0; k < kGroup; ++k) w[k] = to_fix(exp2_acc(xt[k] - Mt, chi, clo));
         }
       };
-      // ---- pass B: this CTA's fixed-point mass ----
+      // ---- pass B: each group's mass and this CTA's total ----
       long long mass = 0;
-      for (int e = lo + tid * kGroup; e < hi; e += kSeg) {
-        long long w[kGroup];
-        weights8(e, w);
+      if (ok) {
+        for (int g = tid; g < ngroups; g += kThreads) {
+          long long w[kGroup];
+          weights8(g, w);
+          long long m8 = 0;
 #pragma unroll
-        for (int k = 0; k < kGroup; ++k) mass += w[k];
+          for (int k = 0; k < kGroup; ++k) m8 += w[k];
+          gmass[g] = m8;
+          mass += m8;
+        }
       }
       mass = block_sum_ll(mass, sm.ll_buf);
       if (tid == 0) sm.S[pass] = mass;
       cluster.sync();
-      if (tid == 0) {
-        long long S = 0;
-        for (int q = 0; q < C; ++q) S += *cluster.map_shared_rank(&sm.S[pass], q);
+      if (warp == 0) {
         // the draw: the smallest v whose inclusive prefix exceeds u' * S
+        const long long Sq = lane < C ? *cluster.map_shared_rank(&sm.S[pass], lane) : 0;
+        long long inc = Sq;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long y = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += y;
+        }
+        const long long S = __shfl_sync(0xffffffffu, inc, 31);
         const long long target = (long long)floor((double)ur * (double)S);
-        long long cum = 0, P = 0;
-        int owner = -1, last_pos = -1;
-        for (int q = 0; q < C; ++q) {
-          const long long Sq = *cluster.map_shared_rank(&sm.S[pass], q);
-          if (Sq > 0) last_pos = q;
-          if (owner < 0 && cum + Sq > target) {
-            owner = q;
-            P = cum;
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < C && inc > target);
+        const unsigned has = __ballot_sync(0xffffffffu, Sq > 0);
+        const int owner_l = hit ? __ffs(hit) - 1 : -1;
+        const long long P_l = __shfl_sync(0xffffffffu, inc - Sq, owner_l < 0 ? 0 : owner_l);
+        if (lane == 0) {
+          sm.fallback = (res_pass && S == 0) ? 1 : 0;
+          if (owner_l >= 0) {
+            sm.owner = owner_l;
+            sm.P_owner = P_l;
+          } else {  // u' outside [0, 1): the last token with mass
+            sm.owner = has ? 31 - __clz(has) : -1;
+            sm.P_owner = -1;
           }
-          cum += Sq;
+          sm.target = target;
+          sm.y_hit = INT_MAX;
+          sm.y_last = -1;
         }
-        sm.fallback = (res_pass && S == 0) ? 1 : 0;
-        sm.y_min = INT_MAX;
-        sm.y_last = -1;
-        if (owner < 0) {  // u' outside [0, 1): the last token with mass
-          owner = last_pos;
-          P = -1;
-        }
-        sm.owner = owner;
-        sm.P_owner = P;
-        sm.target = target;
       }
       __syncthreads();
       if (sm.fallback) continue;  // residual without mass: draw from p_a instead
       if (rank == sm.owner) {
-        // ---- pass C: exact prefix sums over this chunk, segment by segment ----
+        // ---- the owner: scan the group masses in order, then the group of the crossing ----
         const long long P = sm.P_owner, target = sm.target;
-        long long carry = 0;
-        for (int s0 = lo; s0 < hi; s0 += kSeg) {
-          const int e = s0 + tid * kGroup;
-          long long w[kGroup];
-          if (e < hi) {
-            weights8(e, w);
-          } else {
+        const int per = (ngroups + kThreads - 1) / kThreads;  // consecutive groups of this thread
+        const int g0 = min(ngroups, tid * per), g1 = min(ngroups, g0 + per);
+        long long local = 0;
+        int last_g = -1;
+        for (int g = g0; g < g1; ++g) {
+          local += gmass[g];
+          if (gmass[g] > 0) last_g = g;
+        }
+        long long seg_total;
+        long long cum = P + block_excl_scan_ll(local, sm.ll_buf, &seg_total);
+        if (last_g >= 0) atomicMax(&sm.y_last, last_g);
+        if (P >= 0) {
+          for (int g = g0; g < g1 && cum <= target; ++g) {
+            if (cum + gmass[g] > target) {  // the group whose prefix range holds the target
+              long long w[kGroup];
+              weights8(g, w);
+              long long c2 = cum;
+              int y = g * kGroup + kGroup - 1;
 #pragma unroll
-            for (int k = 0; k < kGroup; ++k) w[k] = 0;
-          }
-          long long local = 0;
-#pragma unroll
-          for (int k = 0; k < kGroup; ++k) local += w[k];
-          long long seg_total;
-          const long long excl = block_excl_scan_ll(local, sm.ll_buf, &seg_total);
-          long long inc = P + carry + excl;
-#pragma unroll
-          for (int k = 0; k < kGroup; ++k) {
-            inc += w[k];
-            if (w[k] > 0) {
-              if (P >= 0 && inc > target) atomicMin(&sm.y_min, e + k);
-              atomicMax(&sm.y_last, e + k);
+              for (int k = 0; k < kGroup; ++k) {
+                c2 += w[k];
+                if (c2 > target) {
+                  y = g * kGroup + k;
+                  break;
+                }
+              }
+              atomicMin(&sm.y_hit, lo + y);
+              break;
             }
+            cum += gmass[g];
           }
-          carry += seg_total;
         }
         __syncthreads();
         if (tid == 0) {
-          const int y = (sm.y_min != INT_MAX) ? sm.y_min : sm.y_last;
+          int y = sm.y_hit;
+          if (y == INT_MAX) {  // u' at or past the end: the last token with mass
+            const int g = sm.y_last;
+            y = lo + max(0, g) * kGroup;
+            if (g >= 0) {
+              long long w[kGroup];
+              weights8(g, w);
+              for (int k = 0; k < kGroup; ++k)
+                if (w[k] > 0) y = lo + g * kGroup + k;
+            }
+          }
           int32_t *o = args.out_tok + (size_t)b * args.max_q;
           for (int j = 0; j < args.max_q; ++j) o[j] = j < a ? args.draft_tok[d0 + j] : -1;
           o[a] = y;
@@ -589,14 +764,20 @@ int pick_cluster(int batch, int vocab) {
 template <typename T, bool VEC, int MODE>
 cudaError_t launch_t(const SamplerArgs &a, int C, cudaStream_t st) {
   auto kern = sampler_kernel<T, VEC, MODE>;
+  const int pair = ((a.chunk * (int)sizeof(T) + 127) / 128) * 128;
+  const int ring = std::max(2 * kMaxRows * kMaxSub * (int)sizeof(float), 2 * pair);
+  const int groups = (a.chunk + kGroup - 1) / kGroup;
+  const int dyn = ring + groups * (int)sizeof(long long);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  if (e != cudaSuccess) return e;
   if (C > 8) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, a.batch, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -605,9 +786,11 @@ cudaError_t launch_t(const SamplerArgs &a, int C, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  return cudaLaunchKernelEx(&cfg, kern, a, ring);
 }
 
+// rows 16-byte aligned: vector loads and 1-D bulk copies (every chunk then starts on
+// 16 bytes and is a multiple of 16 bytes long); otherwise scalar loads and copies
 template <typename T, int MODE>
 cudaError_t launch_m(const SamplerArgs &a, int C, cudaStream_t st) {
   const bool vec = ((size_t)a.vocab * sizeof(T)) % 16 == 0 && ((uintptr_t)a.tgt % 16 == 0) &&
@@ -634,8 +817,7 @@ cudaError_t launch_sampler(const SamplerArgs &a0, int dtype, int mode, cudaStrea
   return dtype == SV_DTYPE_BF16 ? launch_d<__nv_bfloat16>(a, mode, C, st) : launch_d<float>(a, mode, C, st);
 }
 
-// Largest vocabulary: 16 chunks of kMaxChunk elements (a chunk is at most
-// kMaxSub work items of 1024 or 2048 elements).
+// Largest vocabulary: 16 chunks of kMaxChunk elements.
 bool sampler_supports(int vocab) { return vocab <= 16 * kMaxChunk; }
 
 }  // namespace sv
