@@ -48,6 +48,8 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 template <typename T, int NK /* head_dim / 32 */>
 __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   constexpr int D = NK * 32;
   __shared__ float q_s[kRowsPerPass][D];
   __shared__ float k_s[kKeys][D + 1];
@@ -171,6 +173,8 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a) {
 // One warp per (query row, query head): merge the split partials.
 template <typename T>
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long idx = (long long)blockIdx.x * 4 + warp;
   if (idx >= (long long)a.total_q * a.num_q_heads) return;
@@ -208,8 +212,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 template <typename T, int NK>
 cudaError_t launch_nk(const AttnArgs &a, cudaStream_t st) {
   dim3 grid(a.max_splits, a.kv.num_kv_heads, a.kv.batch);
-  attn_simt_kernel<T, NK><<<grid, kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attn_simt_kernel<T, NK>, grid, dim3(kThreads), 0, st, a);
 }
 
 template <typename T>
@@ -237,9 +240,8 @@ cudaError_t launch_attn_combine(const AttnArgs &a, int dtype, cudaStream_t st) {
   if (a.max_splits <= 1 || a.total_q == 0) return cudaSuccess;
   const long long warps = (long long)a.total_q * a.num_q_heads;
   const unsigned blocks = (unsigned)((warps + 3) / 4);
-  if (dtype == SV_DTYPE_BF16) attn_combine_kernel<__nv_bfloat16><<<blocks, 128, 0, st>>>(a);
-  else attn_combine_kernel<float><<<blocks, 128, 0, st>>>(a);
-  return cudaGetLastError();
+  if (dtype == SV_DTYPE_BF16) return launch_pdl(attn_combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(128), 0, st, a);
+  return launch_pdl(attn_combine_kernel<float>, dim3(blocks), dim3(128), 0, st, a);
 }
 
 }  // namespace sv

@@ -130,6 +130,8 @@ template <int RG /* 16-row groups per CTA */>
 __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                            const __grid_constant__ CUtensorMap tmap_v,
                                                            const TcParams P) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   constexpr int kRows = 16 * RG;
   const AttnArgs &a = P.a;
   const KV &kv = a.kv;
@@ -530,8 +532,7 @@ cudaError_t launch_rg(const AttnArgs &a, const CUtensorMap &mk, const CUtensorMa
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<RG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.max_splits, a.kv.num_kv_heads * p.row_blocks, a.kv.batch);
-  attn_tc_kernel<RG><<<grid, kThreads, smem, st>>>(mk, mv, p);
-  return cudaGetLastError();
+  return launch_pdl(attn_tc_kernel<RG>, grid, dim3(kThreads), smem, st, mk, mv, p);
 }
 
 }  // namespace

@@ -25,21 +25,21 @@
 //
 // Six warps per CTA, each walking the same pieces in the same order:
 //  * warp 0, producer: TMA of 32-key K and V tiles into a 6-stage ring that
-//    runs on across unit boundaries. The pool is viewed as a 3-D tensor (64
-//    elements, rows, 2 halves of head_dim) so that one 128-byte-swizzled box
-//    brings both halves of a group of R = min(block_size, 32) rows: a tile is
-//    32/R groups, each stored [half 0 | half 1]; block ids are read 32 at a
-//    time;
+//    runs on across unit boundaries. The pool is viewed as a 4-D tensor (64
+//    elements, 8 rows, 2 halves of head_dim, groups of 8 rows) so that one
+//    128-byte-swizzled box brings both halves of R = min(block_size, 32) rows
+//    as 1 KB atoms [8 rows of half 0][8 rows of half 1]...; block ids are
+//    read 32 at a time and turned into pool rows by shift and mask;
 //  * warp 1, MMA issuer (one lane) and TMEM owner: S(t) = Q K(t)^T with
-//    tcgen05.mma kind::f16 (M = 128 rows, N = R keys per group, K = 128; A = Q
-//    in TMEM, B = K K-major in shared memory) into one of two TMEM S buffers,
+//    tcgen05.mma kind::f16 (M = 128 rows, N = 32 keys, K = 128; A = Q in
+//    TMEM, B = K K-major in shared memory) into one of two TMEM S buffers,
 //    then O += P(t-1) V(t-1) (A = P in TMEM, B = V MN-major in shared memory,
 //    N = 128; the first tile of a piece overwrites O); tcgen05.commit frees
 //    the K/V stage and signals the softmax. Before the first S of a piece it
 //    waits for that unit's Q;
 //  * warps 2-5, softmax and epilogue: thread = query row = TMEM lane. They
 //    store the unit's Q rows into TMEM (the next unit's as soon as the last S
-//    of the current one has landed, its loads issued one tile earlier), read
+//    of the current one has landed, prefetched into L2 one tile earlier), read
 //    S(t) (tcgen05.ld), mask edge tiles, keep a running maximum that moves
 //    only when the tile maximum exceeds it by more than 2^8 (then O is
 //    rescaled in TMEM), write P = 2^(s - m) as bf16 over S (tcgen05.st), and
@@ -280,6 +280,8 @@ struct Walker {
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                          const __grid_constant__ CUtensorMap tmap_v,
                                                                          const UmmaParams P) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   const AttnArgs &a = P.a;
   const KV &kv = a.kv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -726,48 +728,89 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
-// Merges the partial results of every unit that two or more CTAs shared; one
-// warp per query row, four head_dim elements per lane.
+// Merges the partial results of every unit that two or more CTAs shared.
+// First one thread per query row takes the maximum and the denominator of the
+// pieces' log-sum-exps; then the CTA's threads sweep the (row, 4 head_dim
+// elements) outputs, loading four pieces at a time.
 __global__ void __launch_bounds__(128) attn_umma_combine(const UmmaParams P) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   const AttnArgs &a = P.a;
   const int b = blockIdx.x, kvh = blockIdx.y / P.rb_max, rb = blockIdx.y % P.rb_max;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  __shared__ float row_max[kRowsMax], row_inv[kRowsMax];
+  const int W = P.prefix[a.kv.batch], base = P.prefix[b];  // loaded together with the sequence
   bool bad;
   const Seq s = load_seq(P, b, &bad);
   if (s.tiles == 0 || rb >= s.rbs) return;
-  const int W = P.prefix[a.kv.batch];
   const int per = max(1, (W + P.ctas - 1) / P.ctas);
-  const int T0 = P.prefix[b] + (kvh * s.rbs + rb) * s.tiles, T1 = T0 + s.tiles;
+  const int T0 = base + (kvh * s.rbs + rb) * s.tiles, T1 = T0 + s.tiles;
   const int c0 = T0 / per, c1 = (T1 - 1) / per;
   if (c0 == c1) return;  // one CTA held the whole unit and wrote its rows
-  // CTA c0 holds the unit as its first piece (slot 0) only when the unit starts its range
+  // CTA c0 holds the unit as its first piece (slot 0) only when the unit starts its range;
+  // every later CTA holds it as its first piece
   const int slot0 = T0 == c0 * per ? 0 : 1;
+  auto slot_of = [&](int cc, int row) -> size_t {
+    return ((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * P.rows_cap + row;
+  };
   const int rows = min(kRowsMax, P.G * s.n - rb * kRowsMax);
-  for (int row = warp; row < rows; row += 4) {
+  for (int row = tid; row < rows; row += blockDim.x) {
     float M = -INFINITY;
-    for (int cc = c0; cc <= c1; ++cc) {
-      const size_t slot = ((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * P.rows_cap + row;
-      M = fmaxf(M, P.part_lse[slot]);
-    }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, P.part_lse[slot_of(cc, row)]);
     float den = 0.f;
-    if (M != -INFINITY) {
-      for (int cc = c0; cc <= c1; ++cc) {
-        const size_t slot = ((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * P.rows_cap + row;
-        const float w = exp2f(P.part_lse[slot] - M);
-        const float4 o = *reinterpret_cast<const float4 *>(P.part_o + slot * kD + lane * 4);
-        den += w;
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
+    if (M != -INFINITY)
+      for (int cc = c0; cc <= c1; ++cc) den += exp2f(P.part_lse[slot_of(cc, row)] - M);
+    row_max[row] = M;
+    row_inv[row] = den > 0.f ? 1.f / den : 0.f;
+  }
+  __syncthreads();
+  // outputs (row, 4 head_dim elements): each thread takes up to kUnroll of them at once,
+  // with every piece's loads issued before any is used
+  constexpr int kUnroll = 4;
+  const int outs = rows * (kD / 4);
+  for (int x0 = tid; x0 < outs; x0 += blockDim.x * kUnroll) {
+    float4 acc[kUnroll];
+    int xr[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      xr[u] = x0 + u * blockDim.x;
+    }
+    for (int cc = c0; cc <= c1; ++cc) {
+      float lse[kUnroll];
+      float4 o[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        lse[u] = -INFINITY;
+        o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (xr[u] < outs) {
+          const int row = xr[u] / (kD / 4), c4 = (xr[u] % (kD / 4)) * 4;
+          const size_t sl = slot_of(cc, row);
+          lse[u] = P.part_lse[sl];
+          o[u] = *reinterpret_cast<const float4 *>(P.part_o + sl * kD + c4);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (xr[u] >= outs) continue;
+        const float M = row_max[xr[u] / (kD / 4)];
+        const float wk = M == -INFINITY ? 0.f : exp2f(lse[u] - M);
+        acc[u].x = fmaf(wk, o[u].x, acc[u].x);
+        acc[u].y = fmaf(wk, o[u].y, acc[u].y);
+        acc[u].z = fmaf(wk, o[u].z, acc[u].z);
+        acc[u].w = fmaf(wk, o[u].w, acc[u].w);
       }
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    const int r = rb * kRowsMax + row, i = r / P.G, g = r - i * P.G;
-    const size_t qrow = (size_t)(s.row0 + i) * a.num_q_heads + kvh * P.G + g;
-    *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + qrow * kD + lane * 4) =
-        make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (xr[u] >= outs) continue;
+      const int row = xr[u] / (kD / 4), c4 = (xr[u] % (kD / 4)) * 4;
+      const float inv = row_inv[row];
+      const int r = rb * kRowsMax + row, i = r / P.G, g = r - i * P.G;
+      const size_t qrow = (size_t)(s.row0 + i) * a.num_q_heads + kvh * P.G + g;
+      *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + qrow * kD + c4) =
+          make_uint2(pack_bf16(acc[u].x * inv, acc[u].y * inv), pack_bf16(acc[u].z * inv, acc[u].w * inv));
+    }
   }
 }
 
@@ -875,11 +918,9 @@ cudaError_t launch_attn_umma(const AttnArgs &a, void *workspace, size_t workspac
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_umma_kernel<<<p.ctas, kThreads, kSmemBytes, st>>>(mk, mv, p);
-  e = cudaGetLastError();
+  e = launch_pdl(attn_umma_kernel, dim3(p.ctas), dim3(kThreads), kSmemBytes, st, mk, mv, p);
   if (e != cudaSuccess) return e;
-  attn_umma_combine<<<dim3(a.kv.batch, a.kv.num_kv_heads * p.rb_max), 128, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(attn_umma_combine, dim3(a.kv.batch, a.kv.num_kv_heads * p.rb_max), dim3(128), 0, st, p);
 }
 
 }  // namespace sv

@@ -60,6 +60,8 @@ __device__ __forceinline__ int blocks_for(int tokens, int bs) { return (tokens +
 // append, step 1: block allocation (one CTA)
 // -------------------------------------------------------------------------
 __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int32_t *cu_q, int32_t *status) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   __shared__ int s_flag, s_top;
   if (threadIdx.x == 0) {
     s_flag = status_set(status) ? 1 : 0;
@@ -129,6 +131,8 @@ __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int
 // -------------------------------------------------------------------------
 __global__ void kv_scatter_kernel(KV kv, const uint8_t *new_k, const uint8_t *new_v, const int32_t *cu_q,
                                   int32_t *status) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   if (status_set(status)) return;
   const int row = blockIdx.x;
   int lo = 0, hi = kv.batch;  // the last b with cu_q[b] <= row owns the row
@@ -167,6 +171,8 @@ __global__ void kv_scatter_kernel(KV kv, const uint8_t *new_k, const uint8_t *ne
 // -------------------------------------------------------------------------
 __global__ void kv_tree_compact_kernel(KV kv, const int32_t *cu_q, const int32_t *accept, const int32_t *path,
                                        int max_q, int32_t *status) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   if (status_set(status)) return;
   const int b = blockIdx.x;
   const int n = cu_q[b + 1] - cu_q[b];
@@ -219,6 +225,8 @@ __global__ void kv_tree_compact_kernel(KV kv, const int32_t *cu_q, const int32_t
 // -------------------------------------------------------------------------
 __global__ void __launch_bounds__(kBookThreads) kv_truncate_kernel(KV kv, const int32_t *cu_q,
                                                                    const int32_t *accept, int32_t *status) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   __shared__ int s_flag, s_top;
   if (threadIdx.x == 0) {
     s_flag = status_set(status) ? 1 : 0;
@@ -291,23 +299,20 @@ __global__ void __launch_bounds__(kBookThreads) kv_truncate_kernel(KV kv, const 
 
 cudaError_t launch_kv_append(const KV &kv, const void *new_k, const void *new_v, const int32_t *cu_q,
                              int total_q, int32_t *status, cudaStream_t st) {
-  kv_alloc_kernel<<<1, kBookThreads, 0, st>>>(kv, cu_q, status);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(kv_alloc_kernel, dim3(1), dim3(kBookThreads), 0, st, kv, cu_q, status);
   if (e != cudaSuccess || total_q == 0) return e;
-  kv_scatter_kernel<<<(unsigned)total_q, 128, 0, st>>>(kv, (const uint8_t *)new_k, (const uint8_t *)new_v,
-                                                       cu_q, status);
-  return cudaGetLastError();
+  return launch_pdl(kv_scatter_kernel, dim3((unsigned)total_q), dim3(128), 0, st, kv, (const uint8_t *)new_k,
+                    (const uint8_t *)new_v, cu_q, status);
 }
 
 cudaError_t launch_kv_rollback(const KV &kv, const int32_t *cu_q, const int32_t *accept, const int32_t *path,
                                int max_q, int32_t *status, cudaStream_t st) {
   if (path != nullptr) {
-    kv_tree_compact_kernel<<<kv.batch, 256, 0, st>>>(kv, cu_q, accept, path, max_q, status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kv_tree_compact_kernel, dim3(kv.batch), dim3(256), 0, st, kv, cu_q, accept, path,
+                               max_q, status);
     if (e != cudaSuccess) return e;
   }
-  kv_truncate_kernel<<<1, kBookThreads, 0, st>>>(kv, cu_q, accept, status);
-  return cudaGetLastError();
+  return launch_pdl(kv_truncate_kernel, dim3(1), dim3(kBookThreads), 0, st, kv, cu_q, accept, status);
 }
 
 }  // namespace sv

@@ -220,6 +220,8 @@ struct Smem {
 
 template <typename T, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int ring_bytes) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
   constexpr int IE = item_elems<T, VEC>();
   constexpr int LOADS = ItemCfg<T, VEC>::LOADS, N = ItemCfg<T, VEC>::N;
   cg::cluster_group cluster = cg::this_cluster();
@@ -779,13 +781,15 @@ cudaError_t launch_t(const SamplerArgs &a, int C, cudaStream_t st) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a, ring);
 }
 

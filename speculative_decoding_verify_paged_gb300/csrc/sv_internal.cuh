@@ -32,6 +32,36 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: every kernel of the library is launched with
+// launch_pdl, so its launch and set-up may overlap the end of the kernel
+// before it on the stream. Each kernel calls grid_dependency_wait() first,
+// before it reads or writes any memory and before any early return: the
+// earlier kernel has then completed and its writes are visible, and, since
+// every kernel waits before it can complete, completion stays transitive
+// along the stream. grid_dependents_launch() lets the next kernel launch.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // bounded mbarrier wait: gives up (returns false) once it has waited about
 // kWaitBudgetNs of wall-clock time (globaltimer), so that a kernel whose
 // barrier phase never completes ends within a second instead of spinning on
