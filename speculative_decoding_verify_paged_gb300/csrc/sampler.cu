@@ -54,7 +54,6 @@ constexpr int kMaxQ = 64;
 constexpr int kMaxRows = 2 * kMaxQ;  // target + draft rows of one sequence
 constexpr int kMaxChunk = 16384;     // vocabulary elements per CTA
 constexpr int kGroup = 8;            // consecutive elements of a group
-constexpr int kMaxSub = 32;          // phase 1 work items per row per CTA
 
 // Phase 1 work item: one warp, LOADS loads of N elements per lane (2 KB).
 template <typename T, bool VEC> struct ItemCfg;
@@ -64,7 +63,6 @@ template <typename T> struct ItemCfg<T, false> { static constexpr int N = 1, LOA
 template <typename T, bool VEC> __host__ __device__ constexpr int item_elems() {
   return 32 * ItemCfg<T, VEC>::N * ItemCfg<T, VEC>::LOADS;
 }
-static_assert(kMaxChunk / item_elems<float, true>() <= kMaxSub, "phase 1 items per row");
 
 template <typename T, bool VEC> struct Raw;
 template <typename T> struct Raw<T, true> { uint4 v; };
@@ -126,8 +124,8 @@ __device__ __forceinline__ void am_combine(float &v, int &i, float v2, int i2) {
 // 2^(d * c) for d <= 0 with c = c_hi + c_lo: the product is carried to about
 // 2^-40 before exp2f, so no rounding of c or of d*c shifts all weights alike.
 __device__ __forceinline__ float exp2_acc(float d, float c_hi, float c_lo) {
+  d = fmaxf(d, -200.f);  // -inf logits: 2^(d c) flushes to zero below 2^-126 either way
   const float xh = d * c_hi;
-  if (!(xh > -160.f)) return 0.f;  // -inf logits and underflow
   const float xe = fmaf(d, c_hi, -xh) + d * c_lo;
   return fast_exp2(xh) * fmaf(xe, 0.69314718055994531f, 1.0f);
 }
@@ -175,24 +173,32 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 }
 
 // The eight elements of group g of a shared-memory copy of a chunk, as floats;
-// -inf at and past element n.
+// -inf at and past element n (only the chunk's last group can reach it).
 template <typename T>
 __device__ __forceinline__ void group8(const T *buf, int g, int n, float (&x)[kGroup]) {
   const int e = g * kGroup;
   if constexpr (sizeof(T) == 2) {
     const uint4 r = *reinterpret_cast<const uint4 *>(buf + e);
-    const T *t = reinterpret_cast<const T *>(&r);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(&r);
 #pragma unroll
-    for (int k = 0; k < kGroup; ++k) x[k] = (e + k < n) ? to_f32(t[k]) : -INFINITY;
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = __uint_as_float(w[k] << 16);
+      x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
   } else {
     const uint4 r0 = *reinterpret_cast<const uint4 *>(buf + e);
     const uint4 r1 = *reinterpret_cast<const uint4 *>(buf + e + 4);
     const float *f0 = reinterpret_cast<const float *>(&r0), *f1 = reinterpret_cast<const float *>(&r1);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      x[k] = (e + k < n) ? f0[k] : -INFINITY;
-      x[k + 4] = (e + k + 4 < n) ? f1[k] : -INFINITY;
+      x[k] = f0[k];
+      x[k + 4] = f1[k];
     }
+  }
+  if (e + kGroup > n) {
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k)
+      if (e + k >= n) x[k] = -INFINITY;
   }
 }
 
@@ -231,10 +237,10 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ Smem sm;
   extern __shared__ __align__(128) uint8_t dyn[];
-  // phase 1: per-item partials [kMaxRows][kMaxSub] x 2; phase 3: the row pair (same bytes)
+  // phase 1: per-row partials [kMaxRows][kWarps] x 2; phase 3: the row pair (same bytes)
   uint8_t *ring = dyn;
   float *pm = reinterpret_cast<float *>(dyn);
-  float *ps = pm + kMaxRows * kMaxSub;
+  float *ps = pm + kMaxRows * kWarps;
   long long *gmass = reinterpret_cast<long long *>(dyn + ring_bytes);  // phase 3: per-group mass
 
   const int V = args.vocab;
@@ -263,87 +269,115 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
   __syncthreads();
   bool ok = true;  // false after a bounded wait gave up: the remaining work is skipped, barriers are kept
 
-  // ---------------- phase 1: per-item partial statistics ----------------
-  // warp w takes items w, w + 8, ...; the next item's loads are in flight while
-  // the current one is reduced
+  // ---------------- phase 1: per-row statistics of this CTA's chunk ----------------
+  // The items (2 KB of one row, row-major) are cut into kWarps contiguous runs, one
+  // per warp. A lane accumulates its share of the current row online; the warp
+  // reduces only where its run leaves a row, into slot [row][warp]. The next
+  // item's loads are in flight while the current one is reduced.
   const int nsub = (len + IE - 1) / IE;
   const int items = rows * nsub;
+  const int it_begin = (int)((long long)items * warp / kWarps);
+  const int it_end = (int)((long long)items * (warp + 1) / kWarps);
+  for (int x = tid; x < rows * kWarps; x += kThreads) {
+    pm[x] = (MODE == kStochastic) ? -INFINITY : 0.f;
+    ps[x] = (MODE == kStochastic) ? 0.f : __int_as_float(-1);
+  }
+  __syncthreads();
   int bad = 0;
+  float lm = -INFINITY, ls = 0.f;  // stochastic: this lane's running max and sum of 2^((x - lm) c)
+  float lb = 0.f;                  // greedy: this lane's best value and its index
+  int lbi = -1;
+  int cur_row = -1;
+  auto flush = [&]() {  // warp-uniform: the lanes' state of cur_row into slot [cur_row][warp]
+    if constexpr (MODE == kStochastic) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, lm, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, ls, o);
+        ms_combine(lm, ls, m2, s2, coef);
+      }
+      if (lane == 0) {
+        pm[cur_row * kWarps + warp] = lm;
+        ps[cur_row * kWarps + warp] = ls;
+      }
+      lm = -INFINITY;
+      ls = 0.f;
+    } else {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, lb, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, lbi, o);
+        am_combine(lb, lbi, v2, i2);
+      }
+      if (lane == 0) {
+        pm[cur_row * kWarps + warp] = lb;
+        ps[cur_row * kWarps + warp] = __int_as_float(lbi);
+      }
+      lb = 0.f;
+      lbi = -1;
+    }
+  };
+  // this lane's elements of item it into the running state
   auto reduce_item = [&](int it, const Raw<T, VEC> (&raw)[LOADS], int nv) {
     const int r = it / nsub, sub = it % nsub;
+    if (r != cur_row) {
+      if (cur_row >= 0) flush();
+      cur_row = r;
+    }
     const int e0 = lo + sub * IE;
-    if constexpr (MODE == kStochastic && VEC && sizeof(T) == 2) {
-      // bf16 pairs: the maximum on packed pairs (NaN propagates, so one test of the
-      // item maximum catches NaN and +inf), then sum 2^(x c - m c) with one unpack per half
-      const __nv_bfloat162 ninf2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-      __nv_bfloat162 mx2 = ninf2;
+    if constexpr (MODE == kStochastic) {
+      float mi;
+      if constexpr (VEC && sizeof(T) == 2) {
+        // bf16 pairs: the maximum on packed pairs, NaN propagating
+        __nv_bfloat162 mx2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
 #pragma unroll
-      for (int u = 0; u < LOADS; ++u)
-        if (u < nv) {
-          const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw[u].v);
+        for (int u = 0; u < LOADS; ++u)
+          if (u < nv) {
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw[u].v);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mx2 = __hmax2_nan(mx2, h[k]);
-        }
-      float m = fmaxf(__low2float(mx2), __high2float(mx2));
-      if (__low2float(mx2) != __low2float(mx2) || __high2float(mx2) != __high2float(mx2)) m = NAN;
-      bad |= (m != m) | (m == INFINITY);
-      float sum = 0.f;
-      if (m != -INFINITY && m == m) {
-        const float nmc = -m * coef;
+            for (int k = 0; k < 4; ++k) mx2 = __hmax2_nan(mx2, h[k]);
+          }
+        const float l2 = __low2float(mx2), h2 = __high2float(mx2);
+        mi = (l2 != l2 || h2 != h2) ? NAN : fmaxf(l2, h2);
+      } else {
+        mi = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < LOADS; ++u)
+          if (u < nv)
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+              const float x = elem<T, VEC>(raw[u], k);
+              mi = (x != x || mi != mi) ? NAN : fmaxf(mi, x);
+            }
+      }
+      bad |= (mi != mi) | (mi == INFINITY);
+      if (!(mi == mi) || mi == -INFINITY) return;  // nothing to add (or the row is reported)
+      if (mi > lm) {
+        ls = (lm == -INFINITY) ? 0.f : ls * fast_exp2((lm - mi) * coef);
+        lm = mi;
+      }
+      const float nmc = -lm * coef;
+      float acc = 0.f;
+      if constexpr (VEC && sizeof(T) == 2) {
 #pragma unroll
         for (int u = 0; u < LOADS; ++u)
           if (u < nv) {
             const uint32_t *w = reinterpret_cast<const uint32_t *>(&raw[u].v);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              sum += fast_exp2(fmaf(__uint_as_float(w[k] << 16), coef, nmc));
-              sum += fast_exp2(fmaf(__uint_as_float(w[k] & 0xffff0000u), coef, nmc));
+              acc += fast_exp2(fmaf(__uint_as_float(w[k] << 16), coef, nmc));
+              acc += fast_exp2(fmaf(__uint_as_float(w[k] & 0xffff0000u), coef, nmc));
             }
           }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-        ms_combine(m, sum, m2, s2, coef);
-      }
-      if (lane == 0) {
-        pm[r * kMaxSub + sub] = m;
-        ps[r * kMaxSub + sub] = sum;
-      }
-    } else if constexpr (MODE == kStochastic) {
-      float m = -INFINITY;  // raw logit maximum (exact)
-#pragma unroll
-      for (int u = 0; u < LOADS; ++u)
-        if (u < nv)
-#pragma unroll
-          for (int k = 0; k < N; ++k) {
-            const float x = elem<T, VEC>(raw[u], k);
-            bad |= (x != x) | (x == INFINITY);
-            m = fmaxf(m, x);
-          }
-      float sum = 0.f;
-      if (m != -INFINITY) {
-        const float nmc = -m * coef;
+      } else {
 #pragma unroll
         for (int u = 0; u < LOADS; ++u)
           if (u < nv)
 #pragma unroll
-            for (int k = 0; k < N; ++k) sum += fast_exp2(fmaf(elem<T, VEC>(raw[u], k), coef, nmc));
+            for (int k = 0; k < N; ++k) acc += fast_exp2(fmaf(elem<T, VEC>(raw[u], k), coef, nmc));
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-        ms_combine(m, sum, m2, s2, coef);
-      }
-      if (lane == 0) {
-        pm[r * kMaxSub + sub] = m;
-        ps[r * kMaxSub + sub] = sum;
-      }
+      ls += acc;
     } else {
-      float best = 0.f;
-      int bi = -1;
 #pragma unroll
       for (int u = 0; u < LOADS; ++u)
         if (u < nv)
@@ -351,18 +385,8 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
           for (int k = 0; k < N; ++k) {
             const float x = elem<T, VEC>(raw[u], k);
             bad |= (x != x);
-            am_combine(best, bi, x, e0 + (u * 32 + lane) * N + k);
+            am_combine(lb, lbi, x, e0 + (u * 32 + lane) * N + k);
           }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-        am_combine(best, bi, v2, i2);
-      }
-      if (lane == 0) {
-        pm[r * kMaxSub + sub] = best;
-        ps[r * kMaxSub + sub] = __int_as_float(bi);
-      }
     }
   };
   auto fetch = [&](int it, Raw<T, VEC> (&raw)[LOADS], int &nv) {
@@ -374,31 +398,29 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
   {
     Raw<T, VEC> ra[LOADS], rb[LOADS];
     int na = 0, nb = 0;
-    int it = warp;
-    if (it < items) fetch(it, ra, na);
-    while (it < items) {
-      const int i2 = it + kWarps;
-      if (i2 < items) fetch(i2, rb, nb);
+    int it = it_begin;
+    if (it < it_end) fetch(it, ra, na);
+    while (it < it_end) {
+      if (it + 1 < it_end) fetch(it + 1, rb, nb);
       reduce_item(it, ra, na);
-      it = i2;
-      if (it >= items) break;
-      const int i3 = it + kWarps;
-      if (i3 < items) fetch(i3, ra, na);
+      if (++it >= it_end) break;
+      if (it + 1 < it_end) fetch(it + 1, ra, na);
       reduce_item(it, rb, nb);
-      it = i3;
+      ++it;
     }
+    if (cur_row >= 0) flush();
   }
   __syncthreads();
   for (int r = tid; r < rows; r += kThreads) {
     if constexpr (MODE == kStochastic) {
       float m = -INFINITY, sum = 0.f;
-      for (int k = 0; k < nsub; ++k) ms_combine(m, sum, pm[r * kMaxSub + k], ps[r * kMaxSub + k], coef);
+      for (int w = 0; w < kWarps; ++w) ms_combine(m, sum, pm[r * kWarps + w], ps[r * kWarps + w], coef);
       sm.rm[r] = m;
       sm.rs[r] = sum;
     } else {
       float best = 0.f;
       int bi = -1;
-      for (int k = 0; k < nsub; ++k) am_combine(best, bi, pm[r * kMaxSub + k], __float_as_int(ps[r * kMaxSub + k]));
+      for (int w = 0; w < kWarps; ++w) am_combine(best, bi, pm[r * kWarps + w], __float_as_int(ps[r * kWarps + w]));
       sm.rm[r] = best;
       sm.ri[r] = bi;
     }
@@ -767,7 +789,7 @@ template <typename T, bool VEC, int MODE>
 cudaError_t launch_t(const SamplerArgs &a, int C, cudaStream_t st) {
   auto kern = sampler_kernel<T, VEC, MODE>;
   const int pair = ((a.chunk * (int)sizeof(T) + 127) / 128) * 128;
-  const int ring = std::max(2 * kMaxRows * kMaxSub * (int)sizeof(float), 2 * pair);
+  const int ring = std::max(2 * kMaxRows * kWarps * (int)sizeof(float), 2 * pair);
   const int groups = (a.chunk + kGroup - 1) / kGroup;
   const int dyn = ring + groups * (int)sizeof(long long);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
