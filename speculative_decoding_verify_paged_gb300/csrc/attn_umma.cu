@@ -579,6 +579,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
           uint32_t qr[64];
           store_q(qr, load_q(nxt, qr));
         }
+        if (kt == cur.kt1 - 1 && t >= 1) {
+          // last tile of the piece: P(t-1) V(t-1) must be done before P(t) goes out. Here
+          // P V(t) cannot have started, so o_bar is in the phase of t-1 or t and the parity
+          // wait is unambiguous; the end of the piece then waits for phase t alone.
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_bar), (t - 1) & 1));
+          if (!ok) break;
+        }
         if (valid < kTile) {
           // zero this tile's V rows past the unit's end before P V reads them
           uint8_t *vst = stages + (t % kStages) * kStageBytes + 2 * kHalfBytes;
@@ -671,13 +678,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       // ---- end of the piece: wait for its last P V, then write ----
-      // S(tl) is issued before P(tl-1) V(tl-1), so seeing S(tl) proves only that
-      // P V up to tl-2 finished: o_bar may still be in the phase of tl-1, where a
-      // parity wait for tl alone would pass early.
+      // P V(tl-1) finished before P(tl) went out, and P V(tl+1) cannot start before
+      // this warp's next p_ready: o_bar is in the phase of tl or tl+1.
       const int tl = t - 1;
-      bool w = tl < 1 || mbar_wait(smem_u32(o_bar), (tl - 1) & 1);
-      if (w) w = mbar_wait(smem_u32(o_bar), tl & 1);
-      ok = __all_sync(0xffffffffu, w);
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_bar), tl & 1));
       if (!ok) break;
       tc_fence_after();
       if (warp_live) {
