@@ -217,6 +217,13 @@ sv_status sv_spec_verify_attn_no_alloc(const sv_paged_kv *kv, const void *q, voi
  *   accept_count   int32 [batch] out: a_b
  *   out_tokens     int32 [batch, max_q_per_seq] out: x_1..x_a, y, then -1
  *   num_out        int32 [batch] out: a_b + 1
+ *   workspace      device scratch of at least
+ *                  sv_spec_rejection_sample_workspace_bytes(...) bytes,
+ *                  256-byte aligned, owned by the caller; its contents need no
+ *                  initialisation and are not kept between calls (per-row
+ *                  partial softmax statistics: the statistics kernel writes
+ *                  them, the decision kernel reads them). SV_ERR_WORKSPACE if
+ *                  it is NULL, unaligned or too small.
  *   status_dev     int32 [1] or NULL: SV_ERR_NONFINITE for NaN/+inf logits,
  *                  SV_ERR_BAD_TOKEN for a draft token outside the vocabulary
  * Arithmetic is fp32; decisions equal the exact ones except when a uniform
@@ -226,7 +233,18 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
                                    int32_t vocab, int32_t batch, const int32_t *cu_q, int32_t total_q,
                                    int32_t max_q_per_seq, const int32_t *draft_tokens, const float *u_accept,
                                    const float *u_resample, float temperature, int32_t *accept_count,
-                                   int32_t *out_tokens, int32_t *num_out, int32_t *status_dev, void *stream);
+                                   int32_t *out_tokens, int32_t *num_out, void *workspace, size_t workspace_bytes,
+                                   int32_t *status_dev, void *stream);
+
+/*
+ * Workspace bytes of sv_spec_rejection_sample for these sizes (temperature 0:
+ * greedy, target rows only; also the size for sv_tree_greedy_accept). It is
+ * (rows) x ceil(vocab x element size / 16 KB) x 64 bytes, rows = total_q, plus
+ * total_q - batch draft rows when temperature > 0. Returns 0 for invalid sizes
+ * or types.
+ */
+size_t sv_spec_rejection_sample_workspace_bytes(int32_t logits_dtype, int32_t vocab, int32_t batch, int32_t total_q,
+                                                float temperature);
 
 /*
  * sv_tree_greedy_accept -- greedy verification of a draft tree (the tree mode
@@ -241,12 +259,13 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
  *                 nodes in path order, then -1 (input of sv_kv_rollback)
  *   out_tokens    int32 [batch, max_q_per_seq] out: path tokens, y, then -1
  *   num_out       int32 [batch] out: a_b + 1
+ *   workspace     as for sv_spec_rejection_sample, sized with temperature 0
  */
 sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype, int32_t vocab, int32_t batch,
                                 const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq,
                                 const int32_t *node_tokens, const int32_t *parent, int32_t *accept_count,
-                                int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out,
-                                int32_t *status_dev, void *stream);
+                                int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, void *workspace,
+                                size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /*
  * sv_kv_rollback -- keep each sequence's accepted prefix, give back the rest.

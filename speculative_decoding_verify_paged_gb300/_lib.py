@@ -30,7 +30,8 @@ STATUS_NAMES = {
 }
 
 EXPORTS = ("sv_kv_append", "sv_spec_verify_attn_workspace_bytes", "sv_spec_verify_attn",
-           "sv_spec_verify_attn_no_alloc", "sv_spec_rejection_sample", "sv_tree_greedy_accept", "sv_kv_rollback",
+           "sv_spec_verify_attn_no_alloc", "sv_spec_rejection_sample_workspace_bytes", "sv_spec_rejection_sample",
+           "sv_tree_greedy_accept", "sv_kv_rollback",
            "sv_status_string", "sv_version", "sv_set_option")
 SV_OPT_ATTN_PATH = 1
 ATTN_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "warp_mma": 3}
@@ -77,8 +78,9 @@ def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CD
             "sv_spec_verify_attn_workspace_bytes": (S, [KVP, I, I, I, I]),
             "sv_spec_verify_attn": (I, [KVP, P, P, P, I, I, I, I, F, I, P, P, S, P, P]),
             "sv_spec_verify_attn_no_alloc": (I, [KVP, P, P, P, I, I, I, I, F, I, P, P, P]),
-            "sv_spec_rejection_sample": (I, [P, P, I, I, I, P, I, I, P, P, P, F, P, P, P, P, P]),
-            "sv_tree_greedy_accept": (I, [P, I, I, I, P, I, I, P, P, P, P, P, P, P, P]),
+            "sv_spec_rejection_sample_workspace_bytes": (S, [I, I, I, I, F]),
+            "sv_spec_rejection_sample": (I, [P, P, I, I, I, P, I, I, P, P, P, F, P, P, P, P, S, P, P]),
+            "sv_tree_greedy_accept": (I, [P, I, I, I, P, I, I, P, P, P, P, P, P, P, S, P, P]),
             "sv_kv_rollback": (I, [KVP, P, P, P, I, P, P]),
             "sv_status_string": (ctypes.c_char_p, [I]),
             "sv_version": (I, []),
@@ -202,29 +204,48 @@ def spec_verify_attn_no_alloc(kv: PagedKV, q: torch.Tensor, out: torch.Tensor, c
            "sv_spec_verify_attn_no_alloc")
 
 
+def spec_rejection_sample_workspace_bytes(logits_dtype: torch.dtype, vocab: int, batch: int, total_q: int,
+                                          temperature: float) -> int:
+    code = SV_DTYPE_BF16 if logits_dtype == torch.bfloat16 else SV_DTYPE_F32
+    return int(load().sv_spec_rejection_sample_workspace_bytes(code, int(vocab), int(batch), int(total_q),
+                                                               float(temperature)))
+
+
+def _sampler_workspace(workspace: Optional[torch.Tensor], logits: torch.Tensor, batch: int,
+                       temperature: float) -> tuple:
+    """The caller's workspace, or a new one of the size the library asks for."""
+    if workspace is None:
+        need = spec_rejection_sample_workspace_bytes(logits.dtype, int(logits.shape[1]), batch,
+                                                     int(logits.shape[0]), temperature)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=logits.device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
 def spec_rejection_sample(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor], cu_q: torch.Tensor,
                           draft_tokens: Optional[torch.Tensor], u_accept: Optional[torch.Tensor],
                           u_resample: Optional[torch.Tensor], temperature: float, accept_count: torch.Tensor,
-                          out_tokens: torch.Tensor, num_out: torch.Tensor, *, status: Optional[torch.Tensor] = None,
-                          stream=None) -> None:
+                          out_tokens: torch.Tensor, num_out: torch.Tensor, *, workspace: Optional[torch.Tensor] = None,
+                          status: Optional[torch.Tensor] = None, stream=None) -> None:
     batch = int(cu_q.shape[0]) - 1
+    ws, ws_bytes = _sampler_workspace(workspace, target_logits, batch, temperature)
     _check(load().sv_spec_rejection_sample(
         _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), int(target_logits.shape[1]), batch,
         _ptr(cu_q), int(target_logits.shape[0]), int(out_tokens.shape[1]), _ptr(draft_tokens), _ptr(u_accept),
-        _ptr(u_resample), float(temperature), _ptr(accept_count), _ptr(out_tokens), _ptr(num_out), _ptr(status),
-        _stream(stream)), "sv_spec_rejection_sample")
+        _ptr(u_resample), float(temperature), _ptr(accept_count), _ptr(out_tokens), _ptr(num_out), _ptr(ws),
+        ws_bytes, _ptr(status), _stream(stream)), "sv_spec_rejection_sample")
 
 
 def tree_greedy_accept(target_logits: torch.Tensor, cu_q: torch.Tensor, node_tokens: torch.Tensor,
                        parent: torch.Tensor, accept_count: torch.Tensor, path_nodes: torch.Tensor,
-                       out_tokens: torch.Tensor, num_out: torch.Tensor, *, status: Optional[torch.Tensor] = None,
-                       stream=None) -> None:
+                       out_tokens: torch.Tensor, num_out: torch.Tensor, *, workspace: Optional[torch.Tensor] = None,
+                       status: Optional[torch.Tensor] = None, stream=None) -> None:
     batch = int(cu_q.shape[0]) - 1
+    ws, ws_bytes = _sampler_workspace(workspace, target_logits, batch, 0.0)
     _check(load().sv_tree_greedy_accept(
         _ptr(target_logits), _dtype_code(target_logits), int(target_logits.shape[1]), batch, _ptr(cu_q),
         int(target_logits.shape[0]), int(out_tokens.shape[1]), _ptr(node_tokens), _ptr(parent),
-        _ptr(accept_count), _ptr(path_nodes), _ptr(out_tokens), _ptr(num_out), _ptr(status), _stream(stream)),
-        "sv_tree_greedy_accept")
+        _ptr(accept_count), _ptr(path_nodes), _ptr(out_tokens), _ptr(num_out), _ptr(ws), ws_bytes, _ptr(status),
+        _stream(stream)), "sv_tree_greedy_accept")
 
 
 def kv_rollback(kv: PagedKV, cu_q: torch.Tensor, accept_count: torch.Tensor, status: torch.Tensor, *,

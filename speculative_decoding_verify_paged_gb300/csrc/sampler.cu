@@ -1,4 +1,5 @@
-// Fused verification sampler: one thread-block cluster per sequence.
+// Verification sampler: a row-statistics kernel, then one decision cluster
+// per sequence.
 //
 // What it computes ("Speculative decoding and continuous batching in
 // practice", sec. 1.2; "Speculative decoding principles and a vLLM production
@@ -12,29 +13,34 @@
 //   Tree greedy: walk from the root to the child whose token is the argmax of
 //   the current node's row; y = argmax of the last node's row.
 //
-// How: the vocabulary is cut into C equal chunks, one per CTA of the cluster.
-//   phase 1  every CTA streams its chunk of every row of the sequence (target
-//            rows and draft rows) once; a work item is 2 KB of one row for one
-//            warp, and each warp has its next item's loads in flight while it
-//            reduces the current one to a (max, sum of 2^((l - max) log2(e)/T))
-//            pair, or to an argmax.
-//   phase 2  cluster barrier; every CTA combines the C partial results of
-//            every row through distributed shared memory with a fixed shuffle
-//            tree (one lane per rank), so all CTAs hold identical row
-//            statistics and take identical decisions.
-//   phase 3  (T > 0) the row pair of the draw (target and draft row a, or the
-//            bonus row) is copied once into shared memory. With a 128K
-//            vocabulary the residual CDF has intervals of ~1e-5, so this phase
-//            is exact where fp32 would not be: exponents carry log2(e)/T as a
-//            hi+lo pair, the weights are summed in 64-bit fixed point (2^-40
-//            units, order-free and exact), the draft normaliser enters as the
-//            ratio Z_t/Z_d in hi+lo form, and the target is the integer
-//            floor(u' * S). Pass A sums the two normalisers, pass B each
-//            8-element group's residual mass (kept in shared memory) and each
-//            CTA's total; after a cluster barrier the prefix over ranks picks
-//            the CTA holding the crossing, which scans its group masses and
-//            recomputes the one group that holds it.
-// All reductions run in a fixed order, so results are deterministic.
+// How:
+//   statistics  every row of the batch (target rows, then draft rows) is cut
+//               into 16 KB items; the launch's items are cut into equal
+//               contiguous ranges, one per persistent CTA, so the whole batch
+//               streams through every SM at once whatever the number of
+//               sequences. A producer warp keeps six items in flight with 1-D
+//               bulk copies; eight consumer warps reduce each item to a
+//               (max, sum of 2^((l - max) log2(e)/T)) pair, or to an argmax,
+//               per warp, into a workspace of per-(item, warp) partials.
+//   decisions   one cluster per sequence (one CTA for greedy and tree). Every
+//               CTA combines its sequence's partials in the same fixed order,
+//               so all CTAs hold identical row statistics and take identical
+//               accept decisions. For T > 0 the row pair of the draw (target
+//               and draft row a, or the bonus row) is then read once, cut into
+//               one chunk per CTA. With a 128K vocabulary the residual CDF has
+//               intervals of ~1e-5, so the draw is exact where fp32 would not
+//               be: exponents carry log2(e)/T as a hi+lo pair, the weights are
+//               summed in 64-bit fixed point (2^-40 units, order-free and
+//               exact), and the draft side enters as e_d Z_t/Z_d with the
+//               normaliser ratio (from the row statistics, relative error about
+//               1e-6) in hi+lo form; the target is the integer floor(u' * S).
+//               One pass sums each 8-element group's residual mass (kept in
+//               shared memory) and each CTA's total; after a cluster barrier
+//               the prefix over ranks picks the CTA holding the crossing, which
+//               scans its group masses and recomputes the one group that holds
+//               it.
+// All reductions run in a fixed order for a given device, so results are
+// deterministic.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -48,49 +54,16 @@ namespace cg = cooperative_groups;
 namespace sv {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // decision kernel
 constexpr int kWarps = kThreads / 32;
+constexpr int kStatWarps = 8;                          // statistics kernel: consumer warps
+constexpr int kStatThreads = (kStatWarps + 1) * 32;   // + one producer warp
+constexpr int kStatStages = 6;
+constexpr int kPartBytes = 16384;                      // one statistics item: 16 KB of one row
 constexpr int kMaxQ = 64;
 constexpr int kMaxRows = 2 * kMaxQ;  // target + draft rows of one sequence
 constexpr int kMaxChunk = 16384;     // vocabulary elements per CTA
 constexpr int kGroup = 8;            // consecutive elements of a group
-
-// Phase 1 work item: one warp, LOADS loads of N elements per lane (2 KB).
-template <typename T, bool VEC> struct ItemCfg;
-template <> struct ItemCfg<__nv_bfloat16, true> { static constexpr int N = 8, LOADS = 4; };
-template <> struct ItemCfg<float, true> { static constexpr int N = 4, LOADS = 4; };
-template <typename T> struct ItemCfg<T, false> { static constexpr int N = 1, LOADS = 16; };
-template <typename T, bool VEC> __host__ __device__ constexpr int item_elems() {
-  return 32 * ItemCfg<T, VEC>::N * ItemCfg<T, VEC>::LOADS;
-}
-
-template <typename T, bool VEC> struct Raw;
-template <typename T> struct Raw<T, true> { uint4 v; };
-template <typename T> struct Raw<T, false> { T v; };
-
-template <typename T, bool VEC>
-__device__ __forceinline__ float elem(const Raw<T, VEC> &r, int k) {
-  if constexpr (VEC) return to_f32(reinterpret_cast<const T *>(&r.v)[k]);
-  else return to_f32(r.v);
-}
-
-// The lane's loads of one item: load u covers e0 + (u*32 + lane)*N .. +N.
-// Chunks are multiples of N, so a load is wholly inside or outside [e0, e1).
-template <typename T, bool VEC>
-__device__ __forceinline__ void load_item(const T *__restrict__ row, int e0, int e1, int lane,
-                                          Raw<T, VEC> (&raw)[ItemCfg<T, VEC>::LOADS], int &nvalid) {
-  constexpr int N = ItemCfg<T, VEC>::N, LOADS = ItemCfg<T, VEC>::LOADS;
-  nvalid = 0;
-#pragma unroll
-  for (int u = 0; u < LOADS; ++u) {
-    const int e = e0 + (u * 32 + lane) * N;
-    if (e < e1) {
-      if constexpr (VEC) raw[u].v = __ldg(reinterpret_cast<const uint4 *>(row + e));
-      else raw[u].v = row[e];
-      nvalid = u + 1;
-    }
-  }
-}
 
 // 2^x by the MUFU approximation (flush-to-zero; relative error about 2^-22)
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -131,8 +104,18 @@ __device__ __forceinline__ float exp2_acc(float d, float c_hi, float c_lo) {
 }
 
 // Weights in [0, 1] as 64-bit fixed point with 40 fractional bits: sums of up
-// to 2^23 of them are exact and independent of the order of addition.
-__device__ __forceinline__ long long to_fix(float w) { return __float2ll_rn(w * 1099511627776.0f); }
+// to 2^23 of them are exact and independent of the order of addition. The
+// value is round-to-nearest-even of w 2^40, formed from two 20-bit halves with
+// single-precision adds (a float in [2^23, 2^24) has unit spacing, so adding
+// 2^23 rounds to an integer that its low mantissa bits hold): float-to-64-bit
+// conversions run on a slow unit, these adds on the fast one.
+__device__ __forceinline__ long long to_fix(float w) {
+  const float t = w * 1048576.0f;                      // w 2^20, exact, in [0, 2^20]
+  const float h = __fadd_rd(t, 8388608.0f);            // 2^23 + floor(t)
+  const float r = (t - (h - 8388608.0f)) * 1048576.0f;  // frac(t) 2^20, exact, in [0, 2^20)
+  const float l = __fadd_rn(r, 8388608.0f);            // 2^23 + rint(r)
+  return ((long long)(__float_as_int(h) - 0x4B000000) << 20) + (__float_as_int(l) - 0x4B000000);
+}
 
 __device__ long long block_sum_ll(long long x, long long *buf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -202,18 +185,266 @@ __device__ __forceinline__ void group8(const T *buf, int g, int n, float (&x)[kG
   }
 }
 
+
+// ===========================================================================
+// Row statistics: every target row (and, for T > 0, every draft row) cut into
+// items of 16 KB, the items of the launch cut into equal contiguous ranges,
+// one per CTA. A producer warp streams a CTA's items through a 6-stage ring of
+// 1-D bulk copies; eight consumer warps each reduce an eighth of every item.
+// A lane keeps a running (max, sum of 2^(x c - max c)) or argmax of the
+// current row; where a warp's run of items leaves a row the warp reduces it and
+// writes it as the partial of (the run's first item, warp); every other
+// (item, warp) partial is written as the identity, so each launch writes all
+// of them and nothing needs to start at zero.
+// ===========================================================================
+struct StatsArgs {
+  const void *tgt, *drf;
+  float *pm, *ps;  // [items][kStatWarps]: max (or best value), sum (or best index bits)
+  int32_t *status;
+  int vocab, total_q, rows, nchunk, items, per;
+  float coef;
+};
+
+template <typename T, bool VEC, int MODE>
+__global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
+  constexpr int CH = kPartBytes / (int)sizeof(T);  // elements of an item
+  constexpr int SL = CH / kStatWarps;              // elements of a warp's slice
+  extern __shared__ __align__(128) uint8_t ring[];  // kStatStages x kPartBytes
+  __shared__ uint64_t full[kStatStages], empty[kStatStages];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = blockIdx.x * A.per, i1 = min(A.items, i0 + A.per);
+  const int V = A.vocab;
+  const T *tgt = reinterpret_cast<const T *>(A.tgt);
+  const T *drf = reinterpret_cast<const T *>(A.drf);
+  auto row_ptr = [&](int r) -> const T * {
+    return r < A.total_q ? tgt + (size_t)r * V : drf + (size_t)(r - A.total_q) * V;
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kStatStages; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[s])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[s])), "r"(kStatWarps)
+                   : "memory");
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  bool ok = true;
+
+  if (warp == kStatWarps) {
+    // ---------------- producer ----------------
+    if (VEC && lane == 0) {
+      for (int it = i0, j = 0; it < i1; ++it, ++j) {
+        const int s = j % kStatStages;
+        if (j >= kStatStages && !mbar_wait_bounded(smem_addr(&empty[s]), ((j / kStatStages) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int r = it / A.nchunk, k = it - r * A.nchunk;
+        const int e0 = k * CH, cnt = min(CH, V - e0);
+        const uint32_t bytes = static_cast<uint32_t>(cnt * sizeof(T));
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&full[s])), "r"(bytes)
+                     : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         smem_addr(ring + s * kPartBytes)),
+                     "l"(row_ptr(r) + e0), "r"(bytes), "r"(smem_addr(&full[s]))
+                     : "memory");
+      }
+    }
+  } else {
+    // ---------------- consumers: warp w reduces elements [w SL, (w + 1) SL) of each item ----------------
+    int bad = 0;
+    float lm = -INFINITY, ls = 0.f;  // stochastic: running max, sum of 2^(x c - lm c)
+    float lb = 0.f;                  // greedy: best value and index
+    int lbi = -1;
+    int cur_row = -1, run_start = -1;
+    auto flush = [&]() {  // warp-uniform: the run's statistics into (run_start, warp)
+      if constexpr (MODE == kStochastic) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, lm, o);
+          const float s2 = __shfl_xor_sync(0xffffffffu, ls, o);
+          ms_combine(lm, ls, m2, s2, A.coef);
+        }
+        if (lane == 0) {
+          A.pm[(size_t)run_start * kStatWarps + warp] = lm;
+          A.ps[(size_t)run_start * kStatWarps + warp] = ls;
+        }
+        lm = -INFINITY;
+        ls = 0.f;
+      } else {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float v2 = __shfl_xor_sync(0xffffffffu, lb, o);
+          const int i2 = __shfl_xor_sync(0xffffffffu, lbi, o);
+          am_combine(lb, lbi, v2, i2);
+        }
+        if (lane == 0) {
+          A.pm[(size_t)run_start * kStatWarps + warp] = lb;
+          A.ps[(size_t)run_start * kStatWarps + warp] = __int_as_float(lbi);
+        }
+        lb = 0.f;
+        lbi = -1;
+      }
+    };
+    for (int it = i0, j = 0; it < i1; ++it, ++j) {
+      const int s = j % kStatStages;
+      const int r = it / A.nchunk, k = it - r * A.nchunk;
+      const int e0 = k * CH, cnt = min(CH, V - e0);
+      if (r != cur_row) {
+        if (cur_row >= 0) flush();
+        cur_row = r;
+        run_start = it;
+      } else if (lane == 0) {  // not a run's first item: the identity
+        A.pm[(size_t)it * kStatWarps + warp] = (MODE == kStochastic) ? -INFINITY : 0.f;
+        A.ps[(size_t)it * kStatWarps + warp] = (MODE == kStochastic) ? 0.f : __int_as_float(-1);
+      }
+      const T *src;
+      if constexpr (VEC) {
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[s]), (j / kStatStages) & 1));
+        src = reinterpret_cast<const T *>(ring + s * kPartBytes);
+      } else {
+        src = row_ptr(r) + e0;  // rows not 16-byte aligned: scalar loads straight from memory
+      }
+      // this lane's elements: groups of 8 at slice offset 8 * (lane + 32 u); -inf past the item
+      const int s0 = warp * SL;
+      if (ok && s0 < cnt) {
+        if constexpr (VEC && sizeof(T) == 2 && MODE == kStochastic) {
+          // bf16 pairs: the maximum on packed pairs (NaN-propagating), the sum on floats
+          uint32_t w[SL / 64];
+#pragma unroll
+          for (int u = 0; u < SL / 256; ++u) {
+            const int e = s0 + 8 * (lane + 32 * u);
+            const uint4 q = *reinterpret_cast<const uint4 *>(src + e);
+            w[4 * u] = q.x;
+            w[4 * u + 1] = q.y;
+            w[4 * u + 2] = q.z;
+            w[4 * u + 3] = q.w;
+            if (e + 8 > cnt) {
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                if (e + 2 * p >= cnt) w[4 * u + p] = (w[4 * u + p] & 0xffff0000u) | 0xff80u;
+                if (e + 2 * p + 1 >= cnt) w[4 * u + p] = (w[4 * u + p] & 0xffffu) | 0xff800000u;
+              }
+            }
+          }
+          __nv_bfloat162 m2 = __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));
+#pragma unroll
+          for (int q = 0; q < SL / 64; ++q) m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162 *>(&w[q]));
+          const float ma = __low2float(m2), mb = __high2float(m2);
+          const float mi = (ma != ma || mb != mb) ? NAN : fmaxf(ma, mb);
+          bad |= (mi != mi) | (mi == INFINITY);
+          if (mi == mi && mi != -INFINITY) {
+            if (mi > lm) {
+              ls = (lm == -INFINITY) ? 0.f : ls * fast_exp2((lm - mi) * A.coef);
+              lm = mi;
+            }
+            const float nmc = -lm * A.coef;
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int q = 0; q < SL / 64; ++q) {
+              acc0 += fast_exp2(fmaf(__uint_as_float(w[q] << 16), A.coef, nmc));
+              acc1 += fast_exp2(fmaf(__uint_as_float(w[q] & 0xffff0000u), A.coef, nmc));
+            }
+            ls += acc0 + acc1;
+          }
+        } else {
+        float x[SL / 32];
+#pragma unroll
+        for (int u = 0; u < SL / 256; ++u) {
+          const int e = s0 + 8 * (lane + 32 * u);
+          if constexpr (VEC && sizeof(T) == 2) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(src + e);
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(&q);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              x[8 * u + 2 * p] = __uint_as_float(w[p] << 16);
+              x[8 * u + 2 * p + 1] = __uint_as_float(w[p] & 0xffff0000u);
+            }
+          } else if constexpr (VEC) {
+            const uint4 q0 = *reinterpret_cast<const uint4 *>(src + e);
+            const uint4 q1 = *reinterpret_cast<const uint4 *>(src + e + 4);
+            const float *f0 = reinterpret_cast<const float *>(&q0), *f1 = reinterpret_cast<const float *>(&q1);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              x[8 * u + p] = f0[p];
+              x[8 * u + 4 + p] = f1[p];
+            }
+          } else {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) x[8 * u + p] = (e + p < cnt) ? to_f32(src[e + p]) : -INFINITY;
+          }
+          if (e + 8 > cnt) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+              if (e + p >= cnt) x[8 * u + p] = -INFINITY;
+          }
+        }
+        if constexpr (MODE == kStochastic) {
+          float mi = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < SL / 32; ++q) mi = (x[q] != x[q] || mi != mi) ? NAN : fmaxf(mi, x[q]);
+          bad |= (mi != mi) | (mi == INFINITY);
+          if (mi == mi && mi != -INFINITY) {
+            if (mi > lm) {
+              ls = (lm == -INFINITY) ? 0.f : ls * fast_exp2((lm - mi) * A.coef);
+              lm = mi;
+            }
+            const float nmc = -lm * A.coef;
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < SL / 32; ++q) acc += fast_exp2(fmaf(x[q], A.coef, nmc));
+            ls += acc;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < SL / 256; ++u) {
+            const int e = s0 + 8 * (lane + 32 * u);
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              const float v = x[8 * u + p];
+              bad |= (v != v);
+              if (e + p < cnt) am_combine(lb, lbi, v, e0 + e + p);
+            }
+          }
+        }
+        }
+      }
+      if constexpr (VEC) {
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty[s])) : "memory");
+      }
+    }
+    if (cur_row >= 0) flush();
+    if (bad) record(A.status, SV_ERR_NONFINITE);
+    if (!ok) record(A.status, SV_ERR_TIMEOUT);
+  }
+  // after a failed wait, let the producer's copies in flight land before shared memory is released
+  const bool any_fail = __syncthreads_or(!ok);
+  if (VEC && any_fail && tid == kStatWarps * 32) {
+    const int n = i1 - i0;
+    for (int j = max(0, n - kStatStages); j < n; ++j)
+      mbar_wait_bounded(smem_addr(&full[j % kStatStages]), (j / kStatStages) & 1);
+  }
+}
+
+
+// ===========================================================================
+// Decisions: one cluster per sequence (C CTAs for T > 0, one CTA for greedy
+// and tree). Every CTA combines its sequence's row partials in the same fixed
+// order (one warp per row), so all CTAs hold identical row statistics and take
+// identical decisions; for T > 0 the draw runs over the C vocabulary chunks.
+// ===========================================================================
 struct Smem {
   uint64_t pair;  // phase 3 row pair
-  float rm[kMaxRows];  // per row, this CTA's chunk (cluster-visible)
-  float rs[kMaxRows];
-  int ri[kMaxRows];
-  float tl[kMaxQ];  // target logit of the draft token, if this CTA owns it (cluster-visible)
-  float dl[kMaxQ];
-  float M[kMaxRows];  // per row, whole vocabulary (after phase 2)
+  float M[kMaxRows];  // per row, whole vocabulary
   float Z[kMaxRows];
   int am[kMaxRows];
-  float gtl[kMaxQ], gdl[kMaxQ];
-  long long zt, zd;  // phase 3: this CTA's fixed-point normalisers (cluster-visible)
+  float gtl[kMaxQ], gdl[kMaxQ];  // target and draft logits of the draft tokens
+  float uacc[kMaxQ];             // accept uniforms
+  int tok[kMaxQ];                // draft tokens (chain) or node tokens (tree)
+  int par[kMaxQ];                // tree: parent row of each row
   long long S[2];    // phase 3: this CTA's fixed-point weight sum per pass (cluster-visible)
   long long ll_buf[kWarps];
   long long P_owner, target;
@@ -225,11 +456,10 @@ struct Smem {
 };
 
 template <typename T, bool VEC, int MODE>
-__global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int ring_bytes) {
+__global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, const float *__restrict__ pm,
+                                                          const float *__restrict__ ps, int nchunk, int ring_bytes) {
   grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   grid_dependents_launch();
-  constexpr int IE = item_elems<T, VEC>();
-  constexpr int LOADS = ItemCfg<T, VEC>::LOADS, N = ItemCfg<T, VEC>::N;
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -237,10 +467,7 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ Smem sm;
   extern __shared__ __align__(128) uint8_t dyn[];
-  // phase 1: per-row partials [kMaxRows][kWarps] x 2; phase 3: the row pair (same bytes)
-  uint8_t *ring = dyn;
-  float *pm = reinterpret_cast<float *>(dyn);
-  float *ps = pm + kMaxRows * kWarps;
+  uint8_t *ring = dyn;                                                   // phase 3: the row pair
   long long *gmass = reinterpret_cast<long long *>(dyn + ring_bytes);  // phase 3: per-group mass
 
   const int V = args.vocab;
@@ -266,224 +493,75 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pair)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
   bool ok = true;  // false after a bounded wait gave up: the remaining work is skipped, barriers are kept
 
-  // ---------------- phase 1: per-row statistics of this CTA's chunk ----------------
-  // The items (2 KB of one row, row-major) are cut into kWarps contiguous runs, one
-  // per warp. A lane accumulates its share of the current row online; the warp
-  // reduces only where its run leaves a row, into slot [row][warp]. The next
-  // item's loads are in flight while the current one is reduced.
-  const int nsub = (len + IE - 1) / IE;
-  const int items = rows * nsub;
-  const int it_begin = (int)((long long)items * warp / kWarps);
-  const int it_end = (int)((long long)items * (warp + 1) / kWarps);
-  for (int x = tid; x < rows * kWarps; x += kThreads) {
-    pm[x] = (MODE == kStochastic) ? -INFINITY : 0.f;
-    ps[x] = (MODE == kStochastic) ? 0.f : __int_as_float(-1);
-  }
-  __syncthreads();
-  int bad = 0;
-  float lm = -INFINITY, ls = 0.f;  // stochastic: this lane's running max and sum of 2^((x - lm) c)
-  float lb = 0.f;                  // greedy: this lane's best value and its index
-  int lbi = -1;
-  int cur_row = -1;
-  auto flush = [&]() {  // warp-uniform: the lanes' state of cur_row into slot [cur_row][warp]
-    if constexpr (MODE == kStochastic) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, lm, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, ls, o);
-        ms_combine(lm, ls, m2, s2, coef);
-      }
-      if (lane == 0) {
-        pm[cur_row * kWarps + warp] = lm;
-        ps[cur_row * kWarps + warp] = ls;
-      }
-      lm = -INFINITY;
-      ls = 0.f;
-    } else {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, lb, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, lbi, o);
-        am_combine(lb, lbi, v2, i2);
-      }
-      if (lane == 0) {
-        pm[cur_row * kWarps + warp] = lb;
-        ps[cur_row * kWarps + warp] = __int_as_float(lbi);
-      }
-      lb = 0.f;
-      lbi = -1;
-    }
-  };
-  // this lane's elements of item it into the running state
-  auto reduce_item = [&](int it, const Raw<T, VEC> (&raw)[LOADS], int nv) {
-    const int r = it / nsub, sub = it % nsub;
-    if (r != cur_row) {
-      if (cur_row >= 0) flush();
-      cur_row = r;
-    }
-    const int e0 = lo + sub * IE;
-    if constexpr (MODE == kStochastic) {
-      float mi;
-      if constexpr (VEC && sizeof(T) == 2) {
-        // bf16 pairs: the maximum on packed pairs, NaN propagating
-        __nv_bfloat162 mx2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-#pragma unroll
-        for (int u = 0; u < LOADS; ++u)
-          if (u < nv) {
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw[u].v);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mx2 = __hmax2_nan(mx2, h[k]);
-          }
-        const float l2 = __low2float(mx2), h2 = __high2float(mx2);
-        mi = (l2 != l2 || h2 != h2) ? NAN : fmaxf(l2, h2);
-      } else {
-        mi = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < LOADS; ++u)
-          if (u < nv)
-#pragma unroll
-            for (int k = 0; k < N; ++k) {
-              const float x = elem<T, VEC>(raw[u], k);
-              mi = (x != x || mi != mi) ? NAN : fmaxf(mi, x);
-            }
-      }
-      bad |= (mi != mi) | (mi == INFINITY);
-      if (!(mi == mi) || mi == -INFINITY) return;  // nothing to add (or the row is reported)
-      if (mi > lm) {
-        ls = (lm == -INFINITY) ? 0.f : ls * fast_exp2((lm - mi) * coef);
-        lm = mi;
-      }
-      const float nmc = -lm * coef;
-      float acc = 0.f;
-      if constexpr (VEC && sizeof(T) == 2) {
-#pragma unroll
-        for (int u = 0; u < LOADS; ++u)
-          if (u < nv) {
-            const uint32_t *w = reinterpret_cast<const uint32_t *>(&raw[u].v);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              acc += fast_exp2(fmaf(__uint_as_float(w[k] << 16), coef, nmc));
-              acc += fast_exp2(fmaf(__uint_as_float(w[k] & 0xffff0000u), coef, nmc));
-            }
-          }
-      } else {
-#pragma unroll
-        for (int u = 0; u < LOADS; ++u)
-          if (u < nv)
-#pragma unroll
-            for (int k = 0; k < N; ++k) acc += fast_exp2(fmaf(elem<T, VEC>(raw[u], k), coef, nmc));
-      }
-      ls += acc;
-    } else {
-#pragma unroll
-      for (int u = 0; u < LOADS; ++u)
-        if (u < nv)
-#pragma unroll
-          for (int k = 0; k < N; ++k) {
-            const float x = elem<T, VEC>(raw[u], k);
-            bad |= (x != x);
-            am_combine(lb, lbi, x, e0 + (u * 32 + lane) * N + k);
-          }
-    }
-  };
-  auto fetch = [&](int it, Raw<T, VEC> (&raw)[LOADS], int &nv) {
-    const int r = it / nsub, sub = it % nsub;
-    const T *row = (r < n) ? tgt + (size_t)(t0 + r) * V : drf + (size_t)(d0 + (r - n)) * V;
-    const int e0 = lo + sub * IE;
-    load_item<T, VEC>(row, e0, min(hi, e0 + IE), lane, raw, nv);
-  };
-  {
-    Raw<T, VEC> ra[LOADS], rb[LOADS];
-    int na = 0, nb = 0;
-    int it = it_begin;
-    if (it < it_end) fetch(it, ra, na);
-    while (it < it_end) {
-      if (it + 1 < it_end) fetch(it + 1, rb, nb);
-      reduce_item(it, ra, na);
-      if (++it >= it_end) break;
-      if (it + 1 < it_end) fetch(it + 1, ra, na);
-      reduce_item(it, rb, nb);
-      ++it;
-    }
-    if (cur_row >= 0) flush();
-  }
-  __syncthreads();
-  for (int r = tid; r < rows; r += kThreads) {
-    if constexpr (MODE == kStochastic) {
-      float m = -INFINITY, sum = 0.f;
-      for (int w = 0; w < kWarps; ++w) ms_combine(m, sum, pm[r * kWarps + w], ps[r * kWarps + w], coef);
-      sm.rm[r] = m;
-      sm.rs[r] = sum;
-    } else {
-      float best = 0.f;
-      int bi = -1;
-      for (int w = 0; w < kWarps; ++w) am_combine(best, bi, pm[r * kWarps + w], __float_as_int(ps[r * kWarps + w]));
-      sm.rm[r] = best;
-      sm.ri[r] = bi;
-    }
-  }
-  // token logits of the draft tokens this CTA owns
-  if constexpr (MODE == kStochastic) {
-    if (tid < K) {
-      const int x = args.draft_tok[d0 + tid];
-      if (x < 0 || x >= V) {
-        record(args.status, SV_ERR_BAD_TOKEN);
-      } else if (x >= lo && x < hi) {
-        sm.tl[tid] = to_f32(tgt[(size_t)(t0 + tid) * V + x]);
-        sm.dl[tid] = to_f32(drf[(size_t)(d0 + tid) * V + x]);
-      }
-    }
-  }
-  if (bad) atomicOr(&sm.bad, 1);
-  __syncthreads();
-  if (tid == 0 && sm.bad) record(args.status, SV_ERR_NONFINITE);
-  cluster.sync();
-
-  // ---------------- phase 2: combine across the cluster, one lane per rank ----------------
-  for (int base = 0; base < rows * 16; base += kThreads) {
-    const int x = base + tid, r = x >> 4, q = x & 15;
-    const bool valid = x < rows * 16 && q < C;
+  // ---------------- row statistics from the partials: one warp per row ----------------
+  for (int r = warp; r < rows; r += kWarps) {
+    const int gr = r < n ? t0 + r : args.total_q + d0 + (r - n);  // row of the statistics kernel
+    const size_t p0 = (size_t)gr * nchunk * kStatWarps;
+    const int np = nchunk * kStatWarps;
     if constexpr (MODE == kStochastic) {
       float m = -INFINITY, s = 0.f;
-      if (valid) {
-        m = *cluster.map_shared_rank(&sm.rm[r], q);
-        s = *cluster.map_shared_rank(&sm.rs[r], q);
+      for (int q0 = 0; q0 < np; q0 += 128) {  // four loads of each array in flight per lane
+        float lm[4], lsum[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int q = q0 + 32 * j + lane;
+          lm[j] = q < np ? pm[p0 + q] : -INFINITY;
+          lsum[j] = q < np ? ps[p0 + q] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ms_combine(m, s, lm[j], lsum[j], coef);
       }
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
+      for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
         const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
         ms_combine(m, s, m2, s2, coef);
       }
-      if (x < rows * 16 && q == 0) {
+      if (lane == 0) {
         sm.M[r] = m;
         sm.Z[r] = s;
       }
     } else {
       float best = 0.f;
       int bi = -1;
-      if (valid) {
-        best = *cluster.map_shared_rank(&sm.rm[r], q);
-        bi = *cluster.map_shared_rank(&sm.ri[r], q);
+      for (int q0 = 0; q0 < np; q0 += 128) {
+        float lv[4];
+        int li[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int q = q0 + 32 * j + lane;
+          lv[j] = q < np ? pm[p0 + q] : 0.f;
+          li[j] = q < np ? __float_as_int(ps[p0 + q]) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) am_combine(best, bi, lv[j], li[j]);
       }
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
+      for (int o = 16; o > 0; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
         const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
         am_combine(best, bi, v2, i2);
       }
-      if (x < rows * 16 && q == 0) sm.am[r] = bi;
+      if (lane == 0) sm.am[r] = bi;
     }
   }
+  // the sequence's small inputs into shared memory, so the serial scans below read no global memory
+  if (tid < K) sm.tok[tid] = args.draft_tok[d0 + tid];
+  if (MODE == kTree && tid < n) sm.par[tid] = args.parent[t0 + tid];
   if constexpr (MODE == kStochastic) {
-    if (tid < K) {
+    if (tid < K) {  // the accept uniform and the target and draft logits of each draft token
+      sm.uacc[tid] = args.u_acc[d0 + tid];
       const int x = args.draft_tok[d0 + tid];
-      const int owner = (x >= 0 && x < V) ? min(x / args.chunk, C - 1) : 0;
-      sm.gtl[tid] = *cluster.map_shared_rank(&sm.tl[tid], owner);
-      sm.gdl[tid] = *cluster.map_shared_rank(&sm.dl[tid], owner);
+      if (x < 0 || x >= V) {
+        if (rank == 0) record(args.status, SV_ERR_BAD_TOKEN);
+        sm.gtl[tid] = 0.f;
+        sm.gdl[tid] = 0.f;
+      } else {
+        sm.gtl[tid] = to_f32(tgt[(size_t)(t0 + tid) * V + x]);
+        sm.gdl[tid] = to_f32(drf[(size_t)(d0 + tid) * V + x]);
+      }
     }
   }
   __syncthreads();
@@ -492,12 +570,12 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
     if (rank == 0 && tid == 0) {
       int a = K;
       for (int i = 0; i < K; ++i)
-        if (args.draft_tok[d0 + i] != sm.am[i]) {
+        if (sm.tok[i] != sm.am[i]) {
           a = i;
           break;
         }
       int32_t *o = args.out_tok + (size_t)b * args.max_q;
-      for (int j = 0; j < args.max_q; ++j) o[j] = j < a ? args.draft_tok[d0 + j] : -1;
+      for (int j = 0; j < args.max_q; ++j) o[j] = j < a ? sm.tok[j] : -1;
       o[a] = sm.am[a];
       args.accept[b] = a;
       args.num_out[b] = a + 1;
@@ -513,7 +591,7 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
       int cur = 0, a = 0, am = sm.am[0];
       bool good = true;
       for (int j = 1; j < n; ++j) {
-        const int p = args.parent[t0 + j];
+        const int p = sm.par[j];
         good &= (p >= 0 && p < n && p != j);
       }
       if (!good) record(args.status, SV_ERR_BAD_LENGTH);
@@ -521,7 +599,7 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
         am = sm.am[cur];
         int next = -1;
         for (int j = 1; j < n; ++j)
-          if (args.parent[t0 + j] == cur && args.draft_tok[d0 + j - 1] == am) {
+          if (sm.par[j] == cur && sm.tok[j - 1] == am) {
             next = j;
             break;
           }
@@ -545,7 +623,7 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
         const float p = exp2f((sm.gtl[i] - sm.M[i]) * coef) / Zt;
         const float q = exp2f((sm.gdl[i] - sm.M[n + i]) * coef) / Zd;
         const float thr = q > 0.f ? fminf(1.f, p / q) : 1.f;
-        if (!(args.u_acc[d0 + i] < thr)) {
+        if (!(sm.uacc[i] < thr)) {
           a = i;
           break;
         }
@@ -554,6 +632,10 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
       for (int r = 0; r < rows; ++r)
         if (!(sm.Z[r] > 0.f)) sm.bad = 1;
       if (sm.bad && rank == 0) record(args.status, SV_ERR_NONFINITE);
+      // a residual draw weighs q_v as e_d (Z_t / Z_d) against e_t, the ratio carried as hi + lo
+      const double rho = a < K && sm.Z[n + a] > 0.f ? (double)sm.Z[a] / (double)sm.Z[n + a] : 0.0;
+      sm.rho_hi = (float)rho;
+      sm.rho_lo = (float)(rho - (double)sm.rho_hi);
     }
     __syncthreads();
     const int a = sm.a;
@@ -603,48 +685,6 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
     }
     __syncthreads();
 
-    // ---- pass A: fixed-point normalisers of the row pair (residual draws) ----
-    if (resid) {
-      long long zt = 0, zd = 0;
-      if (ok) {
-        for (int g = tid; g < ngroups; g += kThreads) {
-          float xt[kGroup], xd[kGroup];
-          group8<T>(bt, g, len, xt);
-          group8<T>(bd, g, len, xd);
-#pragma unroll
-          for (int k = 0; k < kGroup; ++k) {
-            zt += to_fix(exp2_acc(xt[k] - Mt, chi, clo));
-            zd += to_fix(exp2_acc(xd[k] - Md, chi, clo));
-          }
-        }
-      }
-      zt = block_sum_ll(zt, sm.ll_buf);
-      zd = block_sum_ll(zd, sm.ll_buf);
-      if (tid == 0) {
-        sm.zt = zt;
-        sm.zd = zd;
-      }
-    }
-    cluster.sync();
-    if (resid && warp == 0) {
-      long long Zt = 0, Zd = 0;
-      if (lane < C) {
-        Zt = *cluster.map_shared_rank(&sm.zt, lane);
-        Zd = *cluster.map_shared_rank(&sm.zd, lane);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        Zt += __shfl_xor_sync(0xffffffffu, Zt, o);
-        Zd += __shfl_xor_sync(0xffffffffu, Zd, o);
-      }
-      if (lane == 0) {
-        // q_v enters as e_d * (Z_t / Z_d), carried as hi + lo
-        const double rho = Zd > 0 ? (double)Zt / (double)Zd : 0.0;
-        sm.rho_hi = (float)rho;
-        sm.rho_lo = (float)(rho - (double)sm.rho_hi);
-      }
-    }
-    __syncthreads();
     const float rho_hi = sm.rho_hi, rho_lo = sm.rho_lo;
 
     for (int pass = 0; pass < 2; ++pass) {
@@ -764,7 +804,7 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
             }
           }
           int32_t *o = args.out_tok + (size_t)b * args.max_q;
-          for (int j = 0; j < args.max_q; ++j) o[j] = j < a ? args.draft_tok[d0 + j] : -1;
+          for (int j = 0; j < args.max_q; ++j) o[j] = j < a ? sm.tok[j] : -1;
           o[a] = y;
           args.accept[b] = a;
           args.num_out[b] = a + 1;
@@ -776,8 +816,9 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(SamplerArgs args, int
   cluster.sync();  // keep this CTA's shared memory alive until every peer is done reading it
 }
 
-// Cluster size: enough CTAs to cover the SMs a few times over, and chunks of at
-// most kMaxChunk elements.
+
+// Decision cluster size for T > 0: enough CTAs to cover the SMs a few times
+// over, and chunks of at most kMaxChunk elements.
 int pick_cluster(int batch, int vocab) {
   const int sms = num_sms();
   int C = (batch * 8 < 3 * sms) ? 16 : 8;
@@ -786,16 +827,47 @@ int pick_cluster(int batch, int vocab) {
 }
 
 template <typename T, bool VEC, int MODE>
-cudaError_t launch_t(const SamplerArgs &a, int C, cudaStream_t st) {
-  auto kern = sampler_kernel<T, VEC, MODE>;
-  const int pair = ((a.chunk * (int)sizeof(T) + 127) / 128) * 128;
-  const int ring = std::max(2 * kMaxRows * kWarps * (int)sizeof(float), 2 * pair);
-  const int groups = (a.chunk + kGroup - 1) / kGroup;
-  const int dyn = ring + groups * (int)sizeof(long long);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int rows, cudaStream_t st) {
+  // ---- statistics ----
+  const int items = rows * nchunk;
+  const int want = std::max(1, std::min(items, 2 * num_sms()));
+  const int per = (items + want - 1) / want;
+  const int grid = (items + per - 1) / per;
+  StatsArgs sa;
+  sa.tgt = a.tgt;
+  sa.drf = a.drf;
+  sa.pm = pm;
+  sa.ps = ps;
+  sa.status = a.status;
+  sa.vocab = a.vocab;
+  sa.total_q = a.total_q;
+  sa.rows = rows;
+  sa.nchunk = nchunk;
+  sa.items = items;
+  sa.per = per;
+  sa.coef = a.coef;
+  auto skern = stats_kernel<T, VEC, MODE>;
+  const int sdyn = VEC ? kStatStages * kPartBytes : 0;
+  cudaError_t e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, sdyn);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(skern, dim3(grid), dim3(kStatThreads), sdyn, st, sa);
+  if (e != cudaSuccess) return e;
+
+  // ---- decisions ----
+  const int C = MODE == kStochastic ? pick_cluster(a.batch, a.vocab) : 1;
+  SamplerArgs da = a;
+  da.chunk = ((a.vocab + C - 1) / C + 7) / 8 * 8;
+  auto dkern = decide_kernel<T, VEC, MODE>;
+  int ring = 0, dyn = 0;
+  if (MODE == kStochastic) {
+    const int pair = ((da.chunk * (int)sizeof(T) + 127) / 128) * 128;
+    ring = 2 * pair;
+    dyn = ring + (da.chunk + kGroup - 1) / kGroup * (int)sizeof(long long);
+  }
+  e = cudaFuncSetAttribute(dkern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
   if (C > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(dkern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -812,38 +884,58 @@ cudaError_t launch_t(const SamplerArgs &a, int C, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a, ring);
+  return cudaLaunchKernelEx(&cfg, dkern, da, static_cast<const float *>(pm), static_cast<const float *>(ps), nchunk,
+                            ring);
 }
 
-// rows 16-byte aligned: vector loads and 1-D bulk copies (every chunk then starts on
-// 16 bytes and is a multiple of 16 bytes long); otherwise scalar loads and copies
+// rows 16-byte aligned: 1-D bulk copies (every item and chunk then starts on 16
+// bytes and is a multiple of 16 bytes long); otherwise scalar loads
 template <typename T, int MODE>
-cudaError_t launch_m(const SamplerArgs &a, int C, cudaStream_t st) {
+cudaError_t launch_m(const SamplerArgs &a, float *pm, float *ps, int nchunk, int rows, cudaStream_t st) {
   const bool vec = ((size_t)a.vocab * sizeof(T)) % 16 == 0 && ((uintptr_t)a.tgt % 16 == 0) &&
                    (a.drf == nullptr || (uintptr_t)a.drf % 16 == 0);
-  return vec ? launch_t<T, true, MODE>(a, C, st) : launch_t<T, false, MODE>(a, C, st);
+  return vec ? launch_t<T, true, MODE>(a, pm, ps, nchunk, rows, st)
+             : launch_t<T, false, MODE>(a, pm, ps, nchunk, rows, st);
 }
 
 template <typename T>
-cudaError_t launch_d(const SamplerArgs &a, int mode, int C, cudaStream_t st) {
+cudaError_t launch_d(const SamplerArgs &a, int mode, float *pm, float *ps, int nchunk, int rows, cudaStream_t st) {
   switch (mode) {
-    case kStochastic: return launch_m<T, kStochastic>(a, C, st);
-    case kGreedy: return launch_m<T, kGreedy>(a, C, st);
-    default: return launch_m<T, kTree>(a, C, st);
+    case kStochastic: return launch_m<T, kStochastic>(a, pm, ps, nchunk, rows, st);
+    case kGreedy: return launch_m<T, kGreedy>(a, pm, ps, nchunk, rows, st);
+    default: return launch_m<T, kTree>(a, pm, ps, nchunk, rows, st);
   }
+}
+
+long long stat_rows(int total_q, int batch, int mode) {
+  return mode == kStochastic ? 2LL * total_q - batch : (long long)total_q;
+}
+
+long long stat_chunks(int vocab, int dtype) {
+  const long long es = dtype == SV_DTYPE_BF16 ? 2 : 4;
+  return ((long long)vocab * es + kPartBytes - 1) / kPartBytes;
 }
 
 }  // namespace
 
-cudaError_t launch_sampler(const SamplerArgs &a0, int dtype, int mode, cudaStream_t st) {
-  SamplerArgs a = a0;
-  if (a.batch == 0) return cudaSuccess;
-  const int C = pick_cluster(a.batch, a.vocab);
-  a.chunk = ((a.vocab + C - 1) / C + 7) / 8 * 8;
-  return dtype == SV_DTYPE_BF16 ? launch_d<__nv_bfloat16>(a, mode, C, st) : launch_d<float>(a, mode, C, st);
+size_t sampler_workspace_bytes(int vocab, int dtype, int total_q, int batch, int mode) {
+  if (vocab < 1 || total_q < 0 || batch < 0 || batch > total_q) return 0;
+  const long long parts = stat_rows(total_q, batch, mode) * stat_chunks(vocab, dtype) * kStatWarps;
+  if (parts >= (1LL << 31)) return 0;
+  return (size_t)parts * 2 * sizeof(float);
 }
 
-// Largest vocabulary: 16 chunks of kMaxChunk elements.
+cudaError_t launch_sampler(const SamplerArgs &a, int dtype, int mode, void *workspace, cudaStream_t st) {
+  if (a.batch == 0) return cudaSuccess;
+  const int nchunk = (int)stat_chunks(a.vocab, dtype);
+  const int rows = (int)stat_rows(a.total_q, a.batch, mode);
+  float *pm = static_cast<float *>(workspace);
+  float *ps = pm + (size_t)rows * nchunk * kStatWarps;
+  return dtype == SV_DTYPE_BF16 ? launch_d<__nv_bfloat16>(a, mode, pm, ps, nchunk, rows, st)
+                                : launch_d<float>(a, mode, pm, ps, nchunk, rows, st);
+}
+
+// Largest vocabulary: 16 decision chunks of kMaxChunk elements.
 bool sampler_supports(int vocab) { return vocab <= 16 * kMaxChunk; }
 
 }  // namespace sv

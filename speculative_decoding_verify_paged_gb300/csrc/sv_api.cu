@@ -97,6 +97,15 @@ size_t attn_workspace(const sv_paged_kv *kv, int32_t num_q_heads, int32_t total_
   return need;
 }
 
+// The sampler's partials workspace: present, 256-byte aligned and large enough.
+sv_status check_sampler_workspace(const void *workspace, size_t workspace_bytes, int dtype, int vocab, int batch,
+                                  int total_q, int mode) {
+  const size_t need = sampler_workspace_bytes(vocab, dtype, total_q, batch, mode);
+  if (need == 0) return SV_ERR_UNSUPPORTED;
+  if (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0 || workspace_bytes < need) return SV_ERR_WORKSPACE;
+  return SV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -118,7 +127,7 @@ const char *sv_status_string(int32_t status) {
   }
 }
 
-int32_t sv_version(void) { return 10000; }
+int32_t sv_version(void) { return 20000; }
 
 sv_status sv_set_option(int32_t option, int32_t value) {
   if (option == SV_OPT_ATTN_PATH && value >= SV_ATTN_AUTO && value <= SV_ATTN_WARP_MMA) {
@@ -207,11 +216,19 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
   return cuda_status(launch_attn_combine(a, kv->dtype, st));
 }
 
+size_t sv_spec_rejection_sample_workspace_bytes(int32_t logits_dtype, int32_t vocab, int32_t batch, int32_t total_q,
+                                                float temperature) {
+  if (logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F32) return 0;
+  if (!(temperature >= 0.f) || temperature == INFINITY) return 0;
+  return sampler_workspace_bytes(vocab, logits_dtype, total_q, batch, temperature == 0.f ? kGreedy : kStochastic);
+}
+
 sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_logits, int32_t logits_dtype,
                                    int32_t vocab, int32_t batch, const int32_t *cu_q, int32_t total_q,
                                    int32_t max_q_per_seq, const int32_t *draft_tokens, const float *u_accept,
                                    const float *u_resample, float temperature, int32_t *accept_count,
-                                   int32_t *out_tokens, int32_t *num_out, int32_t *status_dev, void *stream) {
+                                   int32_t *out_tokens, int32_t *num_out, void *workspace, size_t workspace_bytes,
+                                   int32_t *status_dev, void *stream) {
   if (logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F32) return SV_ERR_INVALID_ARG;
   if (vocab < 1 || batch < 0 || batch > 65535 || total_q < batch || max_q_per_seq < 1 || max_q_per_seq > kMaxQ)
     return SV_ERR_INVALID_ARG;
@@ -225,6 +242,9 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
   if (total_q > batch && draft_tokens == nullptr) return SV_ERR_INVALID_ARG;
   if (!greedy && (u_resample == nullptr || (total_q > batch && (draft_logits == nullptr || u_accept == nullptr))))
     return SV_ERR_INVALID_ARG;
+  const sv_status ws = check_sampler_workspace(workspace, workspace_bytes, logits_dtype, vocab, batch, total_q,
+                                               greedy ? kGreedy : kStochastic);
+  if (ws != SV_OK) return ws;
   SamplerArgs a;
   std::memset(&a, 0, sizeof a);
   a.tgt = target_logits;
@@ -246,14 +266,14 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
     a.coef = (float)c;
     a.coef_lo = (float)(c - (double)a.coef);
   }
-  return cuda_status(launch_sampler(a, logits_dtype, greedy ? kGreedy : kStochastic, (cudaStream_t)stream));
+  return cuda_status(launch_sampler(a, logits_dtype, greedy ? kGreedy : kStochastic, workspace, (cudaStream_t)stream));
 }
 
 sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype, int32_t vocab, int32_t batch,
                                 const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq,
                                 const int32_t *node_tokens, const int32_t *parent, int32_t *accept_count,
-                                int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out,
-                                int32_t *status_dev, void *stream) {
+                                int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, void *workspace,
+                                size_t workspace_bytes, int32_t *status_dev, void *stream) {
   if (logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F32) return SV_ERR_INVALID_ARG;
   if (vocab < 1 || batch < 0 || batch > 65535 || total_q < batch || max_q_per_seq < 1 || max_q_per_seq > kMaxQ)
     return SV_ERR_INVALID_ARG;
@@ -263,6 +283,8 @@ sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype,
       path_nodes == nullptr || out_tokens == nullptr || num_out == nullptr)
     return SV_ERR_INVALID_ARG;
   if (total_q > batch && node_tokens == nullptr) return SV_ERR_INVALID_ARG;
+  const sv_status ws = check_sampler_workspace(workspace, workspace_bytes, logits_dtype, vocab, batch, total_q, kTree);
+  if (ws != SV_OK) return ws;
   SamplerArgs a;
   std::memset(&a, 0, sizeof a);
   a.tgt = target_logits;
@@ -278,7 +300,7 @@ sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype,
   a.batch = batch;
   a.max_q = max_q_per_seq;
   a.total_q = total_q;
-  return cuda_status(launch_sampler(a, logits_dtype, kTree, (cudaStream_t)stream));
+  return cuda_status(launch_sampler(a, logits_dtype, kTree, workspace, (cudaStream_t)stream));
 }
 
 sv_status sv_kv_rollback(const sv_paged_kv *kv, const int32_t *cu_q, const int32_t *accept_count,

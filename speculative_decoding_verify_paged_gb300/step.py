@@ -103,6 +103,7 @@ class DeviceStep:
 class StepBuffers:
     attn_out: torch.Tensor
     workspace: Optional[torch.Tensor]
+    sampler_ws: torch.Tensor
     accept: torch.Tensor
     out_tok: torch.Tensor
     num_out: torch.Tensor
@@ -113,9 +114,13 @@ class StepBuffers:
     def make(cls, kv: L.PagedKV, dstep: DeviceStep, max_seq_len: int, device="cuda") -> "StepBuffers":
         ws = L.spec_verify_attn_workspace_bytes(kv, dstep.num_q_heads, dstep.total_q, dstep.max_q, max_seq_len)
         B = dstep.batch
+        temp = 0.0 if dstep.mask_kind == L.SV_MASK_TREE else dstep.temperature
+        sws = L.spec_rejection_sample_workspace_bytes(dstep.target_logits.dtype, int(dstep.target_logits.shape[1]),
+                                                      B, dstep.total_q, temp)
         return cls(
             attn_out=torch.empty_like(dstep.q),
             workspace=torch.empty(max(ws, 16), dtype=torch.uint8, device=device) if ws > 0 else None,
+            sampler_ws=torch.empty(max(sws, 16), dtype=torch.uint8, device=device),
             accept=torch.empty(B, dtype=torch.int32, device=device),
             out_tok=torch.empty((B, dstep.max_q), dtype=torch.int32, device=device),
             num_out=torch.empty(B, dtype=torch.int32, device=device),
@@ -136,12 +141,13 @@ def attention(kv, d: DeviceStep, buf: StepBuffers, max_seq_len: int, stream=None
 def sample(d: DeviceStep, buf: StepBuffers, stream=None):
     if d.mask_kind == L.SV_MASK_TREE:
         L.tree_greedy_accept(d.target_logits, d.cu_q, d.draft_tokens, d.parent, buf.accept, buf.path, buf.out_tok,
-                             buf.num_out, status=buf.status, stream=stream)
+                             buf.num_out, workspace=buf.sampler_ws, status=buf.status, stream=stream)
     else:
         greedy = d.temperature == 0.0
         L.spec_rejection_sample(d.target_logits, None if greedy else d.draft_logits, d.cu_q, d.draft_tokens,
                                 None if greedy else d.u_accept, None if greedy else d.u_resample, d.temperature,
-                                buf.accept, buf.out_tok, buf.num_out, status=buf.status, stream=stream)
+                                buf.accept, buf.out_tok, buf.num_out, workspace=buf.sampler_ws, status=buf.status,
+                                stream=stream)
 
 
 def rollback(kv, d: DeviceStep, buf: StepBuffers, stream=None):
@@ -159,7 +165,7 @@ def run_step(kv: L.PagedKV, d: DeviceStep, buf: StepBuffers, max_seq_len: int, s
 
 def launches_per_step(d: DeviceStep, max_seq_len: int, kv: L.PagedKV) -> int:
     """Kernels the library launches for one run_step (append 2, attention 1 or
-    2, sampler 1, rollback 1 or 2)."""
+    2, sampler 2: statistics and decisions, rollback 1 or 2)."""
     ws = L.spec_verify_attn_workspace_bytes(kv, d.num_q_heads, d.total_q, d.max_q, max_seq_len)
-    n = 2 + (2 if ws > 0 else 1) + 1 + (2 if d.mask_kind == L.SV_MASK_TREE else 1)
+    n = 2 + (2 if ws > 0 else 1) + 2 + (2 if d.mask_kind == L.SV_MASK_TREE else 1)
     return n
