@@ -239,7 +239,7 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
 /*
  * Workspace bytes of sv_spec_rejection_sample for these sizes (temperature 0:
  * greedy, target rows only; also the size for sv_tree_greedy_accept). It is
- * (rows) x ceil(vocab x element size / 16 KB) x 64 bytes, rows = total_q, plus
+ * (rows) x ceil(vocab x element size / 32 KB) x 64 bytes, rows = total_q, plus
  * total_q - batch draft rows when temperature > 0. Returns 0 for invalid sizes
  * or types.
  */

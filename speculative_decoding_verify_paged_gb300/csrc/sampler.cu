@@ -15,10 +15,10 @@
 //
 // How:
 //   statistics  every row of the batch (target rows, then draft rows) is cut
-//               into 16 KB items; the launch's items are cut into equal
+//               into 32 KB items; the launch's items are cut into equal
 //               contiguous ranges, one per persistent CTA, so the whole batch
 //               streams through every SM at once whatever the number of
-//               sequences. A producer warp keeps six items in flight with 1-D
+//               sequences. A producer warp keeps three items in flight with 1-D
 //               bulk copies; eight consumer warps reduce each item to a
 //               (max, sum of 2^((l - max) log2(e)/T)) pair, or to an argmax,
 //               per warp, into a workspace of per-(item, warp) partials.
@@ -58,8 +58,8 @@ constexpr int kThreads = 256;  // decision kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kStatWarps = 8;                          // statistics kernel: consumer warps
 constexpr int kStatThreads = (kStatWarps + 1) * 32;   // + one producer warp
-constexpr int kStatStages = 6;
-constexpr int kPartBytes = 16384;                      // one statistics item: 16 KB of one row
+constexpr int kStatStages = 3;
+constexpr int kPartBytes = 32768;                      // one statistics item: 32 KB of one row
 constexpr int kMaxQ = 64;
 constexpr int kMaxRows = 2 * kMaxQ;  // target + draft rows of one sequence
 constexpr int kMaxChunk = 16384;     // vocabulary elements per CTA
@@ -188,8 +188,8 @@ __device__ __forceinline__ void group8(const T *buf, int g, int n, float (&x)[kG
 
 // ===========================================================================
 // Row statistics: every target row (and, for T > 0, every draft row) cut into
-// items of 16 KB, the items of the launch cut into equal contiguous ranges,
-// one per CTA. A producer warp streams a CTA's items through a 6-stage ring of
+// items of 32 KB, the items of the launch cut into equal contiguous ranges,
+// one per CTA. A producer warp streams a CTA's items through a 3-stage ring of
 // 1-D bulk copies; eight consumer warps each reduce an eighth of every item.
 // A lane keeps a running (max, sum of 2^(x c - max c)) or argmax of the
 // current row; where a warp's run of items leaves a row the warp reduces it and
@@ -450,7 +450,6 @@ struct Smem {
   long long P_owner, target;
   float rho_hi, rho_lo;
   int a;
-  int bad;
   int owner, fallback;
   int y_hit, y_last;
 };
@@ -489,7 +488,6 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
     return;
   }
   if (tid == 0) {
-    sm.bad = 0;
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pair)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -615,27 +613,33 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
       args.num_out[b] = a + 1;
     }
   } else {
-    // ---------------- accept scan (identical in every CTA) ----------------
-    if (tid == 0) {
-      int a = K;
-      for (int i = 0; i < K; ++i) {
-        const float Zt = sm.Z[i], Zd = sm.Z[n + i];
-        const float p = exp2f((sm.gtl[i] - sm.M[i]) * coef) / Zt;
-        const float q = exp2f((sm.gdl[i] - sm.M[n + i]) * coef) / Zd;
-        const float thr = q > 0.f ? fminf(1.f, p / q) : 1.f;
-        if (!(sm.uacc[i] < thr)) {
-          a = i;
-          break;
+    // ---------------- accept scan (identical in every CTA): one lane per draft, first rejection by ballot ----------------
+    if (warp == 0) {
+      unsigned rej[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        bool r = false;
+        if (i < K) {
+          const float p = exp2f((sm.gtl[i] - sm.M[i]) * coef) / sm.Z[i];
+          const float q = exp2f((sm.gdl[i] - sm.M[n + i]) * coef) / sm.Z[n + i];
+          const float thr = q > 0.f ? fminf(1.f, p / q) : 1.f;
+          r = !(sm.uacc[i] < thr);
         }
+        rej[h] = __ballot_sync(0xffffffffu, r);
       }
-      sm.a = a;
-      for (int r = 0; r < rows; ++r)
-        if (!(sm.Z[r] > 0.f)) sm.bad = 1;
-      if (sm.bad && rank == 0) record(args.status, SV_ERR_NONFINITE);
-      // a residual draw weighs q_v as e_d (Z_t / Z_d) against e_t, the ratio carried as hi + lo
-      const double rho = a < K && sm.Z[n + a] > 0.f ? (double)sm.Z[a] / (double)sm.Z[n + a] : 0.0;
-      sm.rho_hi = (float)rho;
-      sm.rho_lo = (float)(rho - (double)sm.rho_hi);
+      bool nz = false;
+      for (int r = lane; r < rows; r += 32) nz |= !(sm.Z[r] > 0.f);
+      const bool bad = __any_sync(0xffffffffu, nz);
+      if (lane == 0) {
+        const int a = rej[0] ? __ffs(rej[0]) - 1 : rej[1] ? 31 + __ffs(rej[1]) : K;
+        sm.a = a;
+        if (bad && rank == 0) record(args.status, SV_ERR_NONFINITE);
+        // a residual draw weighs q_v as e_d (Z_t / Z_d) against e_t, the ratio carried as hi + lo
+        const double rho = a < K && sm.Z[n + a] > 0.f ? (double)sm.Z[a] / (double)sm.Z[n + a] : 0.0;
+        sm.rho_hi = (float)rho;
+        sm.rho_lo = (float)(rho - (double)sm.rho_hi);
+      }
     }
     __syncthreads();
     const int a = sm.a;

@@ -181,7 +181,7 @@ struct SamplerArgs {
 };
 enum SamplerMode { kStochastic = 0, kGreedy = 1, kTree = 2 };
 // Bytes of the partials workspace: rows (total_q target rows, plus total_q - batch
-// draft rows for kStochastic) x 16 KB items x 8 warps x (max, sum); 0 if the sizes
+// draft rows for kStochastic) x 32 KB items x 8 warps x (max, sum); 0 if the sizes
 // are invalid or too large.
 size_t sampler_workspace_bytes(int vocab, int dtype, int total_q, int batch, int mode);
 cudaError_t launch_sampler(const SamplerArgs &a, int dtype, int mode, void *workspace, cudaStream_t st);

@@ -61,10 +61,10 @@ def test_host_validation_without_gpu(lib):
                                         None, None, None, None, 0, None, None) == 1
     assert lib.sv_spec_rejection_sample(None, None, 0, 100, 1, None, 2, 2, None, None, None, float("nan"),
                                         None, None, None, None, 0, None, None) == 1
-    # the sampler's workspace: 16 KB items x 8 warps x (max, sum); target (+ draft) rows
-    assert lib.sv_spec_rejection_sample_workspace_bytes(0, 128256, 32, 256, 1.0) == (2 * 256 - 32) * 16 * 64
-    assert lib.sv_spec_rejection_sample_workspace_bytes(0, 128256, 32, 256, 0.0) == 256 * 16 * 64
-    assert lib.sv_spec_rejection_sample_workspace_bytes(1, 8192, 1, 1, 0.0) == 2 * 64
+    # the sampler's workspace: 32 KB items x 8 warps x (max, sum); target (+ draft) rows
+    assert lib.sv_spec_rejection_sample_workspace_bytes(0, 128256, 32, 256, 1.0) == (2 * 256 - 32) * 8 * 64
+    assert lib.sv_spec_rejection_sample_workspace_bytes(0, 128256, 32, 256, 0.0) == 256 * 8 * 64
+    assert lib.sv_spec_rejection_sample_workspace_bytes(1, 8192, 1, 1, 0.0) == 64
     assert lib.sv_spec_rejection_sample_workspace_bytes(7, 100, 1, 2, 1.0) == 0
     assert lib.sv_spec_rejection_sample_workspace_bytes(0, 100, 3, 2, 1.0) == 0
     # a workspace that is missing: refused on the host before anything is read
