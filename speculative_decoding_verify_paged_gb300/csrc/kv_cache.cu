@@ -59,32 +59,45 @@ __device__ __forceinline__ int blocks_for(int tokens, int bs) { return (tokens +
 // -------------------------------------------------------------------------
 // append, step 1: block allocation (one CTA)
 // -------------------------------------------------------------------------
+// The kernel is a chain of dependent memory round trips, so it issues every
+// load that does not depend on an earlier one at once: the status word, the
+// free-list top and the first batch of sequence lengths. The ids about to be
+// popped are read once into shared memory, checked, then popped from there.
+constexpr int kIdCache = 4096;
+
 __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int32_t *cu_q, int32_t *status) {
   grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   grid_dependents_launch();
-  __shared__ int s_flag, s_top;
-  if (threadIdx.x == 0) {
-    s_flag = status_set(status) ? 1 : 0;
-    s_top = *kv.free_top;
-  }
-  __syncthreads();
-  if (s_flag) return;
-  const int top = s_top;
+  __shared__ int s_ids[kIdCache];
   const int B = kv.batch, bs = kv.block_size;
+  const bool failed = status_set(status);
+  const int top = *kv.free_top;
+  int c0 = 0, n0 = 0;  // the thread's sequence of the first batch
+  if ((int)threadIdx.x < B) {
+    c0 = kv.seq_lens[threadIdx.x];
+    n0 = cu_q[threadIdx.x + 1] - cu_q[threadIdx.x];
+  }
+  if (failed) return;  // every thread read the same word: the whole CTA leaves
 
-  // pass 1: validate lengths, count blocks
+  // pass 1: validate lengths, count blocks (the first batch's offsets are kept)
   int bad_len = 0;
-  int total = 0;
+  int total = 0, off0 = 0, need0 = 0, tot0 = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     int need = 0;
     if (b < B) {
-      const int c = kv.seq_lens[b], n = cu_q[b + 1] - cu_q[b];
+      const int c = base == 0 ? c0 : kv.seq_lens[b];
+      const int n = base == 0 ? n0 : cu_q[b + 1] - cu_q[b];
       if (c < 0 || n < 0 || blocks_for(c + n, bs) > kv.max_blocks) bad_len = 1;
       else need = blocks_for(c + n, bs) - blocks_for(c, bs);
     }
     int chunk_total;
-    block_excl_scan(need, &chunk_total);
+    const int off = block_excl_scan(need, &chunk_total);
+    if (base == 0) {
+      off0 = off;
+      need0 = need;
+      tot0 = chunk_total;
+    }
     total += chunk_total;
   }
   if (__syncthreads_or(bad_len)) {
@@ -99,6 +112,7 @@ __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int
   int bad_id = 0;
   for (int k = threadIdx.x; k < total; k += blockDim.x) {
     const int id = kv.free_list[top - 1 - k];
+    if (k < kIdCache) s_ids[k] = id;
     if (id < 0 || id >= kv.num_blocks) bad_id = 1;
   }
   if (__syncthreads_or(bad_id)) {
@@ -106,8 +120,12 @@ __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int
     return;
   }
   // pass 3: pop into the block tables
-  int carry = 0;
-  for (int base = 0; base < B; base += blockDim.x) {
+  auto popped = [&](int k) { return k < kIdCache ? s_ids[k] : kv.free_list[top - 1 - k]; };
+  if ((int)threadIdx.x < B)
+    for (int j = 0; j < need0; ++j)
+      kv.block_table[(size_t)threadIdx.x * kv.max_blocks + blocks_for(c0, bs) + j] = popped(off0 + j);
+  int carry = tot0;  // batches past the first (more sequences than threads)
+  for (int base = blockDim.x; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     int need = 0, first = 0;
     if (b < B) {
@@ -117,8 +135,7 @@ __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int
     }
     int chunk_total;
     const int off = carry + block_excl_scan(need, &chunk_total);
-    for (int j = 0; j < need; ++j)
-      kv.block_table[(size_t)b * kv.max_blocks + first + j] = kv.free_list[top - 1 - (off + j)];
+    for (int j = 0; j < need; ++j) kv.block_table[(size_t)b * kv.max_blocks + first + j] = popped(off + j);
     carry += chunk_total;
   }
   __syncthreads();
@@ -129,20 +146,44 @@ __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int
 // -------------------------------------------------------------------------
 // append, step 2: scatter the new rows (one CTA per query row)
 // -------------------------------------------------------------------------
-__global__ void kv_scatter_kernel(KV kv, const uint8_t *new_k, const uint8_t *new_v, const int32_t *cu_q,
-                                  int32_t *status) {
+// The row's source vectors do not depend on where they go: they are loaded
+// first, while cu_q is staged in shared memory for the search of the row's
+// sequence; then the sequence length and the block id, then the stores.
+constexpr int kScatterThreads = 128;
+constexpr int kCuCache = 2048;
+
+__global__ void __launch_bounds__(kScatterThreads) kv_scatter_kernel(KV kv, const uint8_t *new_k,
+                                                                     const uint8_t *new_v, const int32_t *cu_q,
+                                                                     int32_t *status) {
   grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   grid_dependents_launch();
-  if (status_set(status)) return;
+  __shared__ int s_cu[kCuCache];
   const int row = blockIdx.x;
-  int lo = 0, hi = kv.batch;  // the last b with cu_q[b] <= row owns the row
+  const int B = kv.batch;
+  const bool failed = status_set(status);
+  const int row_bytes = kv.head_dim * kv.elem_bytes;  // a multiple of 16
+  const int vec_per_row = row_bytes / 16;
+  const int total = kv.num_kv_heads * vec_per_row;
+  const size_t src_row = (size_t)row * kv.num_kv_heads * row_bytes;
+  uint4 kk0 = make_uint4(0, 0, 0, 0), vv0 = kk0;  // the thread's first vector
+  if ((int)threadIdx.x < total) {
+    kk0 = *reinterpret_cast<const uint4 *>(new_k + src_row + (size_t)threadIdx.x * 16);
+    vv0 = *reinterpret_cast<const uint4 *>(new_v + src_row + (size_t)threadIdx.x * 16);
+  }
+  const bool staged = B + 1 <= kCuCache;
+  if (staged)
+    for (int k = threadIdx.x; k <= B; k += blockDim.x) s_cu[k] = cu_q[k];
+  __syncthreads();
+  if (failed) return;
+  auto cu = [&](int k) { return staged ? s_cu[k] : cu_q[k]; };
+  int lo = 0, hi = B;  // the last b with cu_q[b] <= row owns the row
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (cu_q[mid] <= row) lo = mid;
+    if (cu(mid) <= row) lo = mid;
     else hi = mid;
   }
-  const int b = lo, row0 = cu_q[b], i = row - row0;
-  if (i >= cu_q[b + 1] - row0) return;  // rows past cu_q[batch]: nothing to write
+  const int b = lo, row0 = cu(b), i = row - row0;
+  if (i >= cu(b + 1) - row0) return;  // rows past cu_q[batch]: nothing to write
   const int pos = kv.seq_lens[b] + i;
   const int blk = kv.block_table[(size_t)b * kv.max_blocks + pos / kv.block_size];
   if (blk < 0 || blk >= kv.num_blocks) {
@@ -150,16 +191,14 @@ __global__ void kv_scatter_kernel(KV kv, const uint8_t *new_k, const uint8_t *ne
     return;
   }
   const int slot = pos % kv.block_size;
-  const int row_bytes = kv.head_dim * kv.elem_bytes;  // a multiple of 16
-  const int vec_per_row = row_bytes / 16;
-  const int total = kv.num_kv_heads * vec_per_row;
-  const size_t src_row = (size_t)(row0 + i) * kv.num_kv_heads * row_bytes;
   for (int x = threadIdx.x; x < total; x += blockDim.x) {
     const int h = x / vec_per_row, v = x % vec_per_row;
-    const size_t src = src_row + (size_t)h * row_bytes + (size_t)v * 16;
+    uint4 kk = kk0, vv = vv0;
+    if (x >= (int)blockDim.x) {
+      kk = *reinterpret_cast<const uint4 *>(new_k + src_row + (size_t)x * 16);
+      vv = *reinterpret_cast<const uint4 *>(new_v + src_row + (size_t)x * 16);
+    }
     const size_t dst = (((size_t)blk * kv.num_kv_heads + h) * kv.block_size + slot) * row_bytes + (size_t)v * 16;
-    const uint4 kk = *reinterpret_cast<const uint4 *>(new_k + src);
-    const uint4 vv = *reinterpret_cast<const uint4 *>(new_v + src);
     *reinterpret_cast<uint4 *>((uint8_t *)kv.k_pool + dst) = kk;
     *reinterpret_cast<uint4 *>((uint8_t *)kv.v_pool + dst) = vv;
   }
@@ -227,22 +266,26 @@ __global__ void __launch_bounds__(kBookThreads) kv_truncate_kernel(KV kv, const 
                                                                    const int32_t *accept, int32_t *status) {
   grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   grid_dependents_launch();
-  __shared__ int s_flag, s_top;
-  if (threadIdx.x == 0) {
-    s_flag = status_set(status) ? 1 : 0;
-    s_top = *kv.free_top;
-  }
-  __syncthreads();
-  if (s_flag) return;
-  const int top = s_top;
   const int B = kv.batch, bs = kv.block_size;
+  // every load that depends on no other at once (see kv_alloc_kernel)
+  const bool failed = status_set(status);
+  const int top = *kv.free_top;
+  int c0 = 0, n0 = 0, a0 = 0;
+  if ((int)threadIdx.x < B) {
+    c0 = kv.seq_lens[threadIdx.x];
+    n0 = cu_q[threadIdx.x + 1] - cu_q[threadIdx.x];
+    a0 = accept[threadIdx.x];
+  }
+  if (failed) return;  // every thread read the same word: the whole CTA leaves
   int bad_len = 0, bad_id = 0;
   int total = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     int freed = 0;
     if (b < B) {
-      const int c = kv.seq_lens[b], n = cu_q[b + 1] - cu_q[b], a = accept[b];
+      const int c = base == 0 ? c0 : kv.seq_lens[b];
+      const int n = base == 0 ? n0 : cu_q[b + 1] - cu_q[b];
+      const int a = base == 0 ? a0 : accept[b];
       if (c < 0 || n < 1 || a < 0 || a > n - 1 || blocks_for(c + n, bs) > kv.max_blocks) {
         bad_len = 1;
       } else {
@@ -275,9 +318,9 @@ __global__ void __launch_bounds__(kBookThreads) kv_truncate_kernel(KV kv, const 
     const int b = base + threadIdx.x;
     int freed = 0, old_blocks = 0, c = 0, a = 0;
     if (b < B) {
-      c = kv.seq_lens[b];
-      const int n = cu_q[b + 1] - cu_q[b];
-      a = accept[b];
+      c = base == 0 ? c0 : kv.seq_lens[b];
+      const int n = base == 0 ? n0 : cu_q[b + 1] - cu_q[b];
+      a = base == 0 ? a0 : accept[b];
       old_blocks = blocks_for(c + n, bs);
       freed = old_blocks - blocks_for(c + a + 1, bs);
     }
@@ -301,7 +344,7 @@ cudaError_t launch_kv_append(const KV &kv, const void *new_k, const void *new_v,
                              int total_q, int32_t *status, cudaStream_t st) {
   cudaError_t e = launch_pdl(kv_alloc_kernel, dim3(1), dim3(kBookThreads), 0, st, kv, cu_q, status);
   if (e != cudaSuccess || total_q == 0) return e;
-  return launch_pdl(kv_scatter_kernel, dim3((unsigned)total_q), dim3(128), 0, st, kv, (const uint8_t *)new_k,
+  return launch_pdl(kv_scatter_kernel, dim3((unsigned)total_q), dim3(kScatterThreads), 0, st, kv, (const uint8_t *)new_k,
                     (const uint8_t *)new_v, cu_q, status);
 }
 
