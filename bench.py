@@ -339,6 +339,7 @@ def run_native(args):
         "attn_paths_ms": paths,
         "gpu_launches": S.launches_per_step(d, msl, kv) * args.steps,
         "clocks": clk,
+        "adaptive_k": adaptive_k_timing(),
     }
     if e2e is not None:
         line["e2e"] = e2e
@@ -353,6 +354,24 @@ def run_native(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
+
+
+def adaptive_k_timing(batch=256, calls=2000):
+    """Host cost of the adaptive-K controller (sv_adaptive_k_update through the
+    C ABI) for a 256-sequence batch with a full 50-rate window."""
+    from speculative_decoding_verify_paged_gb300 import AdaptiveK
+    rng = np.random.default_rng(0)
+    ctl = AdaptiveK(batch)
+    drafted = np.full(batch, 8, np.int32)
+    acc = [rng.integers(0, 9, size=batch).astype(np.int32) for _ in range(16)]
+    for i in range(60):
+        ctl.update(acc[i % 16], drafted)
+    t0 = time.perf_counter()
+    for i in range(calls):
+        ctl.update(acc[i % 16], drafted)
+    us = (time.perf_counter() - t0) / calls * 1e6
+    return {"call": "sv_adaptive_k_update", "batch": batch, "window": 50, "us_per_update": us,
+            "note": "host-side, once per step between sampler and the next append"}
 
 
 def attn_path_times(kv, d, buf, msl, stream, reps=10):

@@ -13,6 +13,9 @@
  *                             resample (or greedy / tree-greedy acceptance)
  *   sv_kv_rollback            truncate every sequence at its accepted length
  *
+ * Between steps, on the host, sv_adaptive_k_update turns the accept counts
+ * into each sequence's draft length for the next step.
+ *
  * Conventions shared by every call:
  *  - Pointers are DEVICE pointers owned by the caller, unless stated. The
  *    library never allocates, frees or keeps a pointer after a call returns.
@@ -286,6 +289,50 @@ sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype,
  */
 sv_status sv_kv_rollback(const sv_paged_kv *kv, const int32_t *cu_q, const int32_t *accept_count,
                          const int32_t *path_nodes, int32_t max_q_per_seq, int32_t *status_dev, void *stream);
+
+/*
+ * Adaptive draft length: the host-side controller that picks each sequence's
+ * K for the next step from its observed acceptance ("Speculative decoding
+ * principles and a vLLM production setup", sec. 4.3, the sliding-window
+ * controller; the same rule with a 10-step window and 80% / 50% thresholds is
+ * the tuning advice of "LLM inference optimisation: speculative decoding and
+ * dynamic batching", engineering parameters).
+ *
+ * Per sequence b the state holds K_b and the last `window` acceptance rates
+ * alpha = accepted / max(drafted, 1). An update appends the step's alpha
+ * (dropping the oldest once the window is full); when the window then holds
+ * at least `min_samples` rates, their mean (summed oldest first, in double)
+ * moves K_b up by one if it is above up_threshold, down by one if it is below
+ * down_threshold, within [k_min, k_max]. K_b starts at k_init.
+ *
+ * Every pointer here is a HOST pointer; nothing touches the GPU. The state is
+ * caller-owned memory of sv_adaptive_k_state_bytes bytes, 8-byte aligned,
+ * opaque, written only by these calls; one state must not be used by two host
+ * threads at once.
+ *   params        k_min >= 0, k_min <= k_init <= k_max <= 63 (K + 1 rows must
+ *                 fit max_q_per_seq <= 64), window >= 1, min_samples >= 1
+ *                 (a min_samples above window never moves K, as the sample
+ *                 controller's rule gives), finite thresholds
+ *   accepted      int32 [batch]: a_b of the step, 0 <= a_b <= drafted_b
+ *   drafted       int32 [batch]: K_b of the step, >= 0
+ *   k_next        int32 [batch] out (may be NULL): K_b for the next step
+ * All or nothing: invalid arguments return SV_ERR_INVALID_ARG and leave the
+ * state unchanged.
+ */
+typedef struct sv_adaptive_k_params {
+  int32_t k_min, k_max, k_init;
+  int32_t window, min_samples;
+  double up_threshold, down_threshold;
+} sv_adaptive_k_params;
+
+/* Bytes of state for `batch` sequences and this window; 0 for invalid sizes. */
+size_t sv_adaptive_k_state_bytes(int32_t batch, int32_t window);
+sv_status sv_adaptive_k_init(void *state, size_t state_bytes, int32_t batch, const sv_adaptive_k_params *params);
+sv_status sv_adaptive_k_update(void *state, const int32_t *accepted, const int32_t *drafted, int32_t *k_next);
+/* Sequence slot `seq` starts over (a new request took it): K = k_init, empty window. */
+sv_status sv_adaptive_k_reset(void *state, int32_t seq);
+/* The current K of every sequence into k (int32 [batch]). */
+sv_status sv_adaptive_k_current(const void *state, int32_t *k);
 
 /*
  * Process-wide options (no counterpart on the pages; they select between

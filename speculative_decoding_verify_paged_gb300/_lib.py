@@ -20,6 +20,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
 SV_OK = 0
+SV_ERR_INVALID_ARG = 1
 SV_ERR_WORKSPACE = 10
 SV_DTYPE_BF16, SV_DTYPE_F32 = 0, 1
 SV_MASK_CAUSAL, SV_MASK_TREE = 0, 1
@@ -31,7 +32,8 @@ STATUS_NAMES = {
 
 EXPORTS = ("sv_kv_append", "sv_spec_verify_attn_workspace_bytes", "sv_spec_verify_attn",
            "sv_spec_verify_attn_no_alloc", "sv_spec_rejection_sample_workspace_bytes", "sv_spec_rejection_sample",
-           "sv_tree_greedy_accept", "sv_kv_rollback",
+           "sv_tree_greedy_accept", "sv_kv_rollback", "sv_adaptive_k_state_bytes", "sv_adaptive_k_init",
+           "sv_adaptive_k_update", "sv_adaptive_k_reset", "sv_adaptive_k_current",
            "sv_status_string", "sv_version", "sv_set_option")
 SV_OPT_ATTN_PATH = 1
 ATTN_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "warp_mma": 3}
@@ -41,6 +43,14 @@ class SVError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
         super().__init__(f"{what}: {status_string(code)}")
+
+
+class sv_adaptive_k_params(ctypes.Structure):
+    _fields_ = [
+        ("k_min", ctypes.c_int32), ("k_max", ctypes.c_int32), ("k_init", ctypes.c_int32),
+        ("window", ctypes.c_int32), ("min_samples", ctypes.c_int32),
+        ("up_threshold", ctypes.c_double), ("down_threshold", ctypes.c_double),
+    ]
 
 
 class sv_paged_kv(ctypes.Structure):
@@ -82,6 +92,11 @@ def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CD
             "sv_spec_rejection_sample": (I, [P, P, I, I, I, P, I, I, P, P, P, F, P, P, P, P, S, P, P]),
             "sv_tree_greedy_accept": (I, [P, I, I, I, P, I, I, P, P, P, P, P, P, P, S, P, P]),
             "sv_kv_rollback": (I, [KVP, P, P, P, I, P, P]),
+            "sv_adaptive_k_state_bytes": (S, [I, I]),
+            "sv_adaptive_k_init": (I, [P, S, I, ctypes.POINTER(sv_adaptive_k_params)]),
+            "sv_adaptive_k_update": (I, [P, P, P, P]),
+            "sv_adaptive_k_reset": (I, [P, I]),
+            "sv_adaptive_k_current": (I, [P, P]),
             "sv_status_string": (ctypes.c_char_p, [I]),
             "sv_version": (I, []),
             "sv_set_option": (I, [I, I]),
@@ -253,3 +268,48 @@ def kv_rollback(kv: PagedKV, cu_q: torch.Tensor, accept_count: torch.Tensor, sta
     s = kv.struct()
     _check(load().sv_kv_rollback(ctypes.byref(s), _ptr(cu_q), _ptr(accept_count), _ptr(path_nodes), int(max_q),
                                  _ptr(status), _stream(stream)), "sv_kv_rollback")
+
+
+class AdaptiveK:
+    """Per-sequence draft length from observed acceptance (host side; the
+    sv_adaptive_k_* calls). The state lives in host memory owned here; the
+    arrays passed in and out are host int32 arrays (numpy or CPU tensors)."""
+
+    def __init__(self, batch: int, *, k_min: int = 2, k_max: int = 8, k_init: Optional[int] = None,
+                 window: int = 50, min_samples: int = 10, up_threshold: float = 0.6 + 0.1,
+                 down_threshold: float = 0.6 - 0.1):
+        import numpy as np
+        self._np = np
+        self.batch = int(batch)
+        self.params = sv_adaptive_k_params(int(k_min), int(k_max), int(k_min if k_init is None else k_init),
+                                           int(window), int(min_samples), float(up_threshold),
+                                           float(down_threshold))
+        lib = load()
+        n = int(lib.sv_adaptive_k_state_bytes(self.batch, self.params.window))
+        if n == 0:
+            raise SVError(SV_ERR_INVALID_ARG, "sv_adaptive_k_state_bytes")
+        self._state = (ctypes.c_double * ((n + 7) // 8))()  # 8-byte aligned host memory
+        _check(lib.sv_adaptive_k_init(self._state, n, self.batch, ctypes.byref(self.params)), "sv_adaptive_k_init")
+
+    def _host_i32(self, x):
+        a = self._np.ascontiguousarray(x.cpu().numpy() if isinstance(x, torch.Tensor) else x, dtype=self._np.int32)
+        if a.shape != (self.batch,):
+            raise ValueError(f"expected {self.batch} entries")
+        return a
+
+    def update(self, accepted, drafted):
+        """Feed one step's accept counts and draft lengths; returns next K (int32 numpy array)."""
+        a, d = self._host_i32(accepted), self._host_i32(drafted)
+        out = self._np.empty(self.batch, dtype=self._np.int32)
+        _check(load().sv_adaptive_k_update(self._state, a.ctypes.data, d.ctypes.data, out.ctypes.data),
+               "sv_adaptive_k_update")
+        return out
+
+    def reset(self, seq: int) -> None:
+        _check(load().sv_adaptive_k_reset(self._state, int(seq)), "sv_adaptive_k_reset")
+
+    @property
+    def k(self):
+        out = self._np.empty(self.batch, dtype=self._np.int32)
+        _check(load().sv_adaptive_k_current(self._state, out.ctypes.data), "sv_adaptive_k_current")
+        return out

@@ -1,7 +1,7 @@
 """Build libspecverify.so in-tree with nvcc for sm_103a (GB300).
 
-Each translation unit under csrc/ compiles in its own nvcc process, in
-parallel; the objects link into one shared library with the CUDA runtime
+Each translation unit under csrc/ (CUDA .cu, host-only .cpp) compiles in its
+own nvcc process, in parallel; the objects link into one shared library with the CUDA runtime
 linked statically. Rebuilds only when a source or header is newer than the
 library.
 """
@@ -33,7 +33,7 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
@@ -54,7 +54,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

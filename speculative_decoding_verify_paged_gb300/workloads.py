@@ -366,9 +366,12 @@ def contbatch(seed: int = 3, *, batch: int = 256, vocab: int = 128256, iteration
 
 
 def contbatch_step(seed: int, iteration: int, *, batch: int, vocab: int, sigma_b: np.ndarray,
-                   temperature: float = 1.0) -> StepInputs:
+                   temperature: float = 1.0, K: np.ndarray | None = None) -> StepInputs:
+    """One iteration's inputs; K_b ~ U{2..8} unless the draft lengths are given
+    (e.g. by the adaptive-K controller)."""
     rng = _rng(seed, 30, iteration)
-    K = rng.integers(2, 9, size=batch).astype(np.int32)
+    K_drawn = rng.integers(2, 9, size=batch).astype(np.int32)
+    K = K_drawn if K is None else np.asarray(K, dtype=np.int32)
     return make_chain_step(seed, K + 1, num_q_heads=32, num_kv_heads=8, head_dim=128, qkv_dtype="bf16",
                            vocab=vocab, logits_dtype="bf16", target_sigma=3.0, draft_coef=0.8,
                            draft_sigma=sigma_b, temperature=temperature, stream=iteration + 1)

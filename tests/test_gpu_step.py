@@ -24,7 +24,7 @@ from _helpers import (MAX_TIE_FRACTION, assert_attn_close, assert_kv_equal, attn
 pytestmark = pytest.mark.gpu
 
 
-def _loop(case, iterations, steps_of, attn_check_iters, attn_seqs, with_pools):
+def _loop(case, iterations, steps_of, attn_check_iters, attn_seqs, with_pools, observe=None):
     st = case.state
     kv = S.device_kv(st)
     okv = oracle.OracleKV(st, with_pools=with_pools)
@@ -47,6 +47,8 @@ def _loop(case, iterations, steps_of, attn_check_iters, attn_seqs, with_pools):
         got = gpu_sample_result(buf)
         diverged += compare_samples(step, got, ref, max_fraction=None)
         positions += int(step.n_q.sum())
+        if observe is not None:
+            observe(step, got[0], ref.accept_cnt)
         if not np.array_equal(got[0], ref.accept_cnt):
             buf.accept.copy_(torch.from_numpy(ref.accept_cnt))
         S.rollback(kv, d, buf)
@@ -85,3 +87,38 @@ def test_llama8b_three_steps_with_pools():
             blk = okv.bt[b][pos // okv.bs]
             np.testing.assert_array_equal(kp[blk, :, pos % okv.bs], okv.k_pool[blk, :, pos % okv.bs])
             np.testing.assert_array_equal(vp[blk, :, pos % okv.bs], okv.v_pool[blk, :, pos % okv.bs])
+
+
+def test_contbatch_adaptive_k():
+    """The draft lengths come from the library's adaptive-K controller (sliding
+    window of acceptance rates, page defaults but starting at K = 4), fed with
+    the GPU's accept counts; the oracle's controller, fed with the oracle's, must
+    choose the same K for every sequence at every iteration."""
+    from oracle import adaptive_k as AK
+    from speculative_decoding_verify_paged_gb300 import AdaptiveK
+    iters = 14
+    case = W.contbatch(batch=64, vocab=32000, iterations=iters)
+    sig = case.meta["sigma_b"]
+    B = case.state.batch
+    p = AK.Params(**{**AK.vllm_params().__dict__, "k_init": 4})
+    nat = AdaptiveK(B, k_min=p.k_min, k_max=p.k_max, k_init=p.k_init, window=p.window, min_samples=p.min_samples,
+                    up_threshold=p.up_threshold, down_threshold=p.down_threshold)
+    ora = AK.BatchController(B, p)
+    ks = []
+
+    def steps(it):
+        k = nat.k
+        np.testing.assert_array_equal(k, np.array(ora.k, dtype=np.int32))
+        ks.append(k)
+        return W.contbatch_step(case.seed, it, batch=B, vocab=32000, sigma_b=sig, K=k)
+
+    def observe(step, gpu_acc, ref_acc):
+        drafted = step.n_q - 1
+        # a near-tie divergence: the GPU side takes the oracle's counts, as the rollback does
+        nat.update(gpu_acc if np.array_equal(gpu_acc, ref_acc) else ref_acc, drafted)
+        ora.update(ref_acc, drafted)
+
+    _loop(case, iters, steps, {iters - 1}, [0, 7], with_pools=False, observe=observe)
+    ks = np.stack(ks)
+    assert (ks[:10] == 4).all()  # nothing moves before ten rates are held
+    assert len(set(ks[-1].tolist())) > 1  # then low- and high-noise drafts part ways
