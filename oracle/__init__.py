@@ -97,6 +97,8 @@ def paged_attention(state, step, *, seqs=None, out: np.ndarray | None = None) ->
     block table. `state` must already hold the step's new rows (see
     OracleKV.append). Returns [T_q, Hq, D] float64 (rows of sequences not in
     `seqs` are zero / untouched)."""
+    if state.k_pool is None or state.v_pool is None:
+        raise ValueError("paged_attention needs a state with K/V pools (OracleKV(..., with_pools=True))")
     Tq = step.total_q
     hq = step.num_q_heads
     d = state.head_dim

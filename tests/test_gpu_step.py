@@ -118,7 +118,7 @@ def test_contbatch_adaptive_k():
         nat.update(gpu_acc if np.array_equal(gpu_acc, ref_acc) else ref_acc, drafted)
         ora.update(ref_acc, drafted)
 
-    _loop(case, iters, steps, {iters - 1}, [0, 7], with_pools=False, observe=observe)
+    _loop(case, iters, steps, {iters - 1}, [0, 7], with_pools=True, observe=observe)
     ks = np.stack(ks)
     assert (ks[:10] == 4).all()  # nothing moves before ten rates are held
     assert len(set(ks[-1].tolist())) > 1  # then low- and high-noise drafts part ways

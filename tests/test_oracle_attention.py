@@ -167,3 +167,12 @@ def test_bad_block_id_is_an_error():
     s2.block_table[1, 0] = s2.num_blocks + 3
     with pytest.raises(oracle.OracleError):
         oracle.paged_attention(s2, case.step)
+
+
+def test_paged_attention_refuses_a_state_without_pools():
+    import oracle as O
+    from speculative_decoding_verify_paged_gb300 import workloads as W
+    case = W.tiny()
+    okv = O.OracleKV(case.state, with_pools=False)
+    with pytest.raises(ValueError):
+        O.paged_attention(okv.as_state(), case.step)
