@@ -169,6 +169,7 @@ def tree_greedy(step, *, max_q: int | None = None) -> SampleResult:
 # ----------------------------------------------------------------------------
 OUT_OF_BLOCKS = "out_of_blocks"
 NO_TABLE_ROOM = "no_table_room"
+BAD_LENGTH = "bad_length"
 
 
 class OracleKV:
@@ -197,6 +198,63 @@ class OracleKV:
         self.k_pool = state.k_pool.copy() if with_pools else None
         self.v_pool = state.v_pool.copy() if with_pools else None
         self._state = state
+        self.ref = None  # per-block reference counts once sharing is on
+
+    # ---- copy-on-write sharing ("LLM serving: speculative decoding and
+    # PagedAttention memory management", PagedAttention section: parent and
+    # child sequences of beam search / parallel sampling share physical blocks
+    # copy-on-write). Reading taken: a block's count is the number of block-table
+    # entries that hold it; a sequence about to write into a block whose count is
+    # above one first takes a private copy of it (a fresh block, popped before its
+    # new blocks) holding the rows written so far; a block goes back on the free
+    # list when its count drops to zero.
+    def enable_sharing(self, ref=None) -> None:
+        if ref is None:
+            ref = [0] * self.num_blocks
+            for row, n in zip(self.bt, self.seq_lens):
+                for lb in range(self._blocks(n, self.bs)):
+                    ref[row[lb]] += 1
+        self.ref = [int(x) for x in ref]
+
+    def ref_count(self) -> np.ndarray:
+        return np.array(self.ref, np.int32)
+
+    def fork(self, parents, children):
+        """Each child sequence slot (empty) takes its parent's blocks and length;
+        every shared block's count goes up by one. All or nothing."""
+        assert self.ref is not None
+        B = len(self.seq_lens)
+        ps, cs = [int(x) for x in parents], [int(x) for x in children]
+        if (len(set(cs)) != len(cs) or set(cs) & set(ps)
+                or any(not (0 <= x < B) for x in ps + cs)
+                or any(self.seq_lens[c] != 0 or any(e != -1 for e in self.bt[c]) for c in cs)):
+            return BAD_LENGTH
+        for p_, c in zip(ps, cs):
+            nb = self._blocks(self.seq_lens[p_], self.bs)
+            for lb in range(nb):
+                self.bt[c][lb] = self.bt[p_][lb]
+                self.ref[self.bt[p_][lb]] += 1
+            self.seq_lens[c] = self.seq_lens[p_]
+        return None
+
+    def release(self, seqs):
+        """Drop finished sequences: in the order given, blocks from the highest
+        logical one down lose one reference (every block, without sharing) and go
+        back on the free list at zero; the slot becomes empty."""
+        B = len(self.seq_lens)
+        ss = [int(x) for x in seqs]
+        if len(set(ss)) != len(ss) or any(not (0 <= x < B) for x in ss):
+            return BAD_LENGTH
+        for b in ss:
+            for lb in range(self._blocks(self.seq_lens[b], self.bs) - 1, -1, -1):
+                blk = self.bt[b][lb]
+                if self.ref is not None:
+                    self.ref[blk] -= 1
+                if self.ref is None or self.ref[blk] == 0:
+                    self.free.append(blk)
+                self.bt[b][lb] = -1
+            self.seq_lens[b] = 0
+        return None
 
     @staticmethod
     def _blocks(tokens: int, bs: int) -> int:
@@ -209,14 +267,40 @@ class OracleKV:
         n = [int(step.cu_q[b + 1] - step.cu_q[b]) for b in range(B)]
         need = [self._blocks(self.seq_lens[b] + n[b], self.bs) - self._blocks(self.seq_lens[b], self.bs)
                 for b in range(B)]
+        # copy-on-write: the first new row lands in a partly filled block that is
+        # still shared when this sequence's turn comes (sequences in order; each
+        # copy drops the block's count by one, so the last writer of a block no
+        # other sequence holds writes in place)
+        cow = [False] * B
+        if self.ref is not None:
+            left = {}
+            for b in range(B):
+                if n[b] > 0 and self.seq_lens[b] % self.bs != 0:
+                    blk = self.bt[b][self.seq_lens[b] // self.bs]
+                    r = left.get(blk, self.ref[blk])
+                    if r > 1:
+                        cow[b] = True
+                        left[blk] = r - 1
         if any(self._blocks(self.seq_lens[b] + n[b], self.bs) > self.max_blocks for b in range(B)):
             return NO_TABLE_ROOM
-        if sum(need) > len(self.free):
+        if sum(need) + sum(cow) > len(self.free):
             return OUT_OF_BLOCKS
         for b in range(B):
             first = self._blocks(self.seq_lens[b], self.bs)
+            if cow[b]:
+                lb = self.seq_lens[b] // self.bs
+                old, new = self.bt[b][lb], self.free.pop()
+                if self.k_pool is not None:
+                    used = self.seq_lens[b] % self.bs
+                    self.k_pool[new, :, :used, :] = self.k_pool[old, :, :used, :]
+                    self.v_pool[new, :, :used, :] = self.v_pool[old, :, :used, :]
+                self.ref[old] -= 1
+                self.ref[new] = 1
+                self.bt[b][lb] = new
             for j in range(need[b]):
                 self.bt[b][first + j] = self.free.pop()
+                if self.ref is not None:
+                    self.ref[self.bt[b][first + j]] = 1
         if self.k_pool is not None:
             for b in range(B):
                 for j in range(n[b]):
@@ -249,7 +333,11 @@ class OracleKV:
             old_blocks = self._blocks(c + n, self.bs)
             keep = self._blocks(new_len, self.bs)
             for lb in range(old_blocks - 1, keep - 1, -1):
-                self.free.append(self.bt[b][lb])
+                blk = self.bt[b][lb]
+                if self.ref is not None:
+                    self.ref[blk] -= 1
+                if self.ref is None or self.ref[blk] == 0:
+                    self.free.append(blk)
                 self.bt[b][lb] = -1
             self.seq_lens[b] = new_len
 
