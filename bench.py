@@ -340,6 +340,7 @@ def run_native(args):
         "gpu_launches": S.launches_per_step(d, msl, kv) * args.steps,
         "clocks": clk,
         "adaptive_k": adaptive_k_timing(),
+        "cow": cow_timing(),
     }
     if e2e is not None:
         line["e2e"] = e2e
@@ -354,6 +355,64 @@ def run_native(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
+
+
+def cow_timing(reps=5):
+    """Copy-on-write sharing through the C ABI (parallel sampling): 8 sequences
+    with llama8b-shaped contexts (16-token blocks, 8 KV heads of 128 bf16) fork
+    into 3 children each; then one append of a verify step (K=5) for all 32,
+    where every shared partial last block is copied by all but its last writer;
+    then the children are released. Device time of each call, CUDA events, mean
+    over `reps` rounds."""
+    import torch
+    from speculative_decoding_verify_paged_gb300 import _lib as L
+    from speculative_decoding_verify_paged_gb300 import step as S
+    from speculative_decoding_verify_paged_gb300 import workloads as W
+    P, C = 8, 3
+    B = P * (C + 1)
+    rng = np.random.default_rng(7)
+    ctx = np.zeros(B, np.int32)
+    ctx[:P] = rng.integers(512, 4097, size=P)
+    st = W.make_kv_state(7, ctx, block_size=16, num_kv_heads=8, head_dim=128, dtype="bf16",
+                         growth_tokens=8 * reps + 16)
+    ref = np.zeros(st.num_blocks, np.int32)
+    for b in range(B):
+        ref[st.block_table[b, :(int(ctx[b]) + 15) // 16]] = 1
+    kv = S.device_kv(st, ref_count=ref)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    parents = torch.arange(P, dtype=torch.int32, device="cuda").repeat_interleave(C)
+    children = torch.arange(P, B, dtype=torch.int32, device="cuda")
+    step = W.make_chain_step(7, np.full(B, 6, np.int32), num_q_heads=32, num_kv_heads=8, head_dim=128,
+                             qkv_dtype="bf16", vocab=256, logits_dtype="bf16", target_sigma=3.0, draft_coef=0.8,
+                             draft_sigma=1.0, temperature=0.0)
+    d = S.DeviceStep.from_host(step)
+    accept = torch.zeros(B, dtype=torch.int32, device="cuda")
+    times = {"fork": [], "append_with_copies": [], "release": []}
+    copies = 0
+    for r in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        ev[0].record()
+        L.kv_fork(kv, parents, children, status)
+        ev[1].record()
+        lens = kv.seq_lens.cpu().numpy()
+        copies += int(sum(C for b in range(P) if lens[b] % 16))  # the last of the C + 1 writers writes in place
+        ev[2].record()
+        L.kv_append(kv, d.new_k, d.new_v, d.cu_q, status)
+        ev[3].record()
+        L.kv_rollback(kv, d.cu_q, accept, status, max_q=6)
+        ev[4].record()
+        L.kv_release(kv, children, status)
+        ev[5].record()
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            return {"error": L.status_string(int(status.item()))}
+        times["fork"].append(ev[0].elapsed_time(ev[1]) * 1e3)
+        times["append_with_copies"].append(ev[2].elapsed_time(ev[3]) * 1e3)
+        times["release"].append(ev[4].elapsed_time(ev[5]) * 1e3)
+    out = {k + "_us": float(np.mean(v)) for k, v in times.items()}
+    out.update({"sequences": B, "forked_pairs": P * C, "block_copies_per_append": copies / reps,
+                "note": "sv_kv_fork / sv_kv_append / sv_kv_release with ref_count, device time"})
+    return out
 
 
 def adaptive_k_timing(batch=256, calls=2000):

@@ -14,7 +14,9 @@
  *   sv_kv_rollback            truncate every sequence at its accepted length
  *
  * Between steps, on the host, sv_adaptive_k_update turns the accept counts
- * into each sequence's draft length for the next step.
+ * into each sequence's draft length for the next step. sv_kv_fork lets new
+ * sequences share a parent's blocks (copy-on-write, with kv->ref_count) and
+ * sv_kv_release gives a finished sequence's blocks back.
  *
  * Conventions shared by every call:
  *  - Pointers are DEVICE pointers owned by the caller, unless stated. The
@@ -91,6 +93,16 @@ typedef enum sv_mask_kind { SV_MASK_CAUSAL = 0, SV_MASK_TREE = 1 } sv_mask_kind;
  *   free_list        int32 [num_blocks]: a stack of free physical ids; entries
  *                    [0, *free_top) are valid, entry *free_top-1 is the top
  *   free_top         int32 [1]
+ *   ref_count        int32 [num_blocks], or NULL: no block is shared. With it,
+ *                    sequences may share physical blocks copy-on-write ("LLM
+ *                    serving: speculative decoding and PagedAttention memory
+ *                    management", PagedAttention section: parent and child
+ *                    sequences of beam search or parallel sampling share
+ *                    blocks): ref_count[x] is the number of block-table
+ *                    entries, over all sequences, that hold block x (0 for a
+ *                    free block). The caller sets it up to match the tables
+ *                    (1 per held block when nothing is shared yet); the calls
+ *                    below keep it so.
  * block_size: a power of two in [1, 256]; head_dim: a multiple of 8 in
  * [8, 256]; dtype: SV_DTYPE_BF16 or SV_DTYPE_F32.
  */
@@ -108,6 +120,7 @@ typedef struct sv_paged_kv {
   int32_t head_dim;
   int32_t batch;
   int32_t dtype;
+  int32_t *ref_count;
 } sv_paged_kv;
 
 /*
@@ -120,6 +133,14 @@ typedef struct sv_paged_kv {
  * logical position c_b + j: physical block block_table[b][(c_b+j) / bs], slot
  * (c_b+j) % bs, for every KV head. seq_lens is not changed (the new rows are
  * pending until sv_kv_rollback).
+ * With ref_count: a sequence whose first new row lands in a partly filled
+ * block that is still shared when its turn comes (sequences in order; a block
+ * held by r sequences) first takes a private copy: one more block, popped just
+ * before its new blocks, that receives the block's c_b % bs rows (every KV
+ * head) and replaces it in the table; the shared block's count drops by one.
+ * So of w writers into a block held by r, the first min(w, r - 1) copy and a
+ * last writer that holds the only remaining reference writes in place. New
+ * blocks get count 1.
  *   new_k, new_v  [total_q, num_kv_heads, head_dim] of kv->dtype
  *   cu_q          int32 [batch + 1], cu_q[0] = 0, cu_q[batch] = total_q
  *   status_dev    int32 [1], required
@@ -284,11 +305,49 @@ sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype,
  *   accept_count  int32 [batch]: 0 <= a_b <= n_b - 1
  *   path_nodes    int32 [batch, max_q_per_seq] or NULL (chain drafts)
  *   status_dev    int32 [1], required
+ * With ref_count, the count of each block given back drops by one and the
+ * block is pushed only when it reaches zero (the blocks past the new end were
+ * taken by this step's append, so they are the sequence's own).
  * All or nothing: an accept count or path entry out of range sets
  * SV_ERR_BAD_LENGTH and changes nothing.
  */
 sv_status sv_kv_rollback(const sv_paged_kv *kv, const int32_t *cu_q, const int32_t *accept_count,
                          const int32_t *path_nodes, int32_t max_q_per_seq, int32_t *status_dev, void *stream);
+
+/*
+ * sv_kv_fork -- children share their parents' blocks (copy-on-write; requires
+ * kv->ref_count).
+ *
+ * For pair k, sequence children[k] (an empty slot: length 0, no table entry)
+ * takes the length of parents[k] and the ids of its ceil(len / bs) blocks; each
+ * of those blocks' count goes up by one. Every pair sees the cache as it was
+ * before the call: children are distinct and none is also a parent.
+ *   parents, children  int32 [n_pairs], device
+ *   status_dev         int32 [1], required; nothing happens while it holds an error
+ * All or nothing: an id out of [0, batch), a child that is not empty, a
+ * repeated child or a child that is also a parent sets SV_ERR_BAD_LENGTH; a
+ * parent's block id out of range or with count < 1 sets SV_ERR_BAD_BLOCK_ID.
+ * batch <= 65536.
+ */
+sv_status sv_kv_fork(const sv_paged_kv *kv, const int32_t *parents, const int32_t *children, int32_t n_pairs,
+                     int32_t *status_dev, void *stream);
+
+/*
+ * sv_kv_release -- finished sequences give their blocks back.
+ *
+ * In the order listed, each sequence's blocks, highest logical block first,
+ * lose one reference (without ref_count: every block) and are pushed on the
+ * free list when their count reaches zero; the sequence's table entries become
+ * -1 and its length 0. A block held only by listed sequences is therefore
+ * pushed once, at the last listed sequence that holds it.
+ *   seqs        int32 [n], device: distinct sequence ids
+ *   status_dev  int32 [1], required; nothing happens while it holds an error
+ * All or nothing: an id out of range or repeated sets SV_ERR_BAD_LENGTH; a
+ * block id out of range or a count below the references being dropped sets
+ * SV_ERR_BAD_BLOCK_ID; a free list that would overflow, SV_ERR_OUT_OF_BLOCKS.
+ * batch <= 65536.
+ */
+sv_status sv_kv_release(const sv_paged_kv *kv, const int32_t *seqs, int32_t n, int32_t *status_dev, void *stream);
 
 /*
  * Adaptive draft length: the host-side controller that picks each sequence's

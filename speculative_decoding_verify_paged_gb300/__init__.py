@@ -6,13 +6,14 @@ C ABI in include/spec_verify.h). This package holds the ctypes binding
 seeded synthetic workloads (`workloads`). Importing it loads nothing; the
 library is loaded on the first call and its absence is an error.
 """
-from ._lib import (AdaptiveK, PagedKV, SVError, SV_DTYPE_BF16, SV_DTYPE_F32, SV_MASK_CAUSAL, SV_MASK_TREE, kv_append,
-                   kv_rollback, load, spec_rejection_sample, spec_rejection_sample_workspace_bytes, spec_verify_attn,
-                   spec_verify_attn_workspace_bytes, status_string, tree_greedy_accept)
+from ._lib import (AdaptiveK, PagedKV, SVError, SV_DTYPE_BF16, SV_DTYPE_F32, SV_MASK_CAUSAL, SV_MASK_TREE,
+                   kv_append, kv_fork, kv_release, kv_rollback, load, spec_rejection_sample,
+                   spec_rejection_sample_workspace_bytes, spec_verify_attn, spec_verify_attn_workspace_bytes,
+                   status_string, tree_greedy_accept)
 
 __all__ = [
-    "AdaptiveK", "PagedKV", "SVError", "SV_DTYPE_BF16", "SV_DTYPE_F32", "SV_MASK_CAUSAL", "SV_MASK_TREE", "kv_append",
-    "kv_rollback", "load", "spec_rejection_sample", "spec_rejection_sample_workspace_bytes", "spec_verify_attn",
-    "spec_verify_attn_workspace_bytes",
+    "AdaptiveK", "PagedKV", "SVError", "SV_DTYPE_BF16", "SV_DTYPE_F32", "SV_MASK_CAUSAL", "SV_MASK_TREE",
+    "kv_append", "kv_fork", "kv_release", "kv_rollback", "load", "spec_rejection_sample",
+    "spec_rejection_sample_workspace_bytes", "spec_verify_attn", "spec_verify_attn_workspace_bytes",
     "status_string", "tree_greedy_accept",
 ]

@@ -32,7 +32,7 @@ STATUS_NAMES = {
 
 EXPORTS = ("sv_kv_append", "sv_spec_verify_attn_workspace_bytes", "sv_spec_verify_attn",
            "sv_spec_verify_attn_no_alloc", "sv_spec_rejection_sample_workspace_bytes", "sv_spec_rejection_sample",
-           "sv_tree_greedy_accept", "sv_kv_rollback", "sv_adaptive_k_state_bytes", "sv_adaptive_k_init",
+           "sv_tree_greedy_accept", "sv_kv_rollback", "sv_kv_fork", "sv_kv_release", "sv_adaptive_k_state_bytes", "sv_adaptive_k_init",
            "sv_adaptive_k_update", "sv_adaptive_k_reset", "sv_adaptive_k_current",
            "sv_status_string", "sv_version", "sv_set_option")
 SV_OPT_ATTN_PATH = 1
@@ -61,6 +61,7 @@ class sv_paged_kv(ctypes.Structure):
         ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("max_blocks_per_seq", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("batch", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("ref_count", ctypes.c_void_p),
     ]
 
 
@@ -92,6 +93,8 @@ def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CD
             "sv_spec_rejection_sample": (I, [P, P, I, I, I, P, I, I, P, P, P, F, P, P, P, P, S, P, P]),
             "sv_tree_greedy_accept": (I, [P, I, I, I, P, I, I, P, P, P, P, P, P, P, S, P, P]),
             "sv_kv_rollback": (I, [KVP, P, P, P, I, P, P]),
+            "sv_kv_fork": (I, [KVP, P, P, I, P, P]),
+            "sv_kv_release": (I, [KVP, P, I, P, P]),
             "sv_adaptive_k_state_bytes": (S, [I, I]),
             "sv_adaptive_k_init": (I, [P, S, I, ctypes.POINTER(sv_adaptive_k_params)]),
             "sv_adaptive_k_update": (I, [P, P, P, P]),
@@ -162,13 +165,14 @@ class PagedKV:
     seq_lens: torch.Tensor  # int32 [batch]
     free_list: torch.Tensor  # int32 [num_blocks]
     free_top: torch.Tensor  # int32 [1]
+    ref_count: Optional[torch.Tensor] = None  # int32 [num_blocks]: copy-on-write sharing when given
 
     def struct(self) -> sv_paged_kv:
         nb, hkv, bs, d = self.k_pool.shape
         return sv_paged_kv(
             _ptr(self.k_pool), _ptr(self.v_pool), _ptr(self.block_table), _ptr(self.seq_lens),
             _ptr(self.free_list), _ptr(self.free_top), nb, bs, self.block_table.shape[1], hkv, d,
-            self.seq_lens.shape[0], _dtype_code(self.k_pool))
+            self.seq_lens.shape[0], _dtype_code(self.k_pool), _ptr(self.ref_count))
 
     @property
     def batch(self) -> int:
@@ -268,6 +272,20 @@ def kv_rollback(kv: PagedKV, cu_q: torch.Tensor, accept_count: torch.Tensor, sta
     s = kv.struct()
     _check(load().sv_kv_rollback(ctypes.byref(s), _ptr(cu_q), _ptr(accept_count), _ptr(path_nodes), int(max_q),
                                  _ptr(status), _stream(stream)), "sv_kv_rollback")
+
+
+def kv_fork(kv: PagedKV, parents: torch.Tensor, children: torch.Tensor, status: torch.Tensor, stream=None) -> None:
+    """Children (empty slots) share their parents' blocks copy-on-write; needs kv.ref_count."""
+    s = kv.struct()
+    _check(load().sv_kv_fork(ctypes.byref(s), _ptr(parents), _ptr(children), int(parents.numel()), _ptr(status),
+                             _stream(stream)), "sv_kv_fork")
+
+
+def kv_release(kv: PagedKV, seqs: torch.Tensor, status: torch.Tensor, stream=None) -> None:
+    """Finished sequences give their blocks back (shared blocks at their last holder)."""
+    s = kv.struct()
+    _check(load().sv_kv_release(ctypes.byref(s), _ptr(seqs), int(seqs.numel()), _ptr(status), _stream(stream)),
+           "sv_kv_release")
 
 
 class AdaptiveK:

@@ -63,13 +63,24 @@ __device__ __forceinline__ int blocks_for(int tokens, int bs) { return (tokens +
 // load that does not depend on an earlier one at once: the status word, the
 // free-list top and the first batch of sequence lengths. The ids about to be
 // popped are read once into shared memory, checked, then popped from there.
-constexpr int kIdCache = 4096;
+//
+// With reference counts, a sequence whose first new row lands in a partly
+// filled shared block takes a private copy when the block is still shared at
+// its turn: writer k (in sequence order) of a block held by r sequences copies
+// iff k < r - 1. Its copy is popped just before its new blocks; the new block's
+// count is set to -(old id + 1), which tells the scatter kernel to copy the
+// old block's rows, and the scatter kernel then sets it to 1.
+constexpr int kIdCache = 2048;
+constexpr int kCowMaxBatch = 4096;  // sequences the sharing path handles (one per shared-memory slot)
 
 __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int32_t *cu_q, int32_t *status) {
   grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   grid_dependents_launch();
   __shared__ int s_ids[kIdCache];
+  __shared__ int s_cand[kCowMaxBatch];  // sharing: the shared partial block a sequence writes into, else -1
+  __shared__ int s_copy[kCowMaxBatch];  // sharing: the block a sequence copies, else -1
   const int B = kv.batch, bs = kv.block_size;
+  const bool sharing = kv.ref_count != nullptr;
   const bool failed = status_set(status);
   const int top = *kv.free_top;
   int c0 = 0, n0 = 0;  // the thread's sequence of the first batch
@@ -78,38 +89,86 @@ __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int
     n0 = cu_q[threadIdx.x + 1] - cu_q[threadIdx.x];
   }
   if (failed) return;  // every thread read the same word: the whole CTA leaves
+  auto len_of = [&](int base, int b, int &c, int &n) {
+    c = base == 0 ? c0 : kv.seq_lens[b];
+    n = base == 0 ? n0 : cu_q[b + 1] - cu_q[b];
+  };
 
-  // pass 1: validate lengths, count blocks (the first batch's offsets are kept)
-  int bad_len = 0;
-  int total = 0, off0 = 0, need0 = 0, tot0 = 0;
+  // pass 1: validate lengths; with sharing, find the writers into shared partial blocks
+  int bad_len = 0, bad_id = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    int need = 0;
-    if (b < B) {
-      const int c = base == 0 ? c0 : kv.seq_lens[b];
-      const int n = base == 0 ? n0 : cu_q[b + 1] - cu_q[b];
-      if (c < 0 || n < 0 || blocks_for(c + n, bs) > kv.max_blocks) bad_len = 1;
-      else need = blocks_for(c + n, bs) - blocks_for(c, bs);
+    if (b >= B) continue;
+    int c, n;
+    len_of(base, b, c, n);
+    if (c < 0 || n < 0 || blocks_for(c + n, bs) > kv.max_blocks) {
+      bad_len = 1;
+      continue;
     }
-    int chunk_total;
-    const int off = block_excl_scan(need, &chunk_total);
-    if (base == 0) {
-      off0 = off;
-      need0 = need;
-      tot0 = chunk_total;
+    if (sharing) {
+      int cand = -1;
+      if (n > 0 && c % bs != 0) {
+        const int x = kv.block_table[(size_t)b * kv.max_blocks + c / bs];
+        if (x < 0 || x >= kv.num_blocks) bad_id = 1;
+        else if (kv.ref_count[x] < 1) bad_id = 1;
+        else if (kv.ref_count[x] > 1) cand = x;
+      }
+      s_cand[b] = cand;
     }
-    total += chunk_total;
   }
   if (__syncthreads_or(bad_len)) {
     if (threadIdx.x == 0) record(status, SV_ERR_BAD_LENGTH);
     return;
   }
+  if (__syncthreads_or(bad_id)) {
+    if (threadIdx.x == 0) record(status, SV_ERR_BAD_BLOCK_ID);
+    return;
+  }
+  if (sharing) {  // writer k of a block held by r copies iff k < r - 1
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      const int x = s_cand[b];
+      int copy = -1;
+      if (x >= 0) {
+        int k = 0;
+        for (int e = 0; e < b; ++e) k += s_cand[e] == x;
+        if (k < kv.ref_count[x] - 1) copy = x;
+      }
+      s_copy[b] = copy;
+    }
+    __syncthreads();
+  }
+  // blocks each sequence pops: its copy (if any), then its new blocks
+  auto pops_of = [&](int base, int b, int &first, int &need, int &copy) {
+    int c, n;
+    len_of(base, b, c, n);
+    first = blocks_for(c, bs);
+    need = blocks_for(c + n, bs) - first;
+    copy = sharing ? s_copy[b] : -1;
+  };
+
+  // pass 2: count the pops (the first batch's offsets are kept)
+  int total = 0, off0 = 0, tot0 = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int k = 0;
+    if (b < B) {
+      int first, need, copy;
+      pops_of(base, b, first, need, copy);
+      k = need + (copy >= 0);
+    }
+    int chunk_total;
+    const int off = block_excl_scan(k, &chunk_total);
+    if (base == 0) {
+      off0 = off;
+      tot0 = chunk_total;
+    }
+    total += chunk_total;
+  }
   if (total > top || top > kv.num_blocks) {
     if (threadIdx.x == 0) record(status, SV_ERR_OUT_OF_BLOCKS);
     return;
   }
-  // pass 2: every id about to be popped must be a valid block
-  int bad_id = 0;
+  // pass 3: every id about to be popped must be a valid block
   for (int k = threadIdx.x; k < total; k += blockDim.x) {
     const int id = kv.free_list[top - 1 - k];
     if (k < kIdCache) s_ids[k] = id;
@@ -119,23 +178,37 @@ __global__ void __launch_bounds__(kBookThreads) kv_alloc_kernel(KV kv, const int
     if (threadIdx.x == 0) record(status, SV_ERR_BAD_BLOCK_ID);
     return;
   }
-  // pass 3: pop into the block tables
+  // pass 4: pop into the block tables
   auto popped = [&](int k) { return k < kIdCache ? s_ids[k] : kv.free_list[top - 1 - k]; };
-  if ((int)threadIdx.x < B)
-    for (int j = 0; j < need0; ++j)
-      kv.block_table[(size_t)threadIdx.x * kv.max_blocks + blocks_for(c0, bs) + j] = popped(off0 + j);
+  auto pop_seq = [&](int base, int b, int off) {
+    int first, need, copy;
+    pops_of(base, b, first, need, copy);
+    int32_t *row = kv.block_table + (size_t)b * kv.max_blocks;
+    if (copy >= 0) {
+      const int id = popped(off++);
+      row[first - 1] = id;
+      kv.ref_count[id] = -(copy + 1);  // the scatter kernel copies the rows, then sets 1
+      atomicSub(&kv.ref_count[copy], 1);
+    }
+    for (int j = 0; j < need; ++j) {
+      const int id = popped(off + j);
+      row[first + j] = id;
+      if (sharing) kv.ref_count[id] = 1;
+    }
+  };
+  if ((int)threadIdx.x < B) pop_seq(0, threadIdx.x, off0);
   int carry = tot0;  // batches past the first (more sequences than threads)
   for (int base = blockDim.x; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    int need = 0, first = 0;
+    int k = 0;
     if (b < B) {
-      const int c = kv.seq_lens[b], n = cu_q[b + 1] - cu_q[b];
-      first = blocks_for(c, bs);
-      need = blocks_for(c + n, bs) - first;
+      int first, need, copy;
+      pops_of(base, b, first, need, copy);
+      k = need + (copy >= 0);
     }
     int chunk_total;
-    const int off = carry + block_excl_scan(need, &chunk_total);
-    for (int j = 0; j < need; ++j) kv.block_table[(size_t)b * kv.max_blocks + first + j] = popped(off + j);
+    const int off = carry + block_excl_scan(k, &chunk_total);
+    if (b < B) pop_seq(base, b, off);
     carry += chunk_total;
   }
   __syncthreads();
@@ -191,6 +264,29 @@ __global__ void __launch_bounds__(kScatterThreads) kv_scatter_kernel(KV kv, cons
     return;
   }
   const int slot = pos % kv.block_size;
+  if (i == 0 && slot > 0 && kv.ref_count != nullptr) {
+    // the sequence's first row lands in its private copy of a shared block (see
+    // kv_alloc_kernel): bring over the rows written before, every head, K and V
+    const int m = kv.ref_count[blk];
+    if (m < 0) {
+      const int src = -m - 1;
+      const int per_head = slot * vec_per_row;  // the rows before `slot` are contiguous in a (block, head)
+      const size_t head_bytes = (size_t)kv.block_size * row_bytes;
+      if (src >= 0 && src < kv.num_blocks) {
+        for (int x = threadIdx.x; x < kv.num_kv_heads * per_head; x += blockDim.x) {
+          const int h = x / per_head, v = x - h * per_head;
+          const size_t so = ((size_t)src * kv.num_kv_heads + h) * head_bytes + (size_t)v * 16;
+          const size_t d_o = ((size_t)blk * kv.num_kv_heads + h) * head_bytes + (size_t)v * 16;
+          *reinterpret_cast<uint4 *>((uint8_t *)kv.k_pool + d_o) = *reinterpret_cast<const uint4 *>((const uint8_t *)kv.k_pool + so);
+          *reinterpret_cast<uint4 *>((uint8_t *)kv.v_pool + d_o) = *reinterpret_cast<const uint4 *>((const uint8_t *)kv.v_pool + so);
+        }
+      } else if (threadIdx.x == 0) {
+        record(status, SV_ERR_BAD_BLOCK_ID);
+      }
+      __syncthreads();  // every thread has read the marker
+      if (threadIdx.x == 0) kv.ref_count[blk] = 1;
+    }
+  }
   for (int x = threadIdx.x; x < total; x += blockDim.x) {
     const int h = x / vec_per_row, v = x % vec_per_row;
     uint4 kk = kk0, vv = vv0;
@@ -290,10 +386,12 @@ __global__ void __launch_bounds__(kBookThreads) kv_truncate_kernel(KV kv, const 
         bad_len = 1;
       } else {
         const int old_blocks = blocks_for(c + n, bs), keep = blocks_for(c + a + 1, bs);
-        freed = old_blocks - keep;
-        for (int lb = keep; lb < old_blocks; ++lb) {
+        for (int lb = keep; lb < old_blocks; ++lb) {  // pushed: every block, or (sharing) the last reference
           const int id = kv.block_table[(size_t)b * kv.max_blocks + lb];
           if (id < 0 || id >= kv.num_blocks) bad_id = 1;
+          else if (kv.ref_count == nullptr) ++freed;
+          else if (kv.ref_count[id] < 1) bad_id = 1;
+          else freed += kv.ref_count[id] == 1;
         }
       }
     }
@@ -316,25 +414,234 @@ __global__ void __launch_bounds__(kBookThreads) kv_truncate_kernel(KV kv, const 
   int carry = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    int freed = 0, old_blocks = 0, c = 0, a = 0;
+    int pushed = 0, old_blocks = 0, keep = 0, c = 0, a = 0;
     if (b < B) {
       c = base == 0 ? c0 : kv.seq_lens[b];
       const int n = base == 0 ? n0 : cu_q[b + 1] - cu_q[b];
       a = base == 0 ? a0 : accept[b];
       old_blocks = blocks_for(c + n, bs);
-      freed = old_blocks - blocks_for(c + a + 1, bs);
+      keep = blocks_for(c + a + 1, bs);
+      for (int lb = keep; lb < old_blocks; ++lb)
+        pushed += kv.ref_count == nullptr || kv.ref_count[kv.block_table[(size_t)b * kv.max_blocks + lb]] == 1;
     }
     int chunk_total;
-    const int off = carry + block_excl_scan(freed, &chunk_total);
-    for (int j = 0; j < freed; ++j) {
-      int32_t *e = &kv.block_table[(size_t)b * kv.max_blocks + old_blocks - 1 - j];
-      kv.free_list[top + off + j] = *e;
+    int off = carry + block_excl_scan(pushed, &chunk_total);
+    for (int lb = old_blocks - 1; lb >= keep; --lb) {  // highest logical block first
+      int32_t *e = &kv.block_table[(size_t)b * kv.max_blocks + lb];
+      const int id = *e;
+      if (kv.ref_count == nullptr) {
+        kv.free_list[top + off++] = id;
+      } else if (kv.ref_count[id] == 1) {
+        kv.ref_count[id] = 0;
+        kv.free_list[top + off++] = id;
+      } else {
+        atomicSub(&kv.ref_count[id], 1);
+      }
       *e = -1;
     }
     if (b < B) kv.seq_lens[b] = c + a + 1;
     carry += chunk_total;
   }
   __syncthreads();
+  if (threadIdx.x == 0) *kv.free_top = top + total;
+}
+
+// -------------------------------------------------------------------------
+// fork and release (one CTA each; bitmaps over the sequence ids)
+// -------------------------------------------------------------------------
+constexpr int kMaxSeqBits = 65536;  // sequences the fork and release kernels handle
+
+// Marks bit `i`; true if it was already set.
+__device__ __forceinline__ bool mark(unsigned *bits, int i) {
+  const unsigned m = 1u << (i & 31);
+  return (atomicOr(&bits[i >> 5], m) & m) != 0;
+}
+__device__ __forceinline__ bool marked(const unsigned *bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
+
+__global__ void __launch_bounds__(kBookThreads) kv_fork_kernel(KV kv, const int32_t *parents, const int32_t *children,
+                                                               int n, int32_t *status) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
+  __shared__ unsigned s_child[kMaxSeqBits / 32], s_parent[kMaxSeqBits / 32];
+  const int B = kv.batch, bs = kv.block_size;
+  if (status_set(status)) return;
+  for (int w = threadIdx.x; w < kMaxSeqBits / 32; w += blockDim.x) s_child[w] = s_parent[w] = 0u;
+  __syncthreads();
+  int bad_len = 0, bad_id = 0;
+  for (int k = threadIdx.x; k < n; k += blockDim.x) {
+    const int p = parents[k], c = children[k];
+    if (p < 0 || p >= B || c < 0 || c >= B) {
+      bad_len = 1;
+      continue;
+    }
+    if (mark(s_child, c)) bad_len = 1;  // the same child twice
+    mark(s_parent, p);
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < n && !bad_len; k += blockDim.x) {
+    const int p = parents[k], c = children[k];
+    if (marked(s_parent, c) || kv.seq_lens[c] != 0) {  // a child that is a parent, or not empty
+      bad_len = 1;
+      break;
+    }
+    const int32_t *crow = kv.block_table + (size_t)c * kv.max_blocks;
+    for (int lb = 0; lb < kv.max_blocks; ++lb) bad_len |= crow[lb] != -1;
+    const int len = kv.seq_lens[p];
+    if (len < 0 || blocks_for(len, bs) > kv.max_blocks) {
+      bad_len = 1;
+      break;
+    }
+    const int32_t *prow = kv.block_table + (size_t)p * kv.max_blocks;
+    for (int lb = 0; lb < blocks_for(len, bs); ++lb) {
+      const int id = prow[lb];
+      if (id < 0 || id >= kv.num_blocks || kv.ref_count[id] < 1) bad_id = 1;
+    }
+  }
+  if (__syncthreads_or(bad_len)) {
+    if (threadIdx.x == 0) record(status, SV_ERR_BAD_LENGTH);
+    return;
+  }
+  if (__syncthreads_or(bad_id)) {
+    if (threadIdx.x == 0) record(status, SV_ERR_BAD_BLOCK_ID);
+    return;
+  }
+  for (int k = threadIdx.x; k < n; k += blockDim.x) {
+    const int p = parents[k], c = children[k];
+    const int len = kv.seq_lens[p];
+    const int32_t *prow = kv.block_table + (size_t)p * kv.max_blocks;
+    int32_t *crow = kv.block_table + (size_t)c * kv.max_blocks;
+    for (int lb = 0; lb < blocks_for(len, bs); ++lb) {
+      crow[lb] = prow[lb];
+      atomicAdd(&kv.ref_count[prow[lb]], 1);
+    }
+    kv.seq_lens[c] = len;  // children are not parents: no parent length changes under another thread
+  }
+}
+
+// A block held only by listed sequences goes back at the last listed sequence
+// that holds it. With counts: every listed reference is dropped (atomics); the
+// blocks that reach zero are marked -1, then take the minimum over their
+// holders of -(list index + 2), so the last holder finds its own mark; each
+// sequence then pushes its marked blocks, highest logical block first, at an
+// offset from a scan over the list.
+__global__ void __launch_bounds__(kBookThreads) kv_release_kernel(KV kv, const int32_t *seqs, int n,
+                                                                  int32_t *status) {
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
+  __shared__ unsigned s_seen[kMaxSeqBits / 32];
+  const int B = kv.batch, bs = kv.block_size;
+  const bool sharing = kv.ref_count != nullptr;
+  if (status_set(status)) return;
+  const int top = *kv.free_top;
+  for (int w = threadIdx.x; w < kMaxSeqBits / 32; w += blockDim.x) s_seen[w] = 0u;
+  __syncthreads();
+  int bad_len = 0, bad_id = 0;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int b = seqs[j];
+    if (b < 0 || b >= B || mark(s_seen, b)) {
+      bad_len = 1;
+      continue;
+    }
+    const int len = kv.seq_lens[b];
+    if (len < 0 || blocks_for(len, bs) > kv.max_blocks) {
+      bad_len = 1;
+      continue;
+    }
+    for (int lb = 0; lb < blocks_for(len, bs); ++lb) {
+      const int id = kv.block_table[(size_t)b * kv.max_blocks + lb];
+      if (id < 0 || id >= kv.num_blocks) bad_id = 1;
+    }
+  }
+  if (__syncthreads_or(bad_len)) {
+    if (threadIdx.x == 0) record(status, SV_ERR_BAD_LENGTH);
+    return;
+  }
+  if (__syncthreads_or(bad_id)) {
+    if (threadIdx.x == 0) record(status, SV_ERR_BAD_BLOCK_ID);
+    return;
+  }
+  auto each_ref = [&](auto f) {  // f(list index, block id, logical block) over every listed reference
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+      const int b = seqs[j];
+      for (int lb = blocks_for(kv.seq_lens[b], bs) - 1; lb >= 0; --lb) f(j, kv.block_table[(size_t)b * kv.max_blocks + lb], lb);
+    }
+  };
+  if (sharing) {
+    each_ref([&](int, int id, int) { atomicSub(&kv.ref_count[id], 1); });
+    __syncthreads();
+    each_ref([&](int, int id, int) { bad_id |= kv.ref_count[id] < 0; });
+    if (__syncthreads_or(bad_id)) {  // more references dropped than counted: put the counts back
+      each_ref([&](int, int id, int) { atomicAdd(&kv.ref_count[id], 1); });
+      if (threadIdx.x == 0) record(status, SV_ERR_BAD_BLOCK_ID);
+      return;
+    }
+    each_ref([&](int, int id, int) {
+      if (kv.ref_count[id] == 0) kv.ref_count[id] = -1;  // every writer stores the same value
+    });
+    __syncthreads();
+    each_ref([&](int j, int id, int) {
+      if (kv.ref_count[id] < 0) atomicMin(&kv.ref_count[id], -(j + 2));
+    });
+    __syncthreads();
+  }
+  // pushes of each listed sequence, in list order
+  int total = 0, carry = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    int pushes = 0;
+    if (j < n) {
+      const int b = seqs[j];
+      for (int lb = 0; lb < blocks_for(kv.seq_lens[b], bs); ++lb) {
+        const int id = kv.block_table[(size_t)b * kv.max_blocks + lb];
+        pushes += !sharing || kv.ref_count[id] == -(j + 2);
+      }
+    }
+    int chunk_total;
+    block_excl_scan(pushes, &chunk_total);
+    total += chunk_total;
+  }
+  if (top < 0 || top + total > kv.num_blocks) {
+    // a free list that would overflow: nothing has moved but the counts, which go back
+    if (sharing) {
+      each_ref([&](int, int id, int) {
+        if (kv.ref_count[id] < 0) kv.ref_count[id] = 0;
+      });
+      __syncthreads();
+      each_ref([&](int, int id, int) { atomicAdd(&kv.ref_count[id], 1); });
+    }
+    if (threadIdx.x == 0) record(status, SV_ERR_OUT_OF_BLOCKS);
+    return;
+  }
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    int pushes = 0, b = 0, nb = 0;
+    if (j < n) {
+      b = seqs[j];
+      nb = blocks_for(kv.seq_lens[b], bs);
+      for (int lb = 0; lb < nb; ++lb) {
+        const int id = kv.block_table[(size_t)b * kv.max_blocks + lb];
+        pushes += !sharing || kv.ref_count[id] == -(j + 2);
+      }
+    }
+    int chunk_total;
+    int off = carry + block_excl_scan(pushes, &chunk_total);
+    for (int lb = nb - 1; lb >= 0; --lb) {  // highest logical block first
+      const int id = kv.block_table[(size_t)b * kv.max_blocks + lb];
+      if (!sharing || kv.ref_count[id] == -(j + 2)) kv.free_list[top + off++] = id;
+    }
+    carry += chunk_total;
+  }
+  __syncthreads();  // every mark has been read
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int b = seqs[j];
+    int32_t *row = kv.block_table + (size_t)b * kv.max_blocks;
+    for (int lb = blocks_for(kv.seq_lens[b], bs) - 1; lb >= 0; --lb) {
+      if (sharing && kv.ref_count[row[lb]] < 0) kv.ref_count[row[lb]] = 0;
+      row[lb] = -1;
+    }
+  }
+  __syncthreads();  // lengths are read above until every row is cleared
+  for (int j = threadIdx.x; j < n; j += blockDim.x) kv.seq_lens[seqs[j]] = 0;
   if (threadIdx.x == 0) *kv.free_top = top + total;
 }
 
@@ -357,5 +664,17 @@ cudaError_t launch_kv_rollback(const KV &kv, const int32_t *cu_q, const int32_t 
   }
   return launch_pdl(kv_truncate_kernel, dim3(1), dim3(kBookThreads), 0, st, kv, cu_q, accept, status);
 }
+
+cudaError_t launch_kv_fork(const KV &kv, const int32_t *parents, const int32_t *children, int n_pairs,
+                           int32_t *status, cudaStream_t st) {
+  return launch_pdl(kv_fork_kernel, dim3(1), dim3(kBookThreads), 0, st, kv, parents, children, n_pairs, status);
+}
+
+cudaError_t launch_kv_release(const KV &kv, const int32_t *seqs, int n, int32_t *status, cudaStream_t st) {
+  return launch_pdl(kv_release_kernel, dim3(1), dim3(kBookThreads), 0, st, kv, seqs, n, status);
+}
+
+int kv_cow_max_batch() { return kCowMaxBatch; }
+int kv_max_seq_bits() { return kMaxSeqBits; }
 
 }  // namespace sv

@@ -127,7 +127,7 @@ const char *sv_status_string(int32_t status) {
   }
 }
 
-int32_t sv_version(void) { return 20000; }
+int32_t sv_version(void) { return 30000; }
 
 sv_status sv_set_option(int32_t option, int32_t value) {
   if (option == SV_OPT_ATTN_PATH && value >= SV_ATTN_AUTO && value <= SV_ATTN_WARP_MMA) {
@@ -145,6 +145,7 @@ sv_status sv_kv_append(const sv_paged_kv *kv, const void *new_k, const void *new
   if (total_q > 0 && (new_k == nullptr || new_v == nullptr || !aligned16(new_k) || !aligned16(new_v)))
     return SV_ERR_INVALID_ARG;
   if (kv->batch == 0) return SV_OK;
+  if (kv->ref_count != nullptr && kv->batch > kv_cow_max_batch()) return SV_ERR_UNSUPPORTED;
   return cuda_status(
       launch_kv_append(make_kv(*kv), new_k, new_v, cu_q, total_q, status_dev, (cudaStream_t)stream));
 }
@@ -312,6 +313,26 @@ sv_status sv_kv_rollback(const sv_paged_kv *kv, const int32_t *cu_q, const int32
   if (cu_q == nullptr || accept_count == nullptr) return SV_ERR_INVALID_ARG;
   return cuda_status(launch_kv_rollback(make_kv(*kv), cu_q, accept_count, path_nodes, max_q_per_seq, status_dev,
                                         (cudaStream_t)stream));
+}
+
+sv_status sv_kv_fork(const sv_paged_kv *kv, const int32_t *parents, const int32_t *children, int32_t n_pairs,
+                     int32_t *status_dev, void *stream) {
+  sv_status s = check_kv(kv, false);
+  if (s != SV_OK) return s;
+  if (kv->ref_count == nullptr || status_dev == nullptr || n_pairs < 0) return SV_ERR_INVALID_ARG;
+  if (n_pairs > 0 && (parents == nullptr || children == nullptr)) return SV_ERR_INVALID_ARG;
+  if (kv->batch > kv_max_seq_bits()) return SV_ERR_UNSUPPORTED;
+  if (n_pairs == 0 || kv->batch == 0) return SV_OK;
+  return cuda_status(launch_kv_fork(make_kv(*kv), parents, children, n_pairs, status_dev, (cudaStream_t)stream));
+}
+
+sv_status sv_kv_release(const sv_paged_kv *kv, const int32_t *seqs, int32_t n, int32_t *status_dev, void *stream) {
+  sv_status s = check_kv(kv, true);
+  if (s != SV_OK) return s;
+  if (status_dev == nullptr || n < 0 || (n > 0 && seqs == nullptr)) return SV_ERR_INVALID_ARG;
+  if (kv->batch > kv_max_seq_bits()) return SV_ERR_UNSUPPORTED;
+  if (n == 0 || kv->batch == 0) return SV_OK;
+  return cuda_status(launch_kv_release(make_kv(*kv), seqs, n, status_dev, (cudaStream_t)stream));
 }
 
 }  // extern "C"

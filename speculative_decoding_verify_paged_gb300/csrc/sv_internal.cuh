@@ -103,6 +103,7 @@ struct KV {
   int32_t *seq_lens;
   int32_t *free_list;
   int32_t *free_top;
+  int32_t *ref_count;  // null: no sharing
   int num_blocks, block_size, max_blocks, num_kv_heads, head_dim, batch;
   int elem_bytes;
 };
@@ -115,6 +116,7 @@ inline KV make_kv(const sv_paged_kv &p) {
   k.seq_lens = p.seq_lens;
   k.free_list = p.free_list;
   k.free_top = p.free_top;
+  k.ref_count = p.ref_count;
   k.num_blocks = p.num_blocks;
   k.block_size = p.block_size;
   k.max_blocks = p.max_blocks_per_seq;
@@ -152,6 +154,11 @@ cudaError_t launch_kv_append(const KV &kv, const void *new_k, const void *new_v,
                              int total_q, int32_t *status, cudaStream_t st);
 cudaError_t launch_kv_rollback(const KV &kv, const int32_t *cu_q, const int32_t *accept, const int32_t *path,
                                int max_q, int32_t *status, cudaStream_t st);
+cudaError_t launch_kv_fork(const KV &kv, const int32_t *parents, const int32_t *children, int n_pairs,
+                           int32_t *status, cudaStream_t st);
+cudaError_t launch_kv_release(const KV &kv, const int32_t *seqs, int n, int32_t *status, cudaStream_t st);
+int kv_cow_max_batch();  // batch limit of append and rollback with reference counts
+int kv_max_seq_bits();   // batch limit of fork and release
 cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnArgs &a, int dtype, cudaStream_t st);
 bool attn_tc_supported(const KV &kv, int num_q_heads, int max_q);

@@ -43,13 +43,16 @@ def to_bits(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
-def device_kv(state, device="cuda") -> L.PagedKV:
+def device_kv(state, device="cuda", ref_count=None) -> L.PagedKV:
+    """The cache on the device; `ref_count` (int32 [num_blocks], host) turns on
+    copy-on-write sharing."""
     return L.PagedKV(
         k_pool=_dev(state.k_pool, device, state.dtype), v_pool=_dev(state.v_pool, device, state.dtype),
         block_table=_dev(state.block_table.astype(np.int32), device),
         seq_lens=_dev(state.seq_lens.astype(np.int32), device),
         free_list=_dev(state.free_list.astype(np.int32), device),
-        free_top=torch.tensor([state.free_top], dtype=torch.int32, device=device))
+        free_top=torch.tensor([state.free_top], dtype=torch.int32, device=device),
+        ref_count=None if ref_count is None else _dev(np.asarray(ref_count, np.int32), device))
 
 
 @dataclass
