@@ -48,7 +48,9 @@ def _load():
         lib.so_paged_attention.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, I, P, I, I, P, D, P, I, P]
         lib.so_rejection_sample.argtypes = [I, I, P, P, P, I, P, P, P, D, I, P, P, P, P, P]
         lib.so_tree_greedy.argtypes = [I, I, P, P, I, P, P, I, P, P, P, P]
-        for f in (lib.so_dense_attention, lib.so_paged_attention, lib.so_rejection_sample, lib.so_tree_greedy):
+        lib.so_tree_sample.argtypes = [I, I, P, P, I, P, P, P, P, D, I, P, P, P, P, P, P]
+        for f in (lib.so_dense_attention, lib.so_paged_attention, lib.so_rejection_sample, lib.so_tree_greedy,
+                  lib.so_tree_sample):
             f.restype = I
         _lib = lib
     return _lib
@@ -162,6 +164,26 @@ def tree_greedy(step, *, max_q: int | None = None) -> SampleResult:
                                 _p(_c(step.parent, np.int32)), mq, _p(acc), _p(path), _p(out_tok), _p(num))
     _check(rc, "tree_greedy")
     return SampleResult(acc, out_tok, num, path_nodes=path)
+
+
+def tree_sample(step, *, temperature: float | None = None, max_q: int | None = None) -> SampleResult:
+    """Lossless tree verification at T > 0 (see so_tree_sample for the reading)."""
+    T = step.temperature if temperature is None else temperature
+    B = step.n_q.shape[0]
+    mq = step.max_q if max_q is None else max_q
+    acc = np.zeros(B, np.int32)
+    path = np.full((B, mq), -1, np.int32)
+    out_tok = np.full((B, mq), -1, np.int32)
+    num = np.zeros(B, np.int32)
+    marg = np.zeros(B, np.float64)
+    fb = np.zeros(B, np.int32)
+    rc = _load().so_tree_sample(B, step.vocab, _p(_c(step.cu_q, np.int32)), _p(_c(step.target_logits)),
+                                _DT[step.logits_dtype], _p(_c(step.draft_tokens, np.int32)),
+                                _p(_c(step.parent, np.int32)), _p(_c(step.u_accept, np.float32)),
+                                _p(_c(step.u_resample, np.float32)), float(T), mq, _p(acc), _p(path), _p(out_tok),
+                                _p(num), _p(marg), _p(fb))
+    _check(rc, "tree_sample")
+    return SampleResult(acc, out_tok, num, marg, fb, path_nodes=path)
 
 
 # ----------------------------------------------------------------------------

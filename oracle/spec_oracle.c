@@ -416,3 +416,108 @@ int so_tree_greedy(int batch, int vocab, const int32_t *cu_q, const void *tgt, i
   }
   return SO_OK;
 }
+
+/*
+ * Lossless verification of a draft tree at temperature T > 0.
+ *
+ * The pages fix only the greedy tree rule; the reading taken: a node's
+ * children carry distinct candidate tokens picked without sampling (the top-k
+ * of the draft at that node), so each child is a proposal that puts all its
+ * mass on its token. The rejection rule with such a proposal accepts x with
+ * probability p(x), and on rejection leaves the residual p with x's mass
+ * removed, renormalised. Walking from the root: at the current node v (target
+ * distribution p_v = softmax(row v / T)), its children are tried in row order;
+ * child c with token x is accepted iff u_acc[c] < p'(x), where p' is p_v with
+ * the tokens of the siblings rejected before it removed and renormalised (0 if
+ * x itself was removed); the first accepted child becomes the current node.
+ * When no child is accepted (or v has none), y is drawn by inverse CDF with
+ * u_res from p' (p_v without the rejected tokens); if they held all of p_v's
+ * mass, from p_v itself (fallback[b] = 1). Each emitted token is distributed
+ * as the target's p at its position.
+ *
+ * Node j >= 1 of sequence b: row cu_q[b]+j, parent row parent[cu_q[b]+j],
+ * token node_tok[cu_q[b]-b+j-1], accept uniform u_acc[cu_q[b]-b+j-1].
+ * Outputs as so_tree_greedy; margin[b] = the smallest distance between a
+ * uniform and the threshold it was compared with (u_acc against p'(x), and the
+ * CDF crossing of the draw).
+ */
+int so_tree_sample(int batch, int vocab, const int32_t *cu_q, const void *tgt, int dtype, const int32_t *node_tok,
+                   const int32_t *parent, const float *u_acc, const float *u_res, double temperature, int max_q,
+                   int32_t *accept_cnt, int32_t *path_nodes, int32_t *out_tok, int32_t *num_out, double *margin,
+                   int32_t *fallback) {
+  if (batch < 0 || vocab <= 0 || max_q <= 0 || !(temperature > 0.0)) return SO_ERR_ARG;
+  double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
+  double *w = (double *)malloc(sizeof(double) * (size_t)vocab);
+  if (!p || !w) {
+    free(p);
+    free(w);
+    return SO_ERR_NOMEM;
+  }
+  int rc = SO_OK;
+  for (int b = 0; b < batch && rc == SO_OK; ++b) {
+    int n = cu_q[b + 1] - cu_q[b];
+    if (n < 1 || n > max_q) {
+      rc = SO_ERR_ARG;
+      break;
+    }
+    size_t t0 = (size_t)cu_q[b];
+    size_t d0 = (size_t)cu_q[b] - (size_t)b;
+    for (int j = 0; j < max_q; ++j) {
+      out_tok[(size_t)b * max_q + j] = -1;
+      path_nodes[(size_t)b * max_q + j] = -1;
+    }
+    double marg = INFINITY;
+    int cur = 0, a = 0, y = -1, fb = 0;
+    for (;;) {
+      if ((rc = softmax_row(tgt, dtype, t0 + cur, vocab, temperature, p)) != SO_OK) break;
+      for (int v = 0; v < vocab; ++v) w[v] = p[v];  /* p' before normalisation: removed tokens get 0 */
+      double removed = 0.0;
+      int next = -1;
+      for (int j = 1; j < n && next < 0; ++j) {
+        if (parent[t0 + j] != cur) continue;
+        int x = node_tok[d0 + j - 1];
+        if (x < 0 || x >= vocab) {
+          rc = SO_ERR_TOKEN;
+          break;
+        }
+        double thr = removed < 1.0 ? w[x] / (1.0 - removed) : 0.0;
+        double u = (double)u_acc[d0 + j - 1];
+        double dist = fabs(u - thr);
+        if (dist < marg) marg = dist;
+        if (u < thr) {
+          next = j;
+        } else {
+          removed += w[x];
+          w[x] = 0.0;
+        }
+      }
+      if (rc != SO_OK) break;
+      if (next < 0) {
+        double S = 0.0, m2 = INFINITY;
+        for (int v = 0; v < vocab; ++v) S += w[v];
+        double ur = (double)u_res[b];
+        if (S > 0.0) {
+          y = inverse_cdf(w, vocab, ur * S, S, &m2);
+        } else {
+          fb = 1;
+          y = inverse_cdf(p, vocab, ur, 1.0, &m2);
+        }
+        if (m2 < marg) marg = m2;
+        break;
+      }
+      path_nodes[(size_t)b * max_q + a] = next;
+      out_tok[(size_t)b * max_q + a] = node_tok[d0 + next - 1];
+      ++a;
+      cur = next;
+    }
+    if (rc != SO_OK) break;
+    out_tok[(size_t)b * max_q + a] = y;
+    accept_cnt[b] = a;
+    num_out[b] = a + 1;
+    if (margin) margin[b] = marg;
+    if (fallback) fallback[b] = fb;
+  }
+  free(p);
+  free(w);
+  return rc;
+}
