@@ -341,6 +341,7 @@ def run_native(args):
         "clocks": clk,
         "adaptive_k": adaptive_k_timing(),
         "cow": cow_timing(),
+        "tree_sampler": tree_sampler_timing(hbm_peak),
     }
     if e2e is not None:
         line["e2e"] = e2e
@@ -355,6 +356,39 @@ def run_native(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
+
+
+def tree_sampler_timing(hbm_peak, reps=20):
+    """The tree sampler on the draft-tree workload (16 trees of 60 nodes + root,
+    V = 32000 bf16): greedy (sv_tree_greedy_accept) and lossless at T = 1
+    (sv_tree_rejection_sample). Device time per call, CUDA events, L2 flushed
+    before each call; bytes = every target row once."""
+    import torch
+    from speculative_decoding_verify_paged_gb300 import step as S
+    from speculative_decoding_verify_paged_gb300 import workloads as W
+    out = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for name, T in (("greedy", 0.0), ("t1", 1.0)):
+        case = W.tree(temperature=T)
+        d = S.DeviceStep.from_host(case.step)
+        kv = S.device_kv(case.state)
+        buf = S.StepBuffers.make(kv, d, int((case.state.seq_lens + case.step.n_q).max()))
+        S.sample(d, buf)
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            S.sample(d, buf)
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        t = float(np.mean(ms))
+        nbytes = case.step.target_logits.shape[0] * case.step.vocab * 2
+        out[name] = {"us": t * 1e3, "bytes": int(nbytes), "achieved_gbs": nbytes / (t / 1e3) / 1e9,
+                     "frac": nbytes / (t / 1e3) / 1e9 / hbm_peak, "status": int(buf.status.item())}
+        del kv, buf, d
+    return out
 
 
 def cow_timing(reps=5):

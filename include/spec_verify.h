@@ -292,6 +292,36 @@ sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype,
                                 size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /*
+ * sv_tree_rejection_sample -- lossless verification of a draft tree at
+ * temperature T > 0 (T == 0: sv_tree_greedy_accept). The pages fix only the
+ * greedy tree rule; the reading implemented: a node's children carry distinct
+ * candidate tokens picked without sampling (the top-k of the draft at that
+ * node), so each child is a proposal with all its mass on its token, which the
+ * rejection rule accepts with probability p(x), leaving on rejection p with x
+ * removed, renormalised. From the root, at node v (p_v = softmax(row v / T)):
+ * children in row order; child c with token x is accepted iff
+ * u_accept[cu_q[b] - b + c - 1] < p'(x), p' being p_v without the tokens of
+ * the siblings rejected before (0 for a token already rejected); the first
+ * accepted child becomes the current node. When no child is accepted, or v has
+ * none, y is drawn by inverse CDF with u_resample[b] from p' (from p_v if the
+ * rejected tokens held all its mass). Every emitted token is then distributed
+ * as p at its position. Node rows are in BFS order (parent row < row), else
+ * SV_ERR_BAD_LENGTH.
+ *   arguments and outputs as sv_tree_greedy_accept, plus u_accept (float
+ *   [total_q - batch]) and u_resample (float [batch]) in [0, 1); the workspace
+ *   is sized with sv_spec_rejection_sample_workspace_bytes(..., temperature 0)
+ *   (target rows only); no draft logits are read.
+ * Arithmetic as sv_spec_rejection_sample: p'(x) in fp32 from the row
+ * statistics, the draw exact in 64-bit fixed point.
+ */
+sv_status sv_tree_rejection_sample(const void *target_logits, int32_t logits_dtype, int32_t vocab, int32_t batch,
+                                   const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq,
+                                   const int32_t *node_tokens, const int32_t *parent, const float *u_accept,
+                                   const float *u_resample, float temperature, int32_t *accept_count,
+                                   int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, void *workspace,
+                                   size_t workspace_bytes, int32_t *status_dev, void *stream);
+
+/*
  * sv_kv_rollback -- keep each sequence's accepted prefix, give back the rest.
  *
  * The new length is c_b + a_b + 1: the last emitted token and the a_b

@@ -9,11 +9,11 @@ library is loaded on the first call and its absence is an error.
 from ._lib import (AdaptiveK, PagedKV, SVError, SV_DTYPE_BF16, SV_DTYPE_F32, SV_MASK_CAUSAL, SV_MASK_TREE,
                    kv_append, kv_fork, kv_release, kv_rollback, load, spec_rejection_sample,
                    spec_rejection_sample_workspace_bytes, spec_verify_attn, spec_verify_attn_workspace_bytes,
-                   status_string, tree_greedy_accept)
+                   status_string, tree_greedy_accept, tree_rejection_sample)
 
 __all__ = [
     "AdaptiveK", "PagedKV", "SVError", "SV_DTYPE_BF16", "SV_DTYPE_F32", "SV_MASK_CAUSAL", "SV_MASK_TREE",
     "kv_append", "kv_fork", "kv_release", "kv_rollback", "load", "spec_rejection_sample",
     "spec_rejection_sample_workspace_bytes", "spec_verify_attn", "spec_verify_attn_workspace_bytes",
-    "status_string", "tree_greedy_accept",
+    "status_string", "tree_greedy_accept", "tree_rejection_sample",
 ]

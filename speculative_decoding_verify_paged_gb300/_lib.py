@@ -32,7 +32,7 @@ STATUS_NAMES = {
 
 EXPORTS = ("sv_kv_append", "sv_spec_verify_attn_workspace_bytes", "sv_spec_verify_attn",
            "sv_spec_verify_attn_no_alloc", "sv_spec_rejection_sample_workspace_bytes", "sv_spec_rejection_sample",
-           "sv_tree_greedy_accept", "sv_kv_rollback", "sv_kv_fork", "sv_kv_release", "sv_adaptive_k_state_bytes", "sv_adaptive_k_init",
+           "sv_tree_greedy_accept", "sv_tree_rejection_sample", "sv_kv_rollback", "sv_kv_fork", "sv_kv_release", "sv_adaptive_k_state_bytes", "sv_adaptive_k_init",
            "sv_adaptive_k_update", "sv_adaptive_k_reset", "sv_adaptive_k_current",
            "sv_status_string", "sv_version", "sv_set_option")
 SV_OPT_ATTN_PATH = 1
@@ -92,6 +92,7 @@ def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CD
             "sv_spec_rejection_sample_workspace_bytes": (S, [I, I, I, I, F]),
             "sv_spec_rejection_sample": (I, [P, P, I, I, I, P, I, I, P, P, P, F, P, P, P, P, S, P, P]),
             "sv_tree_greedy_accept": (I, [P, I, I, I, P, I, I, P, P, P, P, P, P, P, S, P, P]),
+            "sv_tree_rejection_sample": (I, [P, I, I, I, P, I, I, P, P, P, P, F, P, P, P, P, P, S, P, P]),
             "sv_kv_rollback": (I, [KVP, P, P, P, I, P, P]),
             "sv_kv_fork": (I, [KVP, P, P, I, P, P]),
             "sv_kv_release": (I, [KVP, P, I, P, P]),
@@ -265,6 +266,21 @@ def tree_greedy_accept(target_logits: torch.Tensor, cu_q: torch.Tensor, node_tok
         int(target_logits.shape[0]), int(out_tokens.shape[1]), _ptr(node_tokens), _ptr(parent),
         _ptr(accept_count), _ptr(path_nodes), _ptr(out_tokens), _ptr(num_out), _ptr(ws), ws_bytes, _ptr(status),
         _stream(stream)), "sv_tree_greedy_accept")
+
+
+def tree_rejection_sample(target_logits: torch.Tensor, cu_q: torch.Tensor, node_tokens: torch.Tensor,
+                          parent: torch.Tensor, u_accept: torch.Tensor, u_resample: torch.Tensor, temperature: float,
+                          accept_count: torch.Tensor, path_nodes: torch.Tensor, out_tokens: torch.Tensor,
+                          num_out: torch.Tensor, *, workspace: Optional[torch.Tensor] = None,
+                          status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Lossless tree verification at T > 0 (children as point-mass proposals)."""
+    batch = int(cu_q.shape[0]) - 1
+    ws, ws_bytes = _sampler_workspace(workspace, target_logits, batch, 0.0)
+    _check(load().sv_tree_rejection_sample(
+        _ptr(target_logits), _dtype_code(target_logits), int(target_logits.shape[1]), batch, _ptr(cu_q),
+        int(target_logits.shape[0]), int(out_tokens.shape[1]), _ptr(node_tokens), _ptr(parent), _ptr(u_accept),
+        _ptr(u_resample), float(temperature), _ptr(accept_count), _ptr(path_nodes), _ptr(out_tokens), _ptr(num_out),
+        _ptr(ws), ws_bytes, _ptr(status), _stream(stream)), "sv_tree_rejection_sample")
 
 
 def kv_rollback(kv: PagedKV, cu_q: torch.Tensor, accept_count: torch.Tensor, status: torch.Tensor, *,

@@ -445,6 +445,10 @@ struct Smem {
   float uacc[kMaxQ];             // accept uniforms
   int tok[kMaxQ];                // draft tokens (chain) or node tokens (tree)
   int par[kMaxQ];                // tree: parent row of each row
+  int path[kMaxQ];               // tree at T > 0: rows of the accepted nodes
+  int excl[kMaxQ];               // tree at T > 0: tokens rejected at the final node
+  int nexcl;
+  int cur;                       // tree at T > 0: the final node's row
   long long S[2];    // phase 3: this CTA's fixed-point weight sum per pass (cluster-visible)
   long long ll_buf[kWarps];
   long long P_owner, target;
@@ -476,6 +480,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
   const int d0 = t0 - b;
   const int lo = min(V, rank * args.chunk), hi = min(V, lo + args.chunk);
   const int len = hi - lo;
+  constexpr bool STOCH = MODE == kStochastic || MODE == kTreeStochastic;  // (max, sum) statistics
   const int rows = (MODE == kStochastic) ? n + K : n;
   const T *tgt = reinterpret_cast<const T *>(args.tgt);
   const T *drf = reinterpret_cast<const T *>(args.drf);
@@ -498,7 +503,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
     const int gr = r < n ? t0 + r : args.total_q + d0 + (r - n);  // row of the statistics kernel
     const size_t p0 = (size_t)gr * nchunk * kStatWarps;
     const int np = nchunk * kStatWarps;
-    if constexpr (MODE == kStochastic) {
+    if constexpr (STOCH) {
       float m = -INFINITY, s = 0.f;
       for (int q0 = 0; q0 < np; q0 += 128) {  // four loads of each array in flight per lane
         float lm[4], lsum[4];
@@ -547,7 +552,19 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
   }
   // the sequence's small inputs into shared memory, so the serial scans below read no global memory
   if (tid < K) sm.tok[tid] = args.draft_tok[d0 + tid];
-  if (MODE == kTree && tid < n) sm.par[tid] = args.parent[t0 + tid];
+  if ((MODE == kTree || MODE == kTreeStochastic) && tid < n) sm.par[tid] = args.parent[t0 + tid];
+  if constexpr (MODE == kTreeStochastic) {
+    if (tid < K) {  // node tid + 1: its accept uniform and its token's target logit in its parent's row
+      sm.uacc[tid] = args.u_acc[d0 + tid];
+      const int x = args.draft_tok[d0 + tid], pr = args.parent[t0 + tid + 1];
+      sm.gtl[tid] = 0.f;
+      if (x < 0 || x >= V) {
+        if (rank == 0) record(args.status, SV_ERR_BAD_TOKEN);
+      } else if (pr >= 0 && pr < n) {
+        sm.gtl[tid] = to_f32(tgt[(size_t)(t0 + pr) * V + x]);
+      }
+    }
+  }
   if constexpr (MODE == kStochastic) {
     if (tid < K) {  // the accept uniform and the target and draft logits of each draft token
       sm.uacc[tid] = args.u_acc[d0 + tid];
@@ -613,6 +630,41 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
       args.num_out[b] = a + 1;
     }
   } else {
+    if constexpr (MODE == kTreeStochastic) {
+      // ---------------- the tree walk (identical in every CTA, one thread) ----------------
+      // at the current node, children in row order: child x is accepted iff u < p'(x), p'
+      // the node's p without the tokens of the siblings rejected before, renormalised
+      if (tid == 0) {
+        bool good = true;
+        for (int j = 1; j < n; ++j) good &= sm.par[j] >= 0 && sm.par[j] < j;
+        bool nz = false;
+        for (int r = 0; r < n; ++r) nz |= !(sm.Z[r] > 0.f);
+        if (nz && rank == 0) record(args.status, SV_ERR_NONFINITE);
+        if (!good && rank == 0) record(args.status, SV_ERR_BAD_LENGTH);
+        int cur = 0, a = 0, nexcl = 0;
+        float removed = 0.f;
+        for (int j = 1; good && j < n; ++j) {
+          if (sm.par[j] != cur) continue;
+          const int x = sm.tok[j - 1];
+          bool dup = false;
+          for (int e = 0; e < nexcl; ++e) dup |= sm.excl[e] == x;
+          const float px = dup ? 0.f : exp2f((sm.gtl[j - 1] - sm.M[cur]) * coef) / sm.Z[cur];
+          const float thr = removed < 1.f ? px / (1.f - removed) : 0.f;
+          if (sm.uacc[j - 1] < thr) {  // accepted: the walk goes on from this child
+            sm.path[a++] = j;
+            cur = j;
+            nexcl = 0;
+            removed = 0.f;
+          } else {
+            removed += px;
+            if (!dup) sm.excl[nexcl++] = x;
+          }
+        }
+        sm.a = a;
+        sm.cur = cur;
+        sm.nexcl = nexcl;
+      }
+    } else {
     // ---------------- accept scan (identical in every CTA): one lane per draft, first rejection by ballot ----------------
     if (warp == 0) {
       unsigned rej[2];
@@ -641,12 +693,16 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
         sm.rho_lo = (float)(rho - (double)sm.rho_hi);
       }
     }
+    }
     __syncthreads();
     const int a = sm.a;
-    const bool resid = a < K;
-    const T *trow = tgt + (size_t)(t0 + a) * V;
+    // the row of the draw: the first rejected position (chain) or the walk's last node (tree)
+    const int dr = MODE == kTreeStochastic ? sm.cur : a;
+    const bool resid = MODE == kStochastic && a < K;         // residual max(0, p - q) of a chain
+    const int nexcl = MODE == kTreeStochastic ? sm.nexcl : 0;  // tokens left out of p (tree)
+    const T *trow = tgt + (size_t)(t0 + dr) * V;
     const T *drow = resid ? drf + (size_t)(d0 + a) * V : nullptr;
-    const float Mt = sm.M[a], Md = resid ? sm.M[n + a] : 0.f;
+    const float Mt = sm.M[dr], Md = resid ? sm.M[n + a] : 0.f;
     const float chi = args.coef, clo = args.coef_lo;
     const float ur = args.u_res[b];
     const int pair_off = ((len * (int)sizeof(T) + 127) / 128) * 128;
@@ -693,6 +749,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
 
     for (int pass = 0; pass < 2; ++pass) {
       const bool res_pass = resid && pass == 0;
+      const bool excl_pass = nexcl > 0 && pass == 0;
       // the eight weights of group g, in [0, 1]: proportional to max(0, p_v - q_v)
       // (scaled by Z_t), or to p_v
       auto weights8 = [&](int g, long long (&w)[kGroup]) {
@@ -710,6 +767,13 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
         } else {
 #pragma unroll
           for (int k = 0; k < kGroup; ++k) w[k] = to_fix(exp2_acc(xt[k] - Mt, chi, clo));
+          if (excl_pass) {  // the rejected children's tokens carry no mass
+            const int v0 = lo + g * kGroup;
+            for (int e = 0; e < nexcl; ++e) {
+              const int d = sm.excl[e] - v0;
+              if (d >= 0 && d < kGroup) w[d] = 0;
+            }
+          }
         }
       };
       // ---- pass B: each group's mass and this CTA's total ----
@@ -744,7 +808,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
         const int owner_l = hit ? __ffs(hit) - 1 : -1;
         const long long P_l = __shfl_sync(0xffffffffu, inc - Sq, owner_l < 0 ? 0 : owner_l);
         if (lane == 0) {
-          sm.fallback = (res_pass && S == 0) ? 1 : 0;
+          sm.fallback = ((res_pass || excl_pass) && S == 0) ? 1 : 0;
           if (owner_l >= 0) {
             sm.owner = owner_l;
             sm.P_owner = P_l;
@@ -808,7 +872,15 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
             }
           }
           int32_t *o = args.out_tok + (size_t)b * args.max_q;
-          for (int j = 0; j < args.max_q; ++j) o[j] = j < a ? sm.tok[j] : -1;
+          if constexpr (MODE == kTreeStochastic) {
+            int32_t *path = args.path + (size_t)b * args.max_q;
+            for (int j = 0; j < args.max_q; ++j) {
+              o[j] = j < a ? sm.tok[sm.path[j] - 1] : -1;
+              path[j] = j < a ? sm.path[j] : -1;
+            }
+          } else {
+            for (int j = 0; j < args.max_q; ++j) o[j] = j < a ? sm.tok[j] : -1;
+          }
           o[a] = y;
           args.accept[b] = a;
           args.num_out[b] = a + 1;
@@ -850,7 +922,8 @@ cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int
   sa.items = items;
   sa.per = per;
   sa.coef = a.coef;
-  auto skern = stats_kernel<T, VEC, MODE>;
+  constexpr int SMODE = MODE == kTreeStochastic ? kStochastic : MODE;  // statistics of the target rows
+  auto skern = stats_kernel<T, VEC, SMODE>;
   const int sdyn = VEC ? kStatStages * kPartBytes : 0;
   cudaError_t e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, sdyn);
   if (e != cudaSuccess) return e;
@@ -858,12 +931,13 @@ cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int
   if (e != cudaSuccess) return e;
 
   // ---- decisions ----
-  const int C = MODE == kStochastic ? pick_cluster(a.batch, a.vocab) : 1;
+  constexpr bool STOCH = MODE == kStochastic || MODE == kTreeStochastic;
+  const int C = STOCH ? pick_cluster(a.batch, a.vocab) : 1;
   SamplerArgs da = a;
   da.chunk = ((a.vocab + C - 1) / C + 7) / 8 * 8;
   auto dkern = decide_kernel<T, VEC, MODE>;
   int ring = 0, dyn = 0;
-  if (MODE == kStochastic) {
+  if (STOCH) {
     const int pair = ((da.chunk * (int)sizeof(T) + 127) / 128) * 128;
     ring = 2 * pair;
     dyn = ring + (da.chunk + kGroup - 1) / kGroup * (int)sizeof(long long);
@@ -907,6 +981,7 @@ cudaError_t launch_d(const SamplerArgs &a, int mode, float *pm, float *ps, int n
   switch (mode) {
     case kStochastic: return launch_m<T, kStochastic>(a, pm, ps, nchunk, rows, st);
     case kGreedy: return launch_m<T, kGreedy>(a, pm, ps, nchunk, rows, st);
+    case kTreeStochastic: return launch_m<T, kTreeStochastic>(a, pm, ps, nchunk, rows, st);
     default: return launch_m<T, kTree>(a, pm, ps, nchunk, rows, st);
   }
 }

@@ -304,6 +304,52 @@ sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype,
   return cuda_status(launch_sampler(a, logits_dtype, kTree, workspace, (cudaStream_t)stream));
 }
 
+sv_status sv_tree_rejection_sample(const void *target_logits, int32_t logits_dtype, int32_t vocab, int32_t batch,
+                                   const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq,
+                                   const int32_t *node_tokens, const int32_t *parent, const float *u_accept,
+                                   const float *u_resample, float temperature, int32_t *accept_count,
+                                   int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, void *workspace,
+                                   size_t workspace_bytes, int32_t *status_dev, void *stream) {
+  if (temperature == 0.f)
+    return sv_tree_greedy_accept(target_logits, logits_dtype, vocab, batch, cu_q, total_q, max_q_per_seq,
+                                 node_tokens, parent, accept_count, path_nodes, out_tokens, num_out, workspace,
+                                 workspace_bytes, status_dev, stream);
+  if (logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F32) return SV_ERR_INVALID_ARG;
+  if (vocab < 1 || batch < 0 || batch > 65535 || total_q < batch || max_q_per_seq < 1 || max_q_per_seq > kMaxQ)
+    return SV_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || temperature == INFINITY) return SV_ERR_INVALID_ARG;
+  if (!sampler_supports(vocab)) return SV_ERR_UNSUPPORTED;
+  if (batch == 0) return SV_OK;
+  if (target_logits == nullptr || cu_q == nullptr || parent == nullptr || accept_count == nullptr ||
+      path_nodes == nullptr || out_tokens == nullptr || num_out == nullptr || u_resample == nullptr)
+    return SV_ERR_INVALID_ARG;
+  if (total_q > batch && (node_tokens == nullptr || u_accept == nullptr)) return SV_ERR_INVALID_ARG;
+  const sv_status ws = check_sampler_workspace(workspace, workspace_bytes, logits_dtype, vocab, batch, total_q,
+                                               kTreeStochastic);
+  if (ws != SV_OK) return ws;
+  SamplerArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.tgt = target_logits;
+  a.cu_q = cu_q;
+  a.draft_tok = node_tokens;
+  a.parent = parent;
+  a.u_acc = u_accept;
+  a.u_res = u_resample;
+  a.accept = accept_count;
+  a.out_tok = out_tokens;
+  a.num_out = num_out;
+  a.path = path_nodes;
+  a.status = status_dev;
+  a.vocab = vocab;
+  a.batch = batch;
+  a.max_q = max_q_per_seq;
+  a.total_q = total_q;
+  const double c = 1.4426950408889634 / (double)temperature;
+  a.coef = (float)c;
+  a.coef_lo = (float)(c - (double)a.coef);
+  return cuda_status(launch_sampler(a, logits_dtype, kTreeStochastic, workspace, (cudaStream_t)stream));
+}
+
 sv_status sv_kv_rollback(const sv_paged_kv *kv, const int32_t *cu_q, const int32_t *accept_count,
                          const int32_t *path_nodes, int32_t max_q_per_seq, int32_t *status_dev, void *stream) {
   sv_status s = check_kv(kv, true);

@@ -186,7 +186,7 @@ struct SamplerArgs {
   float coef;     // log2(e) / temperature, rounded to fp32
   float coef_lo;  // log2(e) / temperature - coef
 };
-enum SamplerMode { kStochastic = 0, kGreedy = 1, kTree = 2 };
+enum SamplerMode { kStochastic = 0, kGreedy = 1, kTree = 2, kTreeStochastic = 3 };
 // Bytes of the partials workspace: rows (total_q target rows, plus total_q - batch
 // draft rows for kStochastic) x 32 KB items x 8 warps x (max, sum); 0 if the sizes
 // are invalid or too large.

@@ -142,7 +142,11 @@ def attention(kv, d: DeviceStep, buf: StepBuffers, max_seq_len: int, stream=None
 
 
 def sample(d: DeviceStep, buf: StepBuffers, stream=None):
-    if d.mask_kind == L.SV_MASK_TREE:
+    if d.mask_kind == L.SV_MASK_TREE and d.temperature > 0.0:
+        L.tree_rejection_sample(d.target_logits, d.cu_q, d.draft_tokens, d.parent, d.u_accept, d.u_resample,
+                                d.temperature, buf.accept, buf.path, buf.out_tok, buf.num_out,
+                                workspace=buf.sampler_ws, status=buf.status, stream=stream)
+    elif d.mask_kind == L.SV_MASK_TREE:
         L.tree_greedy_accept(d.target_logits, d.cu_q, d.draft_tokens, d.parent, buf.accept, buf.path, buf.out_tok,
                              buf.num_out, workspace=buf.sampler_ws, status=buf.status, stream=stream)
     else:

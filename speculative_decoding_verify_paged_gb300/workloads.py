@@ -401,8 +401,10 @@ def full_tree(branching) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
 def tree(seed: int = 5, *, batch: int = 16, ctx: int = 8192, block_size: int = 64,
          branching=(4, 3, 2, 2, 1, 1), keep: int = 60, vocab: int = 32000,
          num_q_heads: int = 32, num_kv_heads: int = 8, head_dim: int = 128,
-         target_sigma: float = 3.0, draft_coef: float = 0.8, draft_sigma: float = 1.0) -> Case:
-    """EAGLE/Medusa-style draft trees at long context, greedy acceptance.
+         target_sigma: float = 3.0, draft_coef: float = 0.8, draft_sigma: float = 1.0,
+         temperature: float = 0.0) -> Case:
+    """EAGLE/Medusa-style draft trees at long context, greedy acceptance (or, at
+    temperature > 0, the lossless tree rule with seeded uniforms).
 
     The drafter expands the full tree `branching` (184 nodes for {4,3,2,2,1,1});
     a node's children carry the top-k tokens of the draft distribution at that
@@ -467,9 +469,12 @@ def tree(seed: int = 5, *, batch: int = 16, ctx: int = 8192, block_size: int = 6
     q = to_bf16_bits(rng.standard_normal((Tq, num_q_heads, head_dim), dtype=np.float32))
     new_k = to_bf16_bits(rng.standard_normal((Tq, num_kv_heads, head_dim), dtype=np.float32))
     new_v = to_bf16_bits(rng.standard_normal((Tq, num_kv_heads, head_dim), dtype=np.float32))
+    urng = _rng(seed, 43)
+    u_acc = urng.random(Tq - batch, dtype=np.float32) if temperature > 0 else np.zeros(Tq - batch, np.float32)
+    u_res = urng.random(batch, dtype=np.float32) if temperature > 0 else np.zeros(batch, np.float32)
     step = StepInputs(n_q, cu_q, num_q_heads, q, new_k, new_v, vocab, "bf16",
                       np.concatenate(tgt_rows), np.concatenate(drf_rows), np.concatenate(toks),
-                      np.zeros(Tq - batch, np.float32), np.zeros(batch, np.float32), 0.0,
+                      u_acc, u_res, float(temperature),
                       mask_kind="tree", tree_mask=np.concatenate(masks), parent=np.concatenate(parents))
     return Case("tree", seed, state, step, {"branching": tuple(branching), "keep": keep})
 

@@ -9,7 +9,8 @@ from speculative_decoding_verify_paged_gb300 import _lib as L
 from speculative_decoding_verify_paged_gb300 import step as S
 from speculative_decoding_verify_paged_gb300 import workloads as W
 
-from _helpers import appended_rows, assert_kv_equal, kv_host, status_of, upload
+from _helpers import (appended_rows, assert_kv_equal, compare_samples, gpu_sample_result, kv_host, max_seq_len,
+                      status_of, upload)
 
 pytestmark = pytest.mark.gpu
 
@@ -107,6 +108,31 @@ def test_tree_rollback_compacts_path():
             pos = c0[b] + j
             rows.append((okv.bt[b][pos // okv.bs], pos % okv.bs))
     assert_kv_equal(kv, okv, rows=rows)
+
+
+def test_tree_step_at_temperature():
+    """The whole step with a stochastic tree: append, attention, tree rejection
+    sample, rollback with the accepted path, against the oracle."""
+    case = W.tree(batch=4, ctx=1000, vocab=512, temperature=1.0)
+    kv, d, buf = upload(case)
+    okv = oracle.OracleKV(case.state)
+    c0 = list(okv.seq_lens)
+    S.run_step(kv, d, buf, max_seq_len(case.state, case.step))
+    okv.append(case.step)
+    ref = oracle.tree_sample(case.step)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    got = gpu_sample_result(buf)
+    compare_samples(case.step, got, ref)
+    if np.array_equal(got[0], ref.accept_cnt):
+        np.testing.assert_array_equal(buf.path.cpu().numpy(), ref.path_nodes)
+        okv.rollback(case.step, ref.accept_cnt, path_nodes=ref.path_nodes)
+        rows = []
+        for b in range(case.state.batch):
+            for j in range(ref.accept_cnt[b] + 1):
+                pos = c0[b] + j
+                rows.append((okv.bt[b][pos // okv.bs], pos % okv.bs))
+        assert_kv_equal(kv, okv, rows=rows)
 
 
 def test_out_of_blocks_is_all_or_nothing():

@@ -1,5 +1,5 @@
-"""GPU parity of sv_spec_rejection_sample / sv_tree_greedy_accept against the
-oracle: accept counts and emitted tokens bit-exact, except at oracle-flagged
+"""GPU parity of sv_spec_rejection_sample / sv_tree_greedy_accept /
+sv_tree_rejection_sample against the oracle: accept counts and emitted tokens bit-exact, except at oracle-flagged
 near-ties (|u - min(1, p/q)| < 1e-4 or a CDF crossing within 1e-4), whose
 divergences must stay below 0.01% of the verified positions. Greedy and tree
 decisions are exact (argmax, lowest index on ties)."""
@@ -28,7 +28,10 @@ def _sample(case):
 
 def _check(case):
     got = _sample(case)
-    if case.step.mask_kind == "tree":
+    if case.step.mask_kind == "tree" and case.step.temperature > 0:
+        ref = oracle.tree_sample(case.step)
+        compare_samples(case.step, got, ref)  # near-ties as for chains
+    elif case.step.mask_kind == "tree":
         ref = oracle.tree_greedy(case.step)
         compare_samples(case.step, got, ref, tree=True)
     else:
@@ -54,6 +57,58 @@ def test_contbatch_first_iteration():
 def test_tree_full_size():
     got, ref = _check(W.tree())
     assert ref.accept_cnt.max() >= 2  # the trees do get walked
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_tree_stochastic_full_size(T):
+    """16 trees of 60 nodes at V = 32000: paths and tokens equal the oracle's."""
+    case = W.tree(temperature=T)
+    kv, d, buf = upload(case)
+    S.sample(d, buf)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    got = gpu_sample_result(buf)
+    ref = oracle.tree_sample(case.step)
+    compare_samples(case.step, got, ref)
+    path = buf.path.cpu().numpy()
+    for b in range(case.state.batch):
+        if got[0][b] == ref.accept_cnt[b]:
+            np.testing.assert_array_equal(path[b], ref.path_nodes[b])
+    assert ref.accept_cnt.max() >= 1
+
+
+def test_tree_stochastic_many_small_trees():
+    """3000 copies of a 7-node tree over 8 tokens with fresh uniforms: every
+    decision and draw equals the oracle's (whose law is pinned by chi-square)."""
+    rng = np.random.default_rng(45)
+    V, trials = 8, 3000
+    parent = [-1, 0, 0, 0, 1, 1, 2]
+    n = len(parent)
+    tgt = (rng.standard_normal((n, V)) * 1.5).astype(np.float32)
+    tok = [-1, 3, 0, 6, 1, 2, 5]
+    n_q = np.full(trials, n, np.int32)
+    cu = np.zeros(trials + 1, np.int32)
+    cu[1:] = np.cumsum(n_q)
+    dummy = np.zeros((cu[-1], 1, 1), np.float32)
+    step = W.StepInputs(n_q, cu, 1, dummy, dummy, dummy, V, "f32", np.tile(tgt, (trials, 1)),
+                        np.zeros((trials * (n - 1), V), np.float32), np.tile(np.array(tok[1:], np.int32), trials),
+                        rng.random(trials * (n - 1), dtype=np.float32), rng.random(trials, dtype=np.float32), 0.9,
+                        mask_kind="tree", parent=np.tile(np.array(parent, np.int32), trials))
+    dev = "cuda"
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    acc = torch.empty(trials, dtype=torch.int32, device=dev)
+    path = torch.empty((trials, n), dtype=torch.int32, device=dev)
+    out = torch.empty((trials, n), dtype=torch.int32, device=dev)
+    num = torch.empty(trials, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    L.tree_rejection_sample(t(step.target_logits), t(step.cu_q), t(step.draft_tokens), t(step.parent),
+                            t(step.u_accept), t(step.u_resample), 0.9, acc, path, out, num, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.tree_sample(step)
+    compare_samples(step, (acc.cpu().numpy(), out.cpu().numpy(), num.cpu().numpy()), ref)
+    same = acc.cpu().numpy() == ref.accept_cnt
+    np.testing.assert_array_equal(path.cpu().numpy()[same], ref.path_nodes[same])
 
 
 @pytest.mark.parametrize("V,dtype", [(5, "f32"), (4099, "bf16"), (20000, "f32"), (131072, "bf16"),
