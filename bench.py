@@ -423,13 +423,15 @@ def cow_timing(reps=5):
     accept = torch.zeros(B, dtype=torch.int32, device="cuda")
     times = {"fork": [], "append_with_copies": [], "release": []}
     copies = 0
+    lens = ctx[:P].astype(np.int64)
     for r in range(reps):
+        copies += int(sum(C for b in range(P) if lens[b] % 16))  # the last of the C + 1 writers writes in place
+        lens += 1  # rollback keeps one row of each sequence (a = 0)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        torch.cuda._sleep(2_000_000)  # keeps the GPU busy while the host queues the calls: no launch gaps timed
         ev[0].record()
         L.kv_fork(kv, parents, children, status)
         ev[1].record()
-        lens = kv.seq_lens.cpu().numpy()
-        copies += int(sum(C for b in range(P) if lens[b] % 16))  # the last of the C + 1 writers writes in place
         ev[2].record()
         L.kv_append(kv, d.new_k, d.new_v, d.cu_q, status)
         ev[3].record()

@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(kBookThreads) kv_fork_kernel(KV kv, const int3
   grid_dependents_launch();
   __shared__ unsigned s_child[kMaxSeqBits / 32], s_parent[kMaxSeqBits / 32];
   const int B = kv.batch, bs = kv.block_size;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   if (status_set(status)) return;
   for (int w = threadIdx.x; w < kMaxSeqBits / 32; w += blockDim.x) s_child[w] = s_parent[w] = 0u;
   __syncthreads();
@@ -477,22 +478,22 @@ __global__ void __launch_bounds__(kBookThreads) kv_fork_kernel(KV kv, const int3
     if (mark(s_child, c)) bad_len = 1;  // the same child twice
     mark(s_parent, p);
   }
-  __syncthreads();
-  for (int k = threadIdx.x; k < n && !bad_len; k += blockDim.x) {
+  if (__syncthreads_or(bad_len)) {
+    if (threadIdx.x == 0) record(status, SV_ERR_BAD_LENGTH);
+    return;
+  }
+  // one warp per pair, lanes over the table entries
+  for (int k = warp; k < n; k += nwarps) {
     const int p = parents[k], c = children[k];
-    if (marked(s_parent, c) || kv.seq_lens[c] != 0) {  // a child that is a parent, or not empty
-      bad_len = 1;
-      break;
+    const int len = kv.seq_lens[p];
+    if (marked(s_parent, c) || kv.seq_lens[c] != 0 || len < 0 || blocks_for(len, bs) > kv.max_blocks) {
+      bad_len = 1;  // a child that is a parent, or not empty; a parent too long
+      continue;
     }
     const int32_t *crow = kv.block_table + (size_t)c * kv.max_blocks;
-    for (int lb = 0; lb < kv.max_blocks; ++lb) bad_len |= crow[lb] != -1;
-    const int len = kv.seq_lens[p];
-    if (len < 0 || blocks_for(len, bs) > kv.max_blocks) {
-      bad_len = 1;
-      break;
-    }
     const int32_t *prow = kv.block_table + (size_t)p * kv.max_blocks;
-    for (int lb = 0; lb < blocks_for(len, bs); ++lb) {
+    for (int lb = lane; lb < kv.max_blocks; lb += 32) bad_len |= crow[lb] != -1;
+    for (int lb = lane; lb < blocks_for(len, bs); lb += 32) {
       const int id = prow[lb];
       if (id < 0 || id >= kv.num_blocks || kv.ref_count[id] < 1) bad_id = 1;
     }
@@ -505,16 +506,16 @@ __global__ void __launch_bounds__(kBookThreads) kv_fork_kernel(KV kv, const int3
     if (threadIdx.x == 0) record(status, SV_ERR_BAD_BLOCK_ID);
     return;
   }
-  for (int k = threadIdx.x; k < n; k += blockDim.x) {
+  for (int k = warp; k < n; k += nwarps) {
     const int p = parents[k], c = children[k];
     const int len = kv.seq_lens[p];
     const int32_t *prow = kv.block_table + (size_t)p * kv.max_blocks;
     int32_t *crow = kv.block_table + (size_t)c * kv.max_blocks;
-    for (int lb = 0; lb < blocks_for(len, bs); ++lb) {
+    for (int lb = lane; lb < blocks_for(len, bs); lb += 32) {
       crow[lb] = prow[lb];
       atomicAdd(&kv.ref_count[prow[lb]], 1);
     }
-    kv.seq_lens[c] = len;  // children are not parents: no parent length changes under another thread
+    if (lane == 0) kv.seq_lens[c] = len;  // children are not parents: no parent length changes under another warp
   }
 }
 
@@ -523,13 +524,17 @@ __global__ void __launch_bounds__(kBookThreads) kv_fork_kernel(KV kv, const int3
 // blocks that reach zero are marked -1, then take the minimum over their
 // holders of -(list index + 2), so the last holder finds its own mark; each
 // sequence then pushes its marked blocks, highest logical block first, at an
-// offset from a scan over the list.
+// offset from a scan over the list. One warp per listed sequence, lanes over
+// its blocks; the list goes through in batches of one sequence per thread for
+// the scan.
 __global__ void __launch_bounds__(kBookThreads) kv_release_kernel(KV kv, const int32_t *seqs, int n,
                                                                   int32_t *status) {
   grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   grid_dependents_launch();
   __shared__ unsigned s_seen[kMaxSeqBits / 32];
+  __shared__ int s_cnt[kBookThreads];  // pushes of each sequence of the batch, then its offset
   const int B = kv.batch, bs = kv.block_size;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const bool sharing = kv.ref_count != nullptr;
   if (status_set(status)) return;
   const int top = *kv.free_top;
@@ -543,106 +548,113 @@ __global__ void __launch_bounds__(kBookThreads) kv_release_kernel(KV kv, const i
       continue;
     }
     const int len = kv.seq_lens[b];
-    if (len < 0 || blocks_for(len, bs) > kv.max_blocks) {
-      bad_len = 1;
-      continue;
-    }
-    for (int lb = 0; lb < blocks_for(len, bs); ++lb) {
-      const int id = kv.block_table[(size_t)b * kv.max_blocks + lb];
-      if (id < 0 || id >= kv.num_blocks) bad_id = 1;
-    }
+    if (len < 0 || blocks_for(len, bs) > kv.max_blocks) bad_len = 1;
   }
   if (__syncthreads_or(bad_len)) {
     if (threadIdx.x == 0) record(status, SV_ERR_BAD_LENGTH);
     return;
   }
+  auto each_ref = [&](auto f) {  // f(list index, block id) over every listed reference, a warp per sequence
+    for (int j = warp; j < n; j += nwarps) {
+      const int b = seqs[j];
+      const int32_t *row = kv.block_table + (size_t)b * kv.max_blocks;
+      for (int lb = lane; lb < blocks_for(kv.seq_lens[b], bs); lb += 32) f(j, row[lb]);
+    }
+  };
+  each_ref([&](int, int id) { bad_id |= id < 0 || id >= kv.num_blocks; });
   if (__syncthreads_or(bad_id)) {
     if (threadIdx.x == 0) record(status, SV_ERR_BAD_BLOCK_ID);
     return;
   }
-  auto each_ref = [&](auto f) {  // f(list index, block id, logical block) over every listed reference
-    for (int j = threadIdx.x; j < n; j += blockDim.x) {
-      const int b = seqs[j];
-      for (int lb = blocks_for(kv.seq_lens[b], bs) - 1; lb >= 0; --lb) f(j, kv.block_table[(size_t)b * kv.max_blocks + lb], lb);
-    }
-  };
   if (sharing) {
-    each_ref([&](int, int id, int) { atomicSub(&kv.ref_count[id], 1); });
+    each_ref([&](int, int id) { atomicSub(&kv.ref_count[id], 1); });
     __syncthreads();
-    each_ref([&](int, int id, int) { bad_id |= kv.ref_count[id] < 0; });
+    each_ref([&](int, int id) { bad_id |= kv.ref_count[id] < 0; });
     if (__syncthreads_or(bad_id)) {  // more references dropped than counted: put the counts back
-      each_ref([&](int, int id, int) { atomicAdd(&kv.ref_count[id], 1); });
+      each_ref([&](int, int id) { atomicAdd(&kv.ref_count[id], 1); });
       if (threadIdx.x == 0) record(status, SV_ERR_BAD_BLOCK_ID);
       return;
     }
-    each_ref([&](int, int id, int) {
+    each_ref([&](int, int id) {
       if (kv.ref_count[id] == 0) kv.ref_count[id] = -1;  // every writer stores the same value
     });
     __syncthreads();
-    each_ref([&](int j, int id, int) {
+    each_ref([&](int j, int id) {
       if (kv.ref_count[id] < 0) atomicMin(&kv.ref_count[id], -(j + 2));
     });
     __syncthreads();
   }
-  // pushes of each listed sequence, in list order
-  int total = 0, carry = 0;
-  for (int base = 0; base < n; base += blockDim.x) {
-    const int j = base + threadIdx.x;
-    int pushes = 0;
-    if (j < n) {
-      const int b = seqs[j];
-      for (int lb = 0; lb < blocks_for(kv.seq_lens[b], bs); ++lb) {
-        const int id = kv.block_table[(size_t)b * kv.max_blocks + lb];
-        pushes += !sharing || kv.ref_count[id] == -(j + 2);
-      }
-    }
-    int chunk_total;
-    block_excl_scan(pushes, &chunk_total);
-    total += chunk_total;
-  }
-  if (top < 0 || top + total > kv.num_blocks) {
+  auto pushed = [&](int j, int id) { return !sharing || kv.ref_count[id] == -(j + 2); };
+  // total pushes, to check the free list's room before anything moves
+  int mine = 0;
+  each_ref([&](int j, int id) { mine += pushed(j, id); });
+  __shared__ int s_total;
+  if (threadIdx.x == 0) s_total = 0;
+  __syncthreads();
+  if (mine) atomicAdd(&s_total, mine);
+  __syncthreads();
+  const int all = s_total;
+  if (top < 0 || top + all > kv.num_blocks) {
     // a free list that would overflow: nothing has moved but the counts, which go back
     if (sharing) {
-      each_ref([&](int, int id, int) {
+      each_ref([&](int, int id) {
         if (kv.ref_count[id] < 0) kv.ref_count[id] = 0;
       });
       __syncthreads();
-      each_ref([&](int, int id, int) { atomicAdd(&kv.ref_count[id], 1); });
+      each_ref([&](int, int id) { atomicAdd(&kv.ref_count[id], 1); });
     }
     if (threadIdx.x == 0) record(status, SV_ERR_OUT_OF_BLOCKS);
     return;
   }
+  // pushes in list order: batches of blockDim.x sequences; warps count, threads scan, warps push
+  int carry = 0;
   for (int base = 0; base < n; base += blockDim.x) {
-    const int j = base + threadIdx.x;
-    int pushes = 0, b = 0, nb = 0;
-    if (j < n) {
-      b = seqs[j];
-      nb = blocks_for(kv.seq_lens[b], bs);
-      for (int lb = 0; lb < nb; ++lb) {
-        const int id = kv.block_table[(size_t)b * kv.max_blocks + lb];
-        pushes += !sharing || kv.ref_count[id] == -(j + 2);
+    const int cnt_n = min((int)blockDim.x, n - base);
+    for (int jj = warp; jj < cnt_n; jj += nwarps) {
+      const int j = base + jj, b = seqs[j];
+      const int32_t *row = kv.block_table + (size_t)b * kv.max_blocks;
+      int c = 0;
+      for (int lb = lane; lb < blocks_for(kv.seq_lens[b], bs); lb += 32) c += pushed(j, row[lb]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      if (lane == 0) s_cnt[jj] = c;
+    }
+    __syncthreads();
+    int chunk_total;
+    const int v = (int)threadIdx.x < cnt_n ? s_cnt[threadIdx.x] : 0;
+    const int off = carry + block_excl_scan(v, &chunk_total);
+    if ((int)threadIdx.x < cnt_n) s_cnt[threadIdx.x] = off;
+    __syncthreads();
+    for (int jj = warp; jj < cnt_n; jj += nwarps) {
+      const int j = base + jj, b = seqs[j];
+      const int32_t *row = kv.block_table + (size_t)b * kv.max_blocks;
+      const int nb = blocks_for(kv.seq_lens[b], bs);
+      int pos = top + s_cnt[jj];
+      for (int c0 = 0; c0 < nb; c0 += 32) {  // highest logical block first
+        const int lb = nb - 1 - (c0 + lane);
+        const int id = lb >= 0 ? row[lb] : -1;
+        const bool push = lb >= 0 && pushed(j, id);
+        const unsigned m = __ballot_sync(0xffffffffu, push);
+        if (push) kv.free_list[pos + __popc(m & ((1u << lane) - 1u))] = id;
+        pos += __popc(m);
       }
     }
-    int chunk_total;
-    int off = carry + block_excl_scan(pushes, &chunk_total);
-    for (int lb = nb - 1; lb >= 0; --lb) {  // highest logical block first
-      const int id = kv.block_table[(size_t)b * kv.max_blocks + lb];
-      if (!sharing || kv.ref_count[id] == -(j + 2)) kv.free_list[top + off++] = id;
-    }
     carry += chunk_total;
+    __syncthreads();  // s_cnt is reused by the next batch
   }
   __syncthreads();  // every mark has been read
-  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+  each_ref([&](int, int id) {
+    if (sharing && kv.ref_count[id] < 0) kv.ref_count[id] = 0;
+  });
+  __syncthreads();  // the rows are still read above
+  for (int j = warp; j < n; j += nwarps) {
     const int b = seqs[j];
     int32_t *row = kv.block_table + (size_t)b * kv.max_blocks;
-    for (int lb = blocks_for(kv.seq_lens[b], bs) - 1; lb >= 0; --lb) {
-      if (sharing && kv.ref_count[row[lb]] < 0) kv.ref_count[row[lb]] = 0;
-      row[lb] = -1;
-    }
+    for (int lb = lane; lb < blocks_for(kv.seq_lens[b], bs); lb += 32) row[lb] = -1;
   }
   __syncthreads();  // lengths are read above until every row is cleared
   for (int j = threadIdx.x; j < n; j += blockDim.x) kv.seq_lens[seqs[j]] = 0;
-  if (threadIdx.x == 0) *kv.free_top = top + total;
+  if (threadIdx.x == 0) *kv.free_top = top + all;
 }
 
 }  // namespace

@@ -349,6 +349,39 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
             }
             ls += acc0 + acc1;
           }
+        } else if constexpr (VEC && sizeof(T) == 2) {
+          // argmax on bf16 pairs: a group of 8 is looked into only when its packed
+          // maximum beats the lane's best (ties keep the lower index seen first)
+#pragma unroll
+          for (int u = 0; u < SL / 256; ++u) {
+            const int e = s0 + 8 * (lane + 32 * u);
+            const uint4 q = *reinterpret_cast<const uint4 *>(src + e);
+            uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            if (e + 8 > cnt) {
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                if (e + 2 * p >= cnt) w[p] = (w[p] & 0xffff0000u) | 0xff80u;
+                if (e + 2 * p + 1 >= cnt) w[p] = (w[p] & 0xffffu) | 0xff800000u;
+              }
+            }
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(w);
+            const __nv_bfloat162 m2 = __hmax2_nan(__hmax2_nan(h[0], h[1]), __hmax2_nan(h[2], h[3]));
+            const float ga = __low2float(m2), gb = __high2float(m2);
+            if (ga != ga || gb != gb) {
+              bad = 1;
+            } else if (e < cnt) {
+              const float gm = fmaxf(ga, gb);
+              if (lbi < 0 || gm > lb) {
+                int p = 0;
+                for (; p < 7; ++p) {
+                  const uint32_t wp = w[p >> 1];
+                  if (__uint_as_float((p & 1) ? (wp & 0xffff0000u) : (wp << 16)) == gm) break;
+                }
+                lb = gm;
+                lbi = e0 + e + p;
+              }
+            }
+          }
         } else {
         float x[SL / 32];
 #pragma unroll
