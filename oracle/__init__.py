@@ -30,8 +30,11 @@ def build(force: bool = False) -> str:
     """Compile spec_oracle.c with gcc (IEEE fp64, no fast-math)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
-                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        base = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off"]
+        try:  # OpenMP when the compiler has it (results do not depend on the thread count)
+            subprocess.check_call(base + ["-fopenmp", "-o", tmp, _SRC, "-lm"], stderr=subprocess.DEVNULL)
+        except subprocess.CalledProcessError:
+            subprocess.check_call(base + ["-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -49,11 +52,19 @@ def _load():
         lib.so_rejection_sample.argtypes = [I, I, P, P, P, I, P, P, P, D, I, P, P, P, P, P]
         lib.so_tree_greedy.argtypes = [I, I, P, P, I, P, P, I, P, P, P, P]
         lib.so_tree_sample.argtypes = [I, I, P, P, I, P, P, P, P, D, I, P, P, P, P, P, P]
+        lib.so_set_threads.argtypes = [I]
+        lib.so_set_threads.restype = I
         for f in (lib.so_dense_attention, lib.so_paged_attention, lib.so_rejection_sample, lib.so_tree_greedy,
                   lib.so_tree_sample):
             f.restype = I
         _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Threads of the oracle's parallel loops (OpenMP); returns the count in use.
+    Values do not depend on it."""
+    return int(_load().so_set_threads(int(n)))
 
 
 def _p(a: np.ndarray):

@@ -32,6 +32,11 @@
  * Precision: every sum, product, exp and division is in IEEE fp64, in plain
  * left-to-right loops (compile without -ffast-math). bf16 inputs (uint16 bit
  * patterns) are widened exactly.
+ *
+ * Threads (OpenMP, when built with it): attention runs its (sequence, KV head)
+ * pairs, the chain sampler its sequences, as independent tasks; every result is
+ * computed by one task in the same order as on one thread, so the values do
+ * not depend on the thread count.
  */
 #include <math.h>
 #include <stdint.h>
@@ -44,6 +49,21 @@
 #define SO_ERR_TOKEN (-3)
 #define SO_ERR_NONFINITE (-4)
 #define SO_ERR_NOMEM (-5)
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads of the parallel loops below (1: one thread). Returns the count in use. */
+int so_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}
 
 /* dtype codes: 0 = bf16 stored as uint16 bit patterns, 1 = fp32 */
 static double widen(const void *base, int dtype, size_t i) {
@@ -149,23 +169,29 @@ int so_paged_attention(int batch, int hq, int hkv, int d, int bs, int max_blocks
                        int n_seqs, double *out) {
   if (batch < 0 || bs <= 0 || hkv <= 0 || hq % hkv != 0) return SO_ERR_ARG;
   int count = seqs ? n_seqs : batch;
-  for (int si = 0; si < count; ++si) {
+  for (int si = 0; si < count; ++si) {  /* lengths and table room first */
     int b = seqs ? seqs[si] : si;
     if (b < 0 || b >= batch) return SO_ERR_ARG;
+    int c = ctx_lens[b], n = cu_q[b + 1] - cu_q[b];
+    if (c < 0 || n < 0) return SO_ERR_ARG;
+    if ((c + n + bs - 1) / bs > max_blocks) return SO_ERR_BLOCK;
+  }
+  const int group = hq / hkv;
+  const long ntask = (long)count * hkv;
+  int rc_all = SO_OK;
+  /* one task per (sequence, KV head): its keys and values, its `group` query heads */
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long task = 0; task < ntask; ++task) {
+    int si = (int)(task / hkv), kh = (int)(task % hkv);
+    int b = seqs ? seqs[si] : si;
     int c = ctx_lens[b];
     int n = cu_q[b + 1] - cu_q[b];
     int L = c + n;
-    if (c < 0 || n < 0) return SO_ERR_ARG;
-    if ((L + bs - 1) / bs > max_blocks) return SO_ERR_BLOCK;
-    double *kd = (double *)malloc(sizeof(double) * ((size_t)L * hkv * d + 1));
-    double *vd = (double *)malloc(sizeof(double) * ((size_t)L * hkv * d + 1));
-    double *qd = (double *)malloc(sizeof(double) * ((size_t)n * hq * d + 1));
-    double *od = (double *)malloc(sizeof(double) * ((size_t)n * hq * d + 1));
-    if (!kd || !vd || !qd || !od) {
-      free(kd); free(vd); free(qd); free(od);
-      return SO_ERR_NOMEM;
-    }
-    int rc = SO_OK;
+    double *kd = (double *)malloc(sizeof(double) * ((size_t)L * d + 1));
+    double *vd = (double *)malloc(sizeof(double) * ((size_t)L * d + 1));
+    double *qd = (double *)malloc(sizeof(double) * ((size_t)n * group * d + 1));
+    double *od = (double *)malloc(sizeof(double) * ((size_t)n * group * d + 1));
+    int rc = (kd && vd && qd && od) ? SO_OK : SO_ERR_NOMEM;
     for (int t = 0; t < L && rc == SO_OK; ++t) {
       int blk = block_table[(size_t)b * max_blocks + t / bs];
       if (blk < 0 || blk >= num_blocks) {
@@ -173,26 +199,35 @@ int so_paged_attention(int batch, int hq, int hkv, int d, int bs, int max_blocks
         break;
       }
       int slot = t % bs;
-      for (int kh = 0; kh < hkv; ++kh)
-        for (int e = 0; e < d; ++e) {
-          size_t src = (((size_t)blk * hkv + kh) * bs + slot) * d + e;
-          size_t dst = ((size_t)t * hkv + kh) * d + e;
-          kd[dst] = widen(k_pool, kv_dtype, src);
-          vd[dst] = widen(v_pool, kv_dtype, src);
-        }
+      for (int e = 0; e < d; ++e) {
+        size_t src = (((size_t)blk * hkv + kh) * bs + slot) * d + e;
+        kd[(size_t)t * d + e] = widen(k_pool, kv_dtype, src);
+        vd[(size_t)t * d + e] = widen(v_pool, kv_dtype, src);
+      }
     }
     if (rc == SO_OK) {
       size_t row0 = (size_t)cu_q[b];
-      for (size_t x = 0; x < (size_t)n * hq * d; ++x) qd[x] = widen(q, q_dtype, row0 * hq * d + x);
-      rc = so_dense_attention(L, c, n, hq, hkv, d, kd, vd, qd, mask_kind,
-                              tree_mask ? &tree_mask[row0] : NULL, scale, od);
-      if (rc == SO_OK) memcpy(&out[row0 * hq * d], od, sizeof(double) * (size_t)n * hq * d);
+      for (int i = 0; i < n; ++i)
+        for (int g = 0; g < group; ++g)
+          for (int e = 0; e < d; ++e)
+            qd[((size_t)i * group + g) * d + e] =
+                widen(q, q_dtype, ((row0 + i) * hq + (size_t)kh * group + g) * d + e);
+      rc = so_dense_attention(L, c, n, group, 1, d, kd, vd, qd, mask_kind, tree_mask ? &tree_mask[row0] : NULL,
+                              scale, od);
+      if (rc == SO_OK)
+        for (int i = 0; i < n; ++i)
+          memcpy(&out[((row0 + i) * hq + (size_t)kh * group) * d], &od[(size_t)i * group * d],
+                 sizeof(double) * (size_t)group * d);
     }
     free(kd); free(vd); free(qd); free(od);
-    if (rc != SO_OK) return rc;
+    if (rc != SO_OK) {
+#pragma omp critical(so_rc)
+      rc_all = rc;
+    }
   }
-  return SO_OK;
+  return rc_all;
 }
+
 
 /* ------------------------------------------------------------------------ */
 /* Sampler                                                                  */
@@ -277,97 +312,104 @@ static int inverse_cdf(const double *w, int V, double target, double total, doub
  * threshold it was compared with (|u - min(1,p/q)|, and the CDF crossing);
  * +inf for greedy.
  */
+/* One sequence of so_rejection_sample; p and qd are scratch of `vocab` doubles. */
+static int rejection_one(int b, int vocab, const int32_t *cu_q, const void *tgt, const void *drf, int dtype,
+                         const int32_t *draft_tok, const float *u_acc, const float *u_res, double temperature,
+                         int max_q, int32_t *accept_cnt, int32_t *out_tok, int32_t *num_out, double *margin,
+                         int32_t *fallback, double *p, double *qd) {
+  int rc = SO_OK;
+  int n = cu_q[b + 1] - cu_q[b];
+  int K = n - 1;
+  if (n < 1 || n > max_q) return SO_ERR_ARG;
+  size_t t0 = (size_t)cu_q[b];
+  size_t d0 = (size_t)cu_q[b] - (size_t)b;
+  for (int j = 0; j < max_q; ++j) out_tok[(size_t)b * max_q + j] = -1;
+  double marg = INFINITY;
+  int fb = 0;
+  int a = K, y = -1;
+  if (temperature == 0.0) {
+    for (int i = 0; i < K; ++i) {
+      int am;
+      if ((rc = argmax_row(tgt, dtype, t0 + i, vocab, &am)) != SO_OK) return rc;
+      int x = draft_tok[d0 + i];
+      if (x != am) {
+        a = i;
+        y = am;
+        break;
+      }
+    }
+    if (a == K && (rc = argmax_row(tgt, dtype, t0 + K, vocab, &y)) != SO_OK) return rc;
+  } else {
+    for (int i = 0; i < K; ++i) {
+      int x = draft_tok[d0 + i];
+      if (x < 0 || x >= vocab) return SO_ERR_TOKEN;
+      if ((rc = softmax_row(tgt, dtype, t0 + i, vocab, temperature, p)) != SO_OK) return rc;
+      if ((rc = softmax_row(drf, dtype, d0 + i, vocab, temperature, qd)) != SO_OK) return rc;
+      double ratio = qd[x] > 0.0 ? p[x] / qd[x] : INFINITY;
+      double thr = ratio < 1.0 ? ratio : 1.0;
+      double u = (double)u_acc[d0 + i];
+      double dist = fabs(u - thr);
+      if (dist < marg) marg = dist;
+      if (!(u < thr)) {
+        a = i;
+        break;
+      }
+    }
+    double m2 = INFINITY;
+    double ur = (double)u_res[b];
+    if (a < K) {
+      /* p and qd still hold row a */
+      double S = 0.0;
+      for (int v = 0; v < vocab; ++v) {
+        double r = p[v] - qd[v];
+        qd[v] = r > 0.0 ? r : 0.0;
+        S += qd[v];
+      }
+      if (S > 0.0) {
+        y = inverse_cdf(qd, vocab, ur * S, S, &m2);
+      } else {
+        fb = 1;
+        y = inverse_cdf(p, vocab, ur, 1.0, &m2);
+      }
+    } else {
+      if ((rc = softmax_row(tgt, dtype, t0 + K, vocab, temperature, p)) != SO_OK) return rc;
+      y = inverse_cdf(p, vocab, ur, 1.0, &m2);
+    }
+    if (m2 < marg) marg = m2;
+  }
+  accept_cnt[b] = a;
+  for (int j = 0; j < a; ++j) out_tok[(size_t)b * max_q + j] = draft_tok[d0 + j];
+  out_tok[(size_t)b * max_q + a] = y;
+  num_out[b] = a + 1;
+  if (margin) margin[b] = marg;
+  if (fallback) fallback[b] = fb;
+  return SO_OK;
+}
+
 int so_rejection_sample(int batch, int vocab, const int32_t *cu_q, const void *tgt, const void *drf,
                         int dtype, const int32_t *draft_tok, const float *u_acc, const float *u_res,
                         double temperature, int max_q, int32_t *accept_cnt, int32_t *out_tok,
                         int32_t *num_out, double *margin, int32_t *fallback) {
   if (batch < 0 || vocab <= 0 || max_q <= 0) return SO_ERR_ARG;
-  double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
-  double *qd = (double *)malloc(sizeof(double) * (size_t)vocab);
-  if (!p || !qd) {
+  int rc_all = SO_OK;
+#pragma omp parallel
+  {
+    double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)vocab);
+#pragma omp for schedule(dynamic, 1)
+    for (int b = 0; b < batch; ++b) {
+      int rc = (p && qd) ? rejection_one(b, vocab, cu_q, tgt, drf, dtype, draft_tok, u_acc, u_res, temperature,
+                                         max_q, accept_cnt, out_tok, num_out, margin, fallback, p, qd)
+                         : SO_ERR_NOMEM;
+      if (rc != SO_OK) {
+#pragma omp critical(so_rc)
+        rc_all = rc;
+      }
+    }
     free(p);
     free(qd);
-    return SO_ERR_NOMEM;
   }
-  int rc = SO_OK;
-  for (int b = 0; b < batch && rc == SO_OK; ++b) {
-    int n = cu_q[b + 1] - cu_q[b];
-    int K = n - 1;
-    if (n < 1 || n > max_q) {
-      rc = SO_ERR_ARG;
-      break;
-    }
-    size_t t0 = (size_t)cu_q[b];
-    size_t d0 = (size_t)cu_q[b] - (size_t)b;
-    for (int j = 0; j < max_q; ++j) out_tok[(size_t)b * max_q + j] = -1;
-    double marg = INFINITY;
-    int fb = 0;
-    int a = K, y = -1;
-    if (temperature == 0.0) {
-      for (int i = 0; i < K; ++i) {
-        int am;
-        if ((rc = argmax_row(tgt, dtype, t0 + i, vocab, &am)) != SO_OK) break;
-        int x = draft_tok[d0 + i];
-        if (x != am) {
-          a = i;
-          y = am;
-          break;
-        }
-      }
-      if (rc != SO_OK) break;
-      if (a == K && (rc = argmax_row(tgt, dtype, t0 + K, vocab, &y)) != SO_OK) break;
-    } else {
-      for (int i = 0; i < K; ++i) {
-        int x = draft_tok[d0 + i];
-        if (x < 0 || x >= vocab) {
-          rc = SO_ERR_TOKEN;
-          break;
-        }
-        if ((rc = softmax_row(tgt, dtype, t0 + i, vocab, temperature, p)) != SO_OK) break;
-        if ((rc = softmax_row(drf, dtype, d0 + i, vocab, temperature, qd)) != SO_OK) break;
-        double ratio = qd[x] > 0.0 ? p[x] / qd[x] : INFINITY;
-        double thr = ratio < 1.0 ? ratio : 1.0;
-        double u = (double)u_acc[d0 + i];
-        double dist = fabs(u - thr);
-        if (dist < marg) marg = dist;
-        if (!(u < thr)) {
-          a = i;
-          break;
-        }
-      }
-      if (rc != SO_OK) break;
-      double m2 = INFINITY;
-      double ur = (double)u_res[b];
-      if (a < K) {
-        /* p and qd still hold row a */
-        double S = 0.0;
-        for (int v = 0; v < vocab; ++v) {
-          double r = p[v] - qd[v];
-          qd[v] = r > 0.0 ? r : 0.0;
-          S += qd[v];
-        }
-        if (S > 0.0) {
-          y = inverse_cdf(qd, vocab, ur * S, S, &m2);
-        } else {
-          fb = 1;
-          y = inverse_cdf(p, vocab, ur, 1.0, &m2);
-        }
-      } else {
-        if ((rc = softmax_row(tgt, dtype, t0 + K, vocab, temperature, p)) != SO_OK) break;
-        y = inverse_cdf(p, vocab, ur, 1.0, &m2);
-      }
-      if (m2 < marg) marg = m2;
-    }
-    accept_cnt[b] = a;
-    for (int j = 0; j < a; ++j) out_tok[(size_t)b * max_q + j] = draft_tok[d0 + j];
-    out_tok[(size_t)b * max_q + a] = y;
-    num_out[b] = a + 1;
-    if (margin) margin[b] = marg;
-    if (fallback) fallback[b] = fb;
-  }
-  free(p);
-  free(qd);
-  return rc;
+  return rc_all;
 }
 
 /*

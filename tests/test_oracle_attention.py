@@ -176,3 +176,22 @@ def test_paged_attention_refuses_a_state_without_pools():
     okv = O.OracleKV(case.state, with_pools=False)
     with pytest.raises(ValueError):
         O.paged_attention(okv.as_state(), case.step)
+
+
+def test_threads_do_not_change_values():
+    """The oracle's OpenMP tasks compute every value in the single-thread order."""
+    import os
+    import oracle as O
+    from speculative_decoding_verify_paged_gb300 import workloads as W
+    case = W.tiny()
+    okv = O.OracleKV(case.state)
+    okv.append(case.step)
+    outs = []
+    for t in (1, max(2, os.cpu_count() or 2)):
+        O.set_threads(t)
+        a = O.paged_attention(okv.as_state(), case.step)
+        r = O.rejection_sample(case.step)
+        outs.append((a, r.accept_cnt, r.out_tok, r.margin))
+    O.set_threads(os.cpu_count() or 1)
+    for x, y in zip(*outs):
+        assert np.array_equal(x, y)
