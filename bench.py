@@ -483,7 +483,7 @@ def attn_path_times(kv, d, buf, msl, stream, reps=10):
     from speculative_decoding_verify_paged_gb300 import step as S
     out = {}
     S.append(kv, d, buf, stream)
-    for path in ("tensor_cores", "warp_mma", "cuda_cores"):
+    for path in ("keys_major", "tensor_cores", "warp_mma", "cuda_cores"):
         try:
             L.set_attn_path(path)
             for _ in range(2):

@@ -428,13 +428,17 @@ sv_status sv_adaptive_k_current(const void *state, int32_t *k);
  * complete implementations of the same operation, for measurement).
  *   SV_OPT_ATTN_PATH:
  *     SV_ATTN_AUTO (default): 5th-generation tensor cores (tcgen05, TMEM) for
- *       bf16 caches with head_dim 128 and blocks of 16..256 tokens, CUDA cores
- *       otherwise;
+ *       bf16 caches with head_dim 128 and blocks of 16..256 tokens (the
+ *       query-major kernel), CUDA cores for every other shape;
  *     SV_ATTN_CUDA_CORES: the CUDA-core kernel for every shape;
  *     SV_ATTN_TENSOR_CORES: tcgen05 (an unsupported shape then returns
  *       SV_ERR_UNSUPPORTED from sv_spec_verify_attn);
  *     SV_ATTN_WARP_MMA: warp-level mma.sync tensor-core kernel (same shapes as
- *       tcgen05).
+ *       tcgen05);
+ *     SV_ATTN_KEYS_MAJOR: the keys-major tcgen05 kernel (S^T = K Q^T with keys
+ *       on the MMA's M dimension; units of at most 32 query rows, i.e. query
+ *       heads per KV head x max_q_per_seq <= 32), else SV_ERR_UNSUPPORTED.
+ *       SV_ATTN_TENSOR_CORES is the query-major one.
  * Returns SV_ERR_INVALID_ARG for an unknown option or value. Not thread-safe
  * with respect to calls in flight on other host threads.
  */
@@ -443,7 +447,8 @@ typedef enum sv_attn_path {
   SV_ATTN_AUTO = 0,
   SV_ATTN_CUDA_CORES = 1,
   SV_ATTN_TENSOR_CORES = 2,
-  SV_ATTN_WARP_MMA = 3
+  SV_ATTN_WARP_MMA = 3,
+  SV_ATTN_KEYS_MAJOR = 4
 } sv_attn_path;
 sv_status sv_set_option(int32_t option, int32_t value);
 

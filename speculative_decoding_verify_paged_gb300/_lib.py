@@ -36,7 +36,7 @@ EXPORTS = ("sv_kv_append", "sv_spec_verify_attn_workspace_bytes", "sv_spec_verif
            "sv_adaptive_k_update", "sv_adaptive_k_reset", "sv_adaptive_k_current",
            "sv_status_string", "sv_version", "sv_set_option")
 SV_OPT_ATTN_PATH = 1
-ATTN_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "warp_mma": 3}
+ATTN_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "warp_mma": 3, "keys_major": 4}
 
 
 class SVError(RuntimeError):

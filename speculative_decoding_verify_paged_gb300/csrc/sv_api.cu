@@ -82,6 +82,12 @@ bool umma_usable(const sv_paged_kv *kv, int32_t num_q_heads, int32_t max_q, int3
          attn_umma_fits(make_kv(*kv), num_q_heads, max_q, max_seq_len);
 }
 
+// Whether the keys-major tcgen05 kernel can (units of at most 32 query rows).
+bool keys_usable(const sv_paged_kv *kv, int32_t num_q_heads, int32_t max_q, int32_t max_seq_len) {
+  return umma_usable(kv, num_q_heads, max_q, max_seq_len) &&
+         attn_keys_fits(make_kv(*kv), num_q_heads, max_q, max_seq_len);
+}
+
 // Workspace of whichever kernel a call may select: the split-KV partials of the
 // CUDA-core and mma.sync kernels, or the tcgen05 kernel's slots and tile prefix.
 size_t attn_workspace(const sv_paged_kv *kv, int32_t num_q_heads, int32_t total_q, int32_t max_q,
@@ -94,6 +100,8 @@ size_t attn_workspace(const sv_paged_kv *kv, int32_t num_q_heads, int32_t total_
   }
   if (kv->batch > 0 && umma_usable(kv, num_q_heads, max_q, max_seq_len))
     need = std::max(need, attn_umma_workspace_bytes(make_kv(*kv), num_q_heads, max_q, max_seq_len));
+  if (kv->batch > 0 && keys_usable(kv, num_q_heads, max_q, max_seq_len))
+    need = std::max(need, attn_keys_workspace_bytes(make_kv(*kv), num_q_heads, max_q, max_seq_len));
   return need;
 }
 
@@ -130,7 +138,7 @@ const char *sv_status_string(int32_t status) {
 int32_t sv_version(void) { return 30000; }
 
 sv_status sv_set_option(int32_t option, int32_t value) {
-  if (option == SV_OPT_ATTN_PATH && value >= SV_ATTN_AUTO && value <= SV_ATTN_WARP_MMA) {
+  if (option == SV_OPT_ATTN_PATH && value >= SV_ATTN_AUTO && value <= SV_ATTN_KEYS_MAJOR) {
     g_attn_path = value;
     return SV_OK;
   }
@@ -198,6 +206,7 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = (cudaStream_t)stream;
   const bool umma_ok = umma_usable(kv, num_q_heads, max_q_per_seq, max_seq_len);
+  const bool keys_ok = keys_usable(kv, num_q_heads, max_q_per_seq, max_seq_len);
   const bool mma_ok = kv->dtype == SV_DTYPE_BF16 && attn_tc_supported(a.kv, num_q_heads, max_q_per_seq);
   cudaError_t e;
   switch (g_attn_path) {
@@ -209,6 +218,9 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
       if (!mma_ok) return SV_ERR_UNSUPPORTED;
       e = launch_attn_tc(a, st);
       break;
+    case SV_ATTN_KEYS_MAJOR:
+      if (!keys_ok) return SV_ERR_UNSUPPORTED;
+      return cuda_status(launch_attn_keys(a, workspace, workspace_bytes, st));
     default:
       if (umma_ok) return cuda_status(launch_attn_umma(a, workspace, workspace_bytes, st));
       e = launch_attn_simt(a, kv->dtype, st);

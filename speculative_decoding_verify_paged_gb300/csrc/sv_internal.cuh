@@ -168,6 +168,10 @@ bool attn_umma_fits(const KV &kv, int num_q_heads, int max_q, int max_seq_len);
 size_t attn_umma_workspace_bytes(const KV &kv, int num_q_heads, int max_q, int max_seq_len);
 // launches the persistent tcgen05 kernel and its combine (workspace: attn_umma_workspace_bytes, 256-aligned)
 cudaError_t launch_attn_umma(const AttnArgs &a, void *workspace, size_t workspace_bytes, cudaStream_t st);
+// The keys-major tcgen05 kernel (attn_keys.cu): units of at most 32 query rows.
+bool attn_keys_fits(const KV &kv, int num_q_heads, int max_q, int max_seq_len);
+size_t attn_keys_workspace_bytes(const KV &kv, int num_q_heads, int max_q, int max_seq_len);
+cudaError_t launch_attn_keys(const AttnArgs &a, void *workspace, size_t workspace_bytes, cudaStream_t st);
 
 struct SamplerArgs {
   const void *tgt;

@@ -65,15 +65,31 @@ SMALL = {
 }
 
 
-@pytest.mark.parametrize("path", ["auto", "cuda_cores", "warp_mma"])
+@pytest.mark.parametrize("path", ["auto", "cuda_cores", "warp_mma", "tensor_cores", "keys_major"])
 @pytest.mark.parametrize("name", list(SMALL))
 def test_small_cases(name, path):
     seed, ctx, nq, hq, hkv, d, bs, dt = SMALL[name]
     case = W.custom(seed, batch=len(ctx), ctx_lens=ctx, n_q=nq, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                     block_size=bs, vocab=16, dtype=dt, use_bank=False)
-    if path == "warp_mma" and (dt != "bf16" or d != 128):
-        pytest.skip("the mma.sync kernel covers bf16 with head_dim 128")
+    if path in ("warp_mma", "tensor_cores", "keys_major") and (dt != "bf16" or d != 128):
+        pytest.skip("the tensor-core kernels cover bf16 with head_dim 128")
+    if path == "keys_major" and (hq // hkv) * max(nq) > 32:
+        pytest.skip("the keys-major kernel covers units of at most 32 query rows")
     _run(case, path=path)
+
+
+def test_keys_major_refuses_wide_units():
+    """More than 32 query rows in a unit: the keys-major path is unsupported."""
+    case = W.custom(27, batch=2, ctx_lens=[300, 40], n_q=[5, 5], num_q_heads=64, num_kv_heads=8, head_dim=128,
+                    block_size=16, vocab=16, use_bank=False)
+    kv, d, buf = upload(case)
+    L.set_attn_path("keys_major")
+    try:
+        with pytest.raises(L.SVError) as e:
+            S.attention(kv, d, buf, max_seq_len(case.state, case.step))
+        assert e.value.code == 2
+    finally:
+        L.set_attn_path("auto")
 
 
 def test_tensor_core_path_refuses_unsupported_shapes():
@@ -120,6 +136,7 @@ def test_tree_small(path):
 
 
 @pytest.mark.parametrize("name,seqs,path", [("llama8b", [0, 5, 17, 31], "auto"),
+                                            ("llama8b", [2, 9, 26], "keys_major"),
                                             ("llama8b", [3, 30], "cuda_cores"),
                                             ("llama8b", [1, 20], "warp_mma"),
                                             ("llama70b", [0, 63, 127], "auto")])
