@@ -112,6 +112,14 @@ def paged_attention(state, step, *, seqs=None, out: np.ndarray | None = None) ->
     `seqs` are zero / untouched)."""
     if state.k_pool is None or state.v_pool is None:
         raise ValueError("paged_attention needs a state with K/V pools (OracleKV(..., with_pools=True))")
+    if state.dtype == "e4m3":  # fp8 pool: every code read as its E4M3 value times the pool's scale
+        from copy import copy
+        from . import fp8
+        st = copy(state)
+        st.k_pool = (fp8.decode(state.k_pool) * float(np.float32(state.k_scale))).astype(np.float32)
+        st.v_pool = (fp8.decode(state.v_pool) * float(np.float32(state.v_scale))).astype(np.float32)
+        st.dtype = "f32"
+        state = st
     Tq = step.total_q
     hq = step.num_q_heads
     d = state.head_dim
@@ -120,12 +128,13 @@ def paged_attention(state, step, *, seqs=None, out: np.ndarray | None = None) ->
     sl = None if seqs is None else np.ascontiguousarray(seqs, np.int32)
     kp, vp = _c(state.k_pool), _c(state.v_pool)
     q = _c(step.q)
+    q_dtype = "bf16" if q.dtype == np.uint16 else "f32"  # bf16 arrays hold bit patterns; an fp8 pool takes bf16 Q
     tm = _c(step.tree_mask, np.uint64) if step.tree_mask is not None else None
     rc = _load().so_paged_attention(
         state.batch, hq, state.num_kv_heads, d, state.block_size, state.max_blocks_per_seq,
         state.num_blocks, _p(_c(state.seq_lens, np.int32)), _p(_c(step.cu_q, np.int32)),
         _p(_c(state.block_table, np.int32)), _p(kp), _p(vp), _DT[state.dtype], _p(q),
-        _DT[state.dtype], 0 if step.mask_kind == "causal" else 1, _p(tm), float(step.scale),
+        _DT[q_dtype], 0 if step.mask_kind == "causal" else 1, _p(tm), float(step.scale),
         _p(sl), 0 if sl is None else int(sl.shape[0]), _p(out))
     _check(rc, "paged_attention")
     return out
@@ -335,13 +344,20 @@ class OracleKV:
                 if self.ref is not None:
                     self.ref[self.bt[b][first + j]] = 1
         if self.k_pool is not None:
+            new_k, new_v = step.new_k, step.new_v
+            if self._state.dtype == "e4m3":
+                # fp8 pool: the E4M3 code nearest to x / scale, x the bf16 input (fp32 division)
+                from . import fp8
+                wid = lambda a: (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32)
+                new_k = fp8.encode(wid(new_k) / np.float32(self._state.k_scale))
+                new_v = fp8.encode(wid(new_v) / np.float32(self._state.v_scale))
             for b in range(B):
                 for j in range(n[b]):
                     pos = self.seq_lens[b] + j
                     blk = self.bt[b][pos // self.bs]
                     row = int(step.cu_q[b]) + j
-                    self.k_pool[blk, :, pos % self.bs, :] = step.new_k[row]
-                    self.v_pool[blk, :, pos % self.bs, :] = step.new_v[row]
+                    self.k_pool[blk, :, pos % self.bs, :] = new_k[row]
+                    self.v_pool[blk, :, pos % self.bs, :] = new_v[row]
         return None
 
     def rollback(self, step, accept_cnt, path_nodes=None):

@@ -46,7 +46,7 @@ class KVState:
     max_blocks_per_seq: int
     num_kv_heads: int
     head_dim: int
-    dtype: str  # "bf16" (uint16 bit patterns) or "f32"
+    dtype: str  # "bf16" (uint16 bit patterns), "f32", or "e4m3" (uint8 codes of an fp8 pool)
     k_pool: np.ndarray  # [num_blocks, Hkv, block_size, D]
     v_pool: np.ndarray
     block_table: np.ndarray  # int32 [B, max_blocks_per_seq], -1 = no block
@@ -54,6 +54,8 @@ class KVState:
     free_list: np.ndarray  # int32 [num_blocks]; entries [0, free_top) are free ids
     free_top: int
     held_blocks: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int32))
+    k_scale: float = 1.0  # e4m3 pools: a code's value times the scale
+    v_scale: float = 1.0
 
     @property
     def batch(self) -> int:
@@ -65,7 +67,7 @@ class KVState:
             self.num_kv_heads, self.head_dim, self.dtype,
             self.k_pool.copy(), self.v_pool.copy(), self.block_table.copy(),
             self.seq_lens.copy(), self.free_list.copy(), self.free_top,
-            self.held_blocks.copy())
+            self.held_blocks.copy(), self.k_scale, self.v_scale)
 
 
 @dataclass
@@ -233,8 +235,19 @@ def make_kv_state(seed: int, ctx_lens: np.ndarray, *, block_size: int, num_kv_he
 
     slab = block_size * head_dim
     shape = (num_blocks, num_kv_heads, block_size, head_dim)
-    bank = _Bank(seed)
     pools = []
+    if dtype == "e4m3":
+        # fp8 pools: random codes with exponent fields 3..9 and either sign (magnitudes
+        # 1/16 .. 7.5), read with scale 1/8; no quantisation happens here
+        for which in range(2):
+            r = _rng(seed, 2, which)
+            codes = (r.integers(0, 2, size=shape) << 7) | (r.integers(3, 10, size=shape) << 3) | \
+                r.integers(0, 8, size=shape)
+            pools.append(codes.astype(np.uint8))
+        return KVState(block_size, num_blocks, max_blocks_per_seq, num_kv_heads, head_dim, dtype,
+                       pools[0], pools[1], bt, ctx_lens.copy(), free_list, int(free.shape[0]),
+                       held.astype(np.int32), 0.125, 0.125)
+    bank = _Bank(seed)
     for which in range(2):
         w = bank.windows(_rng(seed, 2, which), num_blocks * num_kv_heads, slab)
         pools.append(_cast(w.reshape(shape), dtype))
@@ -314,14 +327,14 @@ def tiny(seed: int = 0, temperature: float = 1.0) -> Case:
 
 def llama8b(seed: int = 1, temperature: float = 1.0, *, batch: int = 32, ctx_range=(512, 4096),
             K: int = 5, vocab: int = 128256, block_size: int = 16, growth_tokens: int = 0,
-            pool_factor: float = 1.25) -> Case:
+            pool_factor: float = 1.25, kv_dtype: str = "bf16") -> Case:
     """Llama-3-8B-shaped: 32 q / 8 kv heads of dim 128, bf16 KV in 16-token blocks
     of a shuffled pool, contexts U[512, 4096], K = 5 causal, vocab 128256, bf16
     target logits N(0, 3^2), draft = 0.8 target + N(0, 1.5^2)."""
     rng = _rng(seed, 20)
     ctx = rng.integers(ctx_range[0], ctx_range[1] + 1, size=batch).astype(np.int32)
     n_q = np.full(batch, K + 1, np.int32)
-    state = make_kv_state(seed, ctx, block_size=block_size, num_kv_heads=8, head_dim=128, dtype="bf16",
+    state = make_kv_state(seed, ctx, block_size=block_size, num_kv_heads=8, head_dim=128, dtype=kv_dtype,
                           growth_tokens=K + 1 + growth_tokens, pool_factor=pool_factor)
     step = make_chain_step(seed, n_q, num_q_heads=32, num_kv_heads=8, head_dim=128, qkv_dtype="bf16",
                            vocab=vocab, logits_dtype="bf16", target_sigma=3.0, draft_coef=0.8,
@@ -492,8 +505,9 @@ def custom(seed: int, *, batch: int, ctx_lens, n_q, num_q_heads: int, num_kv_hea
                           head_dim=head_dim, dtype=dtype, pool_factor=pool_factor,
                           held_fraction=held_fraction,
                           growth_tokens=int(n_q.max() if batch else 1) + growth_tokens)
+    io = "bf16" if dtype == "e4m3" else dtype  # an fp8 pool takes bf16 rows and queries
     step = make_chain_step(seed, n_q, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
-                           qkv_dtype=dtype, vocab=vocab, logits_dtype=dtype, target_sigma=target_sigma,
+                           qkv_dtype=io, vocab=vocab, logits_dtype=io, target_sigma=target_sigma,
                            draft_coef=draft_coef, draft_sigma=draft_sigma, temperature=temperature,
                            use_bank=use_bank)
     return Case("custom", seed, state, step)
