@@ -74,11 +74,14 @@ typedef enum sv_status {
   SV_ERR_BAD_BLOCK_ID = 6,  /* device: a block id outside [0, num_blocks) */
   SV_ERR_BAD_LENGTH = 7,    /* device: a length, accept count or path entry out of range */
   SV_ERR_BAD_TOKEN = 8,     /* device: a token id outside [0, vocab) */
-  SV_ERR_NONFINITE = 9,     /* device: a NaN or +inf logit, or a row without finite logits */
+  SV_ERR_NONFINITE = 9,     /* device: a NaN or +inf logit, a row without finite logits, or a
+                               query beyond fp16 range on the E4M3 tensor-core path */
   SV_ERR_WORKSPACE = 10     /* host: workspace missing or smaller than required */
 } sv_status;
 
-typedef enum sv_dtype { SV_DTYPE_BF16 = 0, SV_DTYPE_F32 = 1 } sv_dtype;
+/* SV_DTYPE_E4M3 (8-bit floating point: sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, no infinity, largest finite 448) is a KV-pool type only. */
+typedef enum sv_dtype { SV_DTYPE_BF16 = 0, SV_DTYPE_F32 = 1, SV_DTYPE_E4M3 = 2 } sv_dtype;
 
 typedef enum sv_mask_kind { SV_MASK_CAUSAL = 0, SV_MASK_TREE = 1 } sv_mask_kind;
 
@@ -103,8 +106,25 @@ typedef enum sv_mask_kind { SV_MASK_CAUSAL = 0, SV_MASK_TREE = 1 } sv_mask_kind;
  *                    free block). The caller sets it up to match the tables
  *                    (1 per held block when nothing is shared yet); the calls
  *                    below keep it so.
+ *   k_scale, v_scale dequantisation scales of an SV_DTYPE_E4M3 pool (the value
+ *                    of a stored code is its E4M3 value times the scale);
+ *                    finite and > 0; ignored for the other types.
  * block_size: a power of two in [1, 256]; head_dim: a multiple of 8 in
- * [8, 256]; dtype: SV_DTYPE_BF16 or SV_DTYPE_F32.
+ * [8, 256] (of 16 for E4M3); dtype: SV_DTYPE_BF16, SV_DTYPE_F32 or
+ * SV_DTYPE_E4M3.
+ *
+ * fp8 pools (SV_DTYPE_E4M3; the pages mention KV-cache quantisation without a
+ * format, "LLM serving: speculative decoding and PagedAttention memory
+ * management", TensorRT-LLM section; the reading taken: E4M3 codes with one
+ * scale per pool): the new rows given to sv_kv_append and the queries and
+ * outputs of sv_spec_verify_attn are bf16. Append stores each new element x as
+ * the E4M3 code nearest to x / scale (fp32 division; ties to the even
+ * mantissa; saturating at +-448), so it never writes the NaN codes 0x7F and
+ * 0xFF; a pool must not hold them. Attention reads code * scale: the CUDA-core
+ * kernel in fp32; the tcgen05 kernel (head_dim 128) widens the codes to fp16
+ * exactly, rounds the queries and the softmax weights to fp16 and applies the
+ * scales to the scores and the outputs in fp32, so a query element beyond the
+ * fp16 range (|q| > 65504) records SV_ERR_NONFINITE there.
  */
 typedef struct sv_paged_kv {
   void *k_pool;
@@ -121,6 +141,8 @@ typedef struct sv_paged_kv {
   int32_t batch;
   int32_t dtype;
   int32_t *ref_count;
+  float k_scale;
+  float v_scale;
 } sv_paged_kv;
 
 /*
@@ -141,7 +163,7 @@ typedef struct sv_paged_kv {
  * So of w writers into a block held by r, the first min(w, r - 1) copy and a
  * last writer that holds the only remaining reference writes in place. New
  * blocks get count 1.
- *   new_k, new_v  [total_q, num_kv_heads, head_dim] of kv->dtype
+ *   new_k, new_v  [total_q, num_kv_heads, head_dim] of kv->dtype (bf16 for an E4M3 pool)
  *   cu_q          int32 [batch + 1], cu_q[0] = 0, cu_q[batch] = total_q
  *   status_dev    int32 [1], required
  * All or nothing: if the blocks would not fit the block table
@@ -428,17 +450,17 @@ sv_status sv_adaptive_k_current(const void *state, int32_t *k);
  * complete implementations of the same operation, for measurement).
  *   SV_OPT_ATTN_PATH:
  *     SV_ATTN_AUTO (default): 5th-generation tensor cores (tcgen05, TMEM) for
- *       bf16 caches with head_dim 128 and blocks of 16..256 tokens (the
- *       query-major kernel), CUDA cores for every other shape;
+ *       bf16 and E4M3 caches with head_dim 128 and blocks of 16..256 tokens
+ *       (the query-major kernel), CUDA cores for every other shape;
  *     SV_ATTN_CUDA_CORES: the CUDA-core kernel for every shape;
  *     SV_ATTN_TENSOR_CORES: tcgen05 (an unsupported shape then returns
  *       SV_ERR_UNSUPPORTED from sv_spec_verify_attn);
- *     SV_ATTN_WARP_MMA: warp-level mma.sync tensor-core kernel (same shapes as
- *       tcgen05);
+ *     SV_ATTN_WARP_MMA: warp-level mma.sync tensor-core kernel (the bf16
+ *       shapes of tcgen05);
  *     SV_ATTN_KEYS_MAJOR: the keys-major tcgen05 kernel (S^T = K Q^T with keys
  *       on the MMA's M dimension; units of at most 32 query rows, i.e. query
- *       heads per KV head x max_q_per_seq <= 32), else SV_ERR_UNSUPPORTED.
- *       SV_ATTN_TENSOR_CORES is the query-major one.
+ *       heads per KV head x max_q_per_seq <= 32; bf16 caches), else
+ *       SV_ERR_UNSUPPORTED. SV_ATTN_TENSOR_CORES is the query-major one.
  * Returns SV_ERR_INVALID_ARG for an unknown option or value. Not thread-safe
  * with respect to calls in flight on other host threads.
  */

@@ -21,8 +21,9 @@ LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
 SV_OK = 0
 SV_ERR_INVALID_ARG = 1
+SV_ERR_NONFINITE = 9
 SV_ERR_WORKSPACE = 10
-SV_DTYPE_BF16, SV_DTYPE_F32 = 0, 1
+SV_DTYPE_BF16, SV_DTYPE_F32, SV_DTYPE_E4M3 = 0, 1, 2
 SV_MASK_CAUSAL, SV_MASK_TREE = 0, 1
 STATUS_NAMES = {
     0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_CUDA",
@@ -61,7 +62,7 @@ class sv_paged_kv(ctypes.Structure):
         ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("max_blocks_per_seq", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("batch", ctypes.c_int32), ("dtype", ctypes.c_int32),
-        ("ref_count", ctypes.c_void_p),
+        ("ref_count", ctypes.c_void_p), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
     ]
 
 
@@ -167,13 +168,16 @@ class PagedKV:
     free_list: torch.Tensor  # int32 [num_blocks]
     free_top: torch.Tensor  # int32 [1]
     ref_count: Optional[torch.Tensor] = None  # int32 [num_blocks]: copy-on-write sharing when given
+    k_scale: float = 1.0  # E4M3 pools (uint8 codes): dequantisation scales
+    v_scale: float = 1.0
 
     def struct(self) -> sv_paged_kv:
         nb, hkv, bs, d = self.k_pool.shape
         return sv_paged_kv(
             _ptr(self.k_pool), _ptr(self.v_pool), _ptr(self.block_table), _ptr(self.seq_lens),
             _ptr(self.free_list), _ptr(self.free_top), nb, bs, self.block_table.shape[1], hkv, d,
-            self.seq_lens.shape[0], _dtype_code(self.k_pool), _ptr(self.ref_count))
+            self.seq_lens.shape[0], SV_DTYPE_E4M3 if self.k_pool.dtype == torch.uint8 else _dtype_code(self.k_pool),
+            _ptr(self.ref_count), float(self.k_scale), float(self.v_scale))
 
     @property
     def batch(self) -> int:

@@ -19,6 +19,8 @@
 // A sequence whose keys span several splits writes per-split partial results
 // (O normalised by its own l, plus log2-sum-exp m + log2 l); the combine kernel
 // merges them: o = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M).
+#include <cuda_fp8.h>
+
 #include "sv_internal.cuh"
 
 namespace sv {
@@ -46,7 +48,15 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-template <typename T, int NK /* head_dim / 32 */>
+// A pool element as fp32: bf16 or fp32 as is, an E4M3 code (uint8_t) times the pool's scale.
+__device__ __forceinline__ float kv_f32(__nv_bfloat16 x, float) { return __bfloat162float(x); }
+__device__ __forceinline__ float kv_f32(float x, float) { return x; }
+__device__ __forceinline__ float kv_f32(uint8_t x, float scale) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(x, __NV_E4M3);
+  return __half2float(__half(h)) * scale;
+}
+
+template <typename T, typename KT /* pool element */, int NK /* head_dim / 32 */>
 __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a) {
   grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   grid_dependents_launch();
@@ -73,8 +83,8 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a) {
   const int G = a.num_q_heads / kv.num_kv_heads;
   const int R = G * n;
   const T *qp = reinterpret_cast<const T *>(a.q);
-  const T *kp = reinterpret_cast<const T *>(kv.k_pool);
-  const T *vp = reinterpret_cast<const T *>(kv.v_pool);
+  const KT *kp = reinterpret_cast<const KT *>(kv.k_pool);
+  const KT *vp = reinterpret_cast<const KT *>(kv.v_pool);
   if (tid == 0) s_bad = 0;
 
   for (int rg = 0; rg < R; rg += kRowsPerPass) {
@@ -105,8 +115,8 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a) {
           const int blk = kv.block_table[(size_t)b * kv.max_blocks + t / kv.block_size];
           if (blk >= 0 && blk < kv.num_blocks) {
             const size_t off = (((size_t)blk * kv.num_kv_heads + kvh) * kv.block_size + t % kv.block_size) * D + d;
-            kk = to_f32(kp[off]);
-            vv = to_f32(vp[off]);
+            kk = kv_f32(kp[off], kv.k_scale);
+            vv = kv_f32(vp[off], kv.v_scale);
           } else {
             s_bad = 1;
           }
@@ -209,23 +219,23 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
   }
 }
 
-template <typename T, int NK>
+template <typename T, typename KT, int NK>
 cudaError_t launch_nk(const AttnArgs &a, cudaStream_t st) {
   dim3 grid(a.max_splits, a.kv.num_kv_heads, a.kv.batch);
-  return launch_pdl(attn_simt_kernel<T, NK>, grid, dim3(kThreads), 0, st, a);
+  return launch_pdl(attn_simt_kernel<T, KT, NK>, grid, dim3(kThreads), 0, st, a);
 }
 
-template <typename T>
+template <typename T, typename KT>
 cudaError_t launch_t(const AttnArgs &a, cudaStream_t st) {
   switch (a.kv.head_dim / 32) {
-    case 1: return launch_nk<T, 1>(a, st);
-    case 2: return launch_nk<T, 2>(a, st);
-    case 3: return launch_nk<T, 3>(a, st);
-    case 4: return launch_nk<T, 4>(a, st);
-    case 5: return launch_nk<T, 5>(a, st);
-    case 6: return launch_nk<T, 6>(a, st);
-    case 7: return launch_nk<T, 7>(a, st);
-    default: return launch_nk<T, 8>(a, st);
+    case 1: return launch_nk<T, KT, 1>(a, st);
+    case 2: return launch_nk<T, KT, 2>(a, st);
+    case 3: return launch_nk<T, KT, 3>(a, st);
+    case 4: return launch_nk<T, KT, 4>(a, st);
+    case 5: return launch_nk<T, KT, 5>(a, st);
+    case 6: return launch_nk<T, KT, 6>(a, st);
+    case 7: return launch_nk<T, KT, 7>(a, st);
+    default: return launch_nk<T, KT, 8>(a, st);
   }
 }
 
@@ -233,14 +243,16 @@ cudaError_t launch_t(const AttnArgs &a, cudaStream_t st) {
 
 cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t st) {
   if (a.kv.batch == 0) return cudaSuccess;
-  return dtype == SV_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, st) : launch_t<float>(a, st);
+  if (dtype == SV_DTYPE_E4M3) return launch_t<__nv_bfloat16, uint8_t>(a, st);  // bf16 queries and outputs
+  return dtype == SV_DTYPE_BF16 ? launch_t<__nv_bfloat16, __nv_bfloat16>(a, st) : launch_t<float, float>(a, st);
 }
 
 cudaError_t launch_attn_combine(const AttnArgs &a, int dtype, cudaStream_t st) {
   if (a.max_splits <= 1 || a.total_q == 0) return cudaSuccess;
   const long long warps = (long long)a.total_q * a.num_q_heads;
   const unsigned blocks = (unsigned)((warps + 3) / 4);
-  if (dtype == SV_DTYPE_BF16) return launch_pdl(attn_combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(128), 0, st, a);
+  if (dtype == SV_DTYPE_BF16 || dtype == SV_DTYPE_E4M3)
+    return launch_pdl(attn_combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(128), 0, st, a);
   return launch_pdl(attn_combine_kernel<float>, dim3(blocks), dim3(128), 0, st, a);
 }
 

@@ -1,5 +1,5 @@
 // Persistent split-KV paged attention on the 5th-generation tensor cores
-// (tcgen05 + TMEM) for bf16 caches with head_dim 128.
+// (tcgen05 + TMEM) for bf16 and E4M3 caches with head_dim 128.
 //
 // What it computes is the attention of the verify pass ("Speculative decoding
 // and continuous batching in practice", sec. 1.2: the target scores all K+1
@@ -45,8 +45,16 @@
 //    rescaled in TMEM), write P = 2^(s - m) as bf16 over S (tcgen05.st), and
 //    at the end of a piece read O, divide by the row sum and store the rows or
 //    the partial result.
+// An E4M3 cache (the kernel's F8 form) adds two warps: the producer's boxes
+// bring rows of 128 one-byte codes into a ring of code stages, and the two
+// converter warps widen each stage to fp16 (exactly, as the code's value times
+// 2^-8) in the layout above, in a ring of operand stages that the MMA reads;
+// Q and P are fp16, 2^8 k_scale joins the score scale and 2^8 v_scale the
+// output's normalisation.
 // All mbarrier waits are bounded; a wait that gives up records SV_ERR_TIMEOUT.
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 
@@ -68,6 +76,13 @@ constexpr int kColO = 64;
 constexpr int kColQ = 192;
 constexpr float kRescaleThreshold = 8.f;        // log2 units
 constexpr int kCtasPerSm = 2;                   // TMEM: 2 x 256 columns; shared memory: 2 x ~100 KB
+// E4M3 pools: a ring of code stages (K | V codes, 4 KB each) that the TMA fills, two converter
+// warps that widen each stage to fp16 in the operand layout above, and a ring of operand stages
+constexpr int kCodeStages = 6;
+constexpr int kCodeHalf = kTile * 128;          // 32 keys x 128 one-byte codes
+constexpr int kCodeStageBytes = 2 * kCodeHalf;  // K and V codes
+constexpr int kConvStages = 3;
+constexpr int kConvWarps = 2;                   // warps 6-7, after the softmax warps
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -82,6 +97,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
+// One box of an E4M3 pool's (128 codes, rows) view: R rows starting at row y, 128 B each.
+__device__ __forceinline__ void tma_load_codes(uint32_t dst, const CUtensorMap *map, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(bar)
+      : "memory");
+}
 // One box of the (64 elements, 8 rows, 2 halves, row groups) view: R rows
 // starting at row y (a multiple of 8), both halves, as R/8 groups of
 // [half 0: 8 rows x 128 B][half 1: 8 rows x 128 B].
@@ -107,11 +130,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   d |= (uint64_t)2 << 61;
   return d;
 }
-// Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B, A K-major,
-// B K-major or MN-major, N / 8 and M / 16.
-__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 accumulate, bf16 (or fp16) A and B,
+// A K-major, B K-major or MN-major, N / 8 and M / 16.
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int b_mn_major, bool f16 = false) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | ((uint32_t)b_mn_major << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, int accum) {
   asm volatile(
@@ -171,6 +194,28 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+// Two E4M3 codes of a word (bytes sel0 and sel1 of w) as an fp16 pair holding their
+// values times 2^-8, exactly. Both formats put the sign on top and the exponent next,
+// with biases 7 and 15 and subnormals at the lowest exponent field, so code bits
+// s.eeee.mmm placed as fp16 bits s.0eeee.mmm0000000 read as the code's value times
+// 2^(7-15), subnormals and zero included (the NaN codes are never stored: the append
+// saturates). The byte goes to bits 8-15 of its half (prmt), the magnitude one bit down.
+template <int SEL>
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w) {
+  const uint32_t y = __byte_perm(w, 0u, SEL);
+  return (y & 0x80008000u) | ((y >> 1) & 0x3f803f80u);
+}
+constexpr float kF16CodeScale = 256.f;  // 2^8: what the fp16 operands above lack
+// A bf16 pair as an fp16 pair (round to nearest); *over is set when a value leaves the fp16 range.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, bool *over) {
+  const uint32_t h = pack_f16(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+  if ((h & 0x7c00u) == 0x7c00u || (h & 0x7c000000u) == 0x7c000000u) *over = true;  // inf or NaN
+  return h;
+}
 struct UmmaParams {
   AttnArgs a;
   int box_rows;     // rows per TMA box (a group): min(block_size, 32), 16 or 32
@@ -212,6 +257,7 @@ __device__ __forceinline__ int seq_work(const UmmaParams &P, const Seq &s) {
 }
 
 // Inclusive sum over the CTA's threads; *total gets the sum over all of them.
+template <int NT>
 __device__ __forceinline__ int block_scan(int v, int *sh, int *total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -224,7 +270,7 @@ __device__ __forceinline__ int block_scan(int v, int *sh, int *total) {
   __syncthreads();
   int before = 0, all = 0;
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) {
+  for (int w = 0; w < NT / 32; ++w) {
     const int t = sh[w];
     before += w < warp ? t : 0;
     all += t;
@@ -277,11 +323,20 @@ struct Walker {
   }
 };
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                                                                         const __grid_constant__ CUtensorMap tmap_v,
-                                                                         const UmmaParams P) {
+// F8: the pool holds E4M3 codes; the operands are fp16 (codes widened exactly, times 2^-8, by
+// the converter warps; Q and P rounded to fp16); the scores carry 2^8 k_scale and the output
+// 2^8 v_scale.
+template <bool F8>
+__global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kCtasPerSm)
+    attn_umma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                     const UmmaParams P) {
   grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   grid_dependents_launch();
+  constexpr int kNT = F8 ? kThreads + kConvWarps * 32 : kThreads;
+  constexpr int kLS = F8 ? kCodeStages : kStages;  // stages of the ring the TMA fills
+  constexpr int kLoadStageBytes = F8 ? kCodeStageBytes : kStageBytes;
+  constexpr int kMS = F8 ? kConvStages : kStages;  // stages of the ring the MMA reads
+  constexpr int kSoft0 = 2;                        // first softmax warp
   const AttnArgs &a = P.a;
   const KV &kv = a.kv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -289,23 +344,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *stages = base;  // kStages x (K 8 KB | V 8 KB)
-  uint64_t *full = reinterpret_cast<uint64_t *>(stages + kStages * kStageBytes);
-  uint64_t *empty = full + kStages;
-  uint64_t *s_full = empty + kStages;  // [2] S(t) in TMEM buffer t % 2
+  uint8_t *stages = base;  // kLS x (K | V): 16 KB of bf16 operands, or 8 KB of E4M3 codes
+  uint8_t *mstages = F8 ? base + kLS * kLoadStageBytes : base;  // kMS x 16 KB operand stages
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + kLS * kLoadStageBytes + (F8 ? kMS * kStageBytes : 0));
+  uint64_t *empty = full + kLS;
+  uint64_t *s_full = empty + kLS;      // [2] S(t) in TMEM buffer t % 2
   uint64_t *p_ready = s_full + 2;      // [2] P(t) written over buffer t % 2
   uint64_t *o_bar = p_ready + 2;       // one phase per finished P V
   uint64_t *q_ready = o_bar + 1;       // one phase per unit whose Q rows are in TMEM
   uint64_t *mma_done = q_ready + 1;    // every MMA issued has finished
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
-  __shared__ int sh_scan[kThreads / 32];
+  uint64_t *cfull = mma_done + 1;      // [kConvStages] F8: operand stage converted
+  uint64_t *cempty = cfull + kConvStages;  // [kConvStages] F8: operand stage read by its last MMA
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cempty + kConvStages);
+  uint64_t *mfull = F8 ? cfull : full;    // the MMA waits on these ...
+  uint64_t *mempty = F8 ? cempty : empty;  // ... and frees its stages through these
+  __shared__ int sh_scan[kNT / 32];
   __shared__ int sh_first_b, sh_first_base, sh_err;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kLS; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), F8 ? kConvWarps : 1);
     }
+    if (F8)
+      for (int s = 0; s < kConvStages; ++s) {
+        mbar_init(smem_u32(&cfull[s]), kConvWarps);
+        mbar_init(smem_u32(&cempty[s]), 1);
+      }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&s_full[s]), 1);
       mbar_init(smem_u32(&p_ready[s]), kSoftWarps);
@@ -327,18 +392,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
 
   // ---- this CTA's tile range [g0, g1) of the W tiles of the launch ----
   int mine = 0;
-  for (int b = tid; b < B; b += kThreads) {
+  for (int b = tid; b < B; b += kNT) {
     bool bad;
     const Seq s = load_seq(P, b, &bad);
     if (bad && blockIdx.x == 0) record(a.status, SV_ERR_BAD_LENGTH);
     mine += seq_work(P, s);
   }
   int W;
-  block_scan(mine, sh_scan, &W);
+  block_scan<kNT>(mine, sh_scan, &W);
   const int per = max(1, (W + P.ctas - 1) / P.ctas);
   const int g0 = min(W, (int)blockIdx.x * per), g1 = min(W, g0 + per);
   int run = 0;
-  for (int b0 = 0; b0 < B; b0 += kThreads) {  // the sequence holding tile g0; CTA 0 also stores the prefix
+  for (int b0 = 0; b0 < B; b0 += kNT) {  // the sequence holding tile g0; CTA 0 also stores the prefix
     const int b = b0 + tid;
     int v = 0;
     if (b < B) {
@@ -346,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
       v = seq_work(P, load_seq(P, b, &bad));
     }
     int tot;
-    const int excl = run + block_scan(v, sh_scan, &tot) - v;
+    const int excl = run + block_scan<kNT>(v, sh_scan, &tot) - v;
     if (blockIdx.x == 0 && b < B) P.prefix[b] = excl;
     if (v > 0 && excl <= g0 && g0 < excl + v) {
       sh_first_b = b;
@@ -377,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
     // block_size is a power of two: logical blocks and row offsets by shift and mask
     const int bs = kv.block_size, box = P.box_rows;
     const int bs_shift = __ffs(bs) - 1;
-    const uint32_t box_bytes = static_cast<uint32_t>(box) * 256;
+    const uint32_t row_bytes = F8 ? 128u : 256u;  // one key's row of K (or V) as the TMA brings it
+    const uint32_t box_bytes = static_cast<uint32_t>(box) * row_bytes;
     Piece p;
     while (ok && walker.next(P, p)) {
       const int kb = p.kt0 * kTile, ke = min(p.L, p.kt1 * kTile);
@@ -397,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
       int cur = load_y(wbase + lane);
       int nxt = load_y(wbase + 32 + lane);
       for (int kt = p.kt0; kt < p.kt1; ++kt, ++issued) {
-        const int s = issued % kStages;
-        if (issued >= kStages) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), ((issued / kStages) - 1) & 1));
+        const int s = issued % kLS;
+        if (issued >= kLS) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), ((issued / kLS) - 1) & 1));
         if (!ok) break;
         const int k0 = kt * kTile;
         int ys[kTile / 16];
@@ -423,14 +489,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
         if (lane == 0) {
           const uint32_t fb = smem_u32(&full[s]);
           mbar_expect_tx(fb, static_cast<uint32_t>(nbox) * 2u * box_bytes);
-          const uint32_t kdst = smem_u32(stages + s * kStageBytes);
-          const uint32_t vdst = kdst + 2 * kHalfBytes;
+          const uint32_t kdst = smem_u32(stages + s * kLoadStageBytes);
+          const uint32_t vdst = kdst + (F8 ? kCodeHalf : 2 * kHalfBytes);
 #pragma unroll
           for (int j = 0; j < kTile / 16; ++j) {
             if (ys[j] < 0) continue;
-            const uint32_t off = static_cast<uint32_t>(j * box) * 256;  // group of `box` rows, both halves
-            tma_load_rows(kdst + off, &tmap_k, ys[j], fb);
-            tma_load_rows(vdst + off, &tmap_v, ys[j], fb);
+            const uint32_t off = static_cast<uint32_t>(j * box) * row_bytes;  // group of `box` rows
+            if (F8) {
+              tma_load_codes(kdst + off, &tmap_k, ys[j], fb);
+              tma_load_codes(vdst + off, &tmap_v, ys[j], fb);
+            } else {
+              tma_load_rows(kdst + off, &tmap_k, ys[j], fb);
+              tma_load_rows(vdst + off, &tmap_v, ys[j], fb);
+            }
           }
         }
         __syncwarp();
@@ -439,18 +510,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
   } else if (warp == 1) {
     // ================= MMA issuer =================
     const int R = P.box_rows;  // rows per group: 16 or 32
-    const uint32_t idesc_s = mma_idesc(128, kTile, 0);
-    constexpr uint32_t idesc_o = mma_idesc(128, kD, 1);
+    constexpr uint32_t idesc_s = mma_idesc(128, kTile, 0, F8);
+    constexpr uint32_t idesc_o = mma_idesc(128, kD, 1, F8);
     (void)R;
     auto issue_pv = [&](int u, bool accumulate) {  // O (+)= P(u) V(u), 16 keys per MMA
-      const int su = u % kStages;
-      const uint32_t v_base = smem_u32(stages + su * kStageBytes) + 2 * kHalfBytes;
+      const int su = u % kMS;
+      const uint32_t v_base = smem_u32(mstages + su * kStageBytes) + 2 * kHalfBytes;
       const uint32_t p_col = tmem + (u & 1) * kTile;
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk)  // keys 16 kk .. 16 kk + 15: two 8-key groups of 2 KB
         mma_ts(tmem + kColO, p_col + kk * 8, smem_desc(v_base + kk * 4096, 1024, 2048), idesc_o,
                (accumulate || kk > 0) ? 1 : 0);
-      mma_commit(smem_u32(&empty[su]));
+      mma_commit(smem_u32(&mempty[su]));
       mma_commit(smem_u32(o_bar));
     };
     int t = 0, piece = 0;
@@ -458,14 +529,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
     Piece p;
     while (ok && walker.next(P, p)) {
       for (int kt = p.kt0; kt < p.kt1; ++kt, ++t) {
-        const int s = t % kStages;
-        bool w = mbar_wait(smem_u32(&full[s]), (t / kStages) & 1);
+        const int s = t % kMS;
+        bool w = mbar_wait(smem_u32(&mfull[s]), (t / kMS) & 1);
         if (w && kt == p.kt0) w = mbar_wait(smem_u32(q_ready), piece & 1);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t k_base = smem_u32(stages + s * kStageBytes);
+          const uint32_t k_base = smem_u32(mstages + s * kStageBytes);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)  // 8-key groups 2 KB apart, half kk / 4 at +1 KB
             mma_ts(tmem + (t & 1) * kTile, tmem + kColQ + kk * 8,
@@ -498,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
     if (lane == 0) mma_commit(smem_u32(mma_done));
     __syncwarp();
     if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(mma_done), 0))) ok = false;
-  } else {
+  } else if (warp >= kSoft0 && warp < kSoft0 + kSoftWarps) {
     // ================= softmax, one query row per thread =================
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
     const int row = q4 * 32 + lane;          // row within the unit's row block = TMEM lane
@@ -512,12 +583,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
       g = live ? r - i * P.G : 0;
       return live;
     };
-    // this lane's Q row of piece p as bf16 pairs (zeros for a padding lane)
-    auto load_q = [&](const Piece &p, uint32_t (&qr)[64]) -> bool {
+    // this lane's Q row of piece p into TMEM as bf16 pairs, fp16 pairs for F8 (zeros for a
+    // padding lane); then q_ready. All 16 loads go out before the first store.
+    auto load_store_q = [&](const Piece &p) {
       int i, g;
       const bool live = row_of(p, i, g);
+      uint32_t qr[64];
       if (live) {
-        const uint4 *qp = reinterpret_cast<const uint4 *>(qsrc + ((size_t)(p.row0 + i) * a.num_q_heads + p.kvh * P.G + g) * kD);
+        const uint4 *qp =
+            reinterpret_cast<const uint4 *>(qsrc + ((size_t)(p.row0 + i) * a.num_q_heads + p.kvh * P.G + g) * kD);
 #pragma unroll
         for (int v = 0; v < 16; ++v) {
           const uint4 x = qp[v];
@@ -526,11 +600,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
           qr[4 * v + 2] = x.z;
           qr[4 * v + 3] = x.w;
         }
+        if (F8) {
+          bool over = false;
+#pragma unroll
+          for (int v = 0; v < 64; ++v) qr[v] = bf16x2_to_f16x2(qr[v], &over);
+          if (over) record(a.status, SV_ERR_NONFINITE);  // a query element beyond the fp16 range
+        }
       } else {
 #pragma unroll
         for (int v = 0; v < 64; ++v) qr[v] = 0u;
       }
-      return live;
+      if (__any_sync(0xffffffffu, live)) {
+        tmem_st64(lane_addr + kColQ, qr);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(q_ready));
     };
     // the next unit's Q row into L2 while this unit's last S is awaited
     auto prefetch_q = [&](const Piece &p) {
@@ -541,22 +627,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qp + 128));
       }
     };
-    auto store_q = [&](const uint32_t (&qr)[64], bool live) {
-      if (__any_sync(0xffffffffu, live)) {
-        tmem_st64(lane_addr + kColQ, qr);
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(q_ready));
-    };
+    const float sl2 = F8 ? a.scale_log2 * (kv.k_scale * kF16CodeScale) : a.scale_log2;  // scores in log2 units
     Piece cur, nxt;
     bool has_cur = walker.next(P, cur);
     bool has_nxt = has_cur && walker.next(P, nxt);
-    if (has_cur) {
-      uint32_t qr[64];
-      store_q(qr, load_q(cur, qr));
-    }
+    if (has_cur) load_store_q(cur);
     int t = 0;
     bool first_piece = true;
     while (has_cur && ok) {
@@ -575,10 +650,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
         if (!ok) break;
         tc_fence_after();
         // S(t) was this unit's last product with its Q: the next unit's rows can take its place
-        if (handoff) {
-          uint32_t qr[64];
-          store_q(qr, load_q(nxt, qr));
-        }
+        if (handoff) load_store_q(nxt);
         if (kt == cur.kt1 - 1 && t >= 1) {
           // last tile of the piece: P(t-1) V(t-1) must be done before P(t) goes out. Here
           // P V(t) cannot have started, so o_bar is in the phase of t-1 or t and the parity
@@ -586,10 +658,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_bar), (t - 1) & 1));
           if (!ok) break;
         }
-        if (valid < kTile) {
-          // zero this tile's V rows past the unit's end before P V reads them
+        if (!F8 && valid < kTile) {
+          // zero this tile's V rows past the unit's end before P V reads them (F8: the converters do)
           uint8_t *vst = stages + (t % kStages) * kStageBytes + 2 * kHalfBytes;
-          for (int x = (warp - 2) * 32 + lane; x < (kTile - valid) * 16; x += kSoftWarps * 32) {
+          for (int x = (warp - kSoft0) * 32 + lane; x < (kTile - valid) * 16; x += kSoftWarps * 32) {
             const int rr = valid + (x >> 4), ch = x & 15;
             *reinterpret_cast<uint4 *>(vst + (rr >> 3) * 2048 + (ch >> 3) * 1024 + (rr & 7) * 128 + (ch & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -607,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
           float sv[32];
           if (!edge) {
 #pragma unroll
-            for (int k = 0; k < kTile; ++k) sv[k] = __uint_as_float(sr[k]) * a.scale_log2;
+            for (int k = 0; k < kTile; ++k) sv[k] = __uint_as_float(sr[k]) * sl2;
           } else {
 #pragma unroll
             for (int k = 0; k < kTile; ++k) {
@@ -617,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
                 const int j = key - c;
                 vis = (a.mask_kind == SV_MASK_CAUSAL) ? (j <= i) : (j < 64 && ((tm >> j) & 1ull));
               }
-              sv[k] = vis ? __uint_as_float(sr[k]) * a.scale_log2 : -INFINITY;
+              sv[k] = vis ? __uint_as_float(sr[k]) * sl2 : -INFINITY;
             }
           }
           float mx;
@@ -661,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
           for (int k = 0; k < kTile / 2; ++k) {
             const float p0 = fast_exp2(sv[2 * k] - ref), p1 = fast_exp2(sv[2 * k + 1] - ref);
             ps[k] = p0 + p1;
-            pr[k] = pack_bf16(p0, p1);
+            pr[k] = F8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
           }
 #pragma unroll
           for (int w = 8; w > 0; w >>= 1)
@@ -685,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
       if (!ok) break;
       tc_fence_after();
       if (warp_live) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float inv = l_run > 0.f ? (F8 ? kv.v_scale * kF16CodeScale : 1.f) / l_run : 0.f;
         const size_t qrow = (size_t)(cur.row0 + i) * a.num_q_heads + cur.kvh * P.G + g;
         const size_t slot = ((size_t)blockIdx.x * 2 + (first_piece ? 0 : 1)) * P.rows_cap + row;
 #pragma unroll
@@ -717,6 +789,59 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
       has_cur = has_nxt;
       has_nxt = has_cur && walker.next(P, nxt);
     }
+  } else if (F8) {
+    // ================= E4M3 codes -> fp16 operands =================
+    // Each code stage holds K then V as rows of 128 one-byte codes; each operand stage
+    // takes them in the layout the TMA gives bf16 rows (8-row groups of [half 0][half 1],
+    // 16-byte chunks swizzled by the row within the group). Keys past the piece's end
+    // become zero rows, so P V never reads stale values.
+    constexpr int kCT = kConvWarps * 32;             // converter threads
+    constexpr int kPer = (kTile * 8) / kCT;          // 16-code chunks of K (and of V) per thread and tile
+    const int ct = tid - (kSoft0 + kSoftWarps) * 32;
+    int t = 0;
+    Piece p;
+    while (ok && walker.next(P, p)) {
+      const int ke = min(p.L, p.kt1 * kTile);
+      for (int kt = p.kt0; kt < p.kt1; ++kt, ++t) {
+        const int cs = t % kLS, ms = t % kMS;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[cs]), (t / kLS) & 1));
+        if (!ok) break;
+        const int valid = min(kTile, ke - kt * kTile);
+        const uint8_t *src = stages + cs * kCodeStageBytes;
+        uint4 x[2 * kPer];  // 16 codes each: K chunks, then V chunks
+#pragma unroll
+        for (int j = 0; j < 2 * kPer; ++j) {
+          const int chunk = ct + kCT * (j % kPer), r = chunk >> 3, c = chunk & 7;
+          x[j] = r < valid ? *reinterpret_cast<const uint4 *>(src + (j / kPer) * kCodeHalf + r * 128 + c * 16)
+                           : make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[cs]));  // the codes are in registers: the stage can refill
+        if (t >= kMS) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&cempty[ms]), ((t / kMS) - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        uint8_t *dst = mstages + ms * kStageBytes;
+#pragma unroll
+        for (int j = 0; j < 2 * kPer; ++j) {
+          const int half = j / kPer;               // 0: K, 1: V
+          const int chunk = ct + kCT * (j % kPer);  // 16 codes: row chunk >> 3, columns 16 (chunk & 7) ..
+          const int r = chunk >> 3, c = chunk & 7;
+          // byte selectors: codes 0, 1 of a word -> 0x1404; codes 2, 3 -> 0x3424 (zero codes: zero rows)
+          const uint4 lo = make_uint4(e4m3x2_to_f16x2_scaled<0x1404>(x[j].x), e4m3x2_to_f16x2_scaled<0x3424>(x[j].x),
+                                      e4m3x2_to_f16x2_scaled<0x1404>(x[j].y), e4m3x2_to_f16x2_scaled<0x3424>(x[j].y));
+          const uint4 hi = make_uint4(e4m3x2_to_f16x2_scaled<0x1404>(x[j].z), e4m3x2_to_f16x2_scaled<0x3424>(x[j].z),
+                                      e4m3x2_to_f16x2_scaled<0x1404>(x[j].w), e4m3x2_to_f16x2_scaled<0x3424>(x[j].w));
+          uint8_t *row = dst + half * 2 * kHalfBytes + (r >> 3) * 2048 + (c >> 2) * 1024 + (r & 7) * 128;
+          const int j0 = (c & 3) * 2;  // the 16-byte chunk of columns 16 c .. 16 c + 7 within the half row
+          *reinterpret_cast<uint4 *>(row + ((j0 ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4 *>(row + (((j0 + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        fence_proxy_async();  // the generic-proxy stores, visible to the tensor cores
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&cfull[ms]));
+      }
+    }
   }
   if (!ok) {
     if (lane == 0) record(a.status, SV_ERR_TIMEOUT);
@@ -727,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_umma_kernel(const _
   tc_fence_after();
   if (sh_err != 0 && warp == 0 && lane == 0) {
     // after a failed wait, let this CTA's copies in flight land before its shared memory is released
-    for (int k = max(0, issued - kStages); k < issued; ++k) mbar_wait(smem_u32(&full[k % kStages]), (k / kStages) & 1);
+    for (int k = max(0, issued - kLS); k < issued; ++k) mbar_wait(smem_u32(&full[k % kLS]), (k / kLS) & 1);
   }
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
@@ -844,10 +969,22 @@ EncodeTiledFn encode_fn() {
 // group); a box of R rows lands as R/8 groups of [half 0: 8 rows x 128 B]
 // [half 1: 8 rows x 128 B], 128-byte swizzled: every 1 KB is one swizzle
 // atom, and the atoms of one half are 2 KB apart across the whole tile.
+//
+// An E4M3 pool is a 2-D tensor (128 one-byte codes, rows) read without swizzle: a
+// box of R rows lands as R rows of 128 B.
 bool make_map(CUtensorMap *map, void *pool, const KV &kv, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t rows = (cuuint64_t)kv.num_blocks * kv.num_kv_heads * kv.block_size;
+  if (kv.fp8) {
+    const cuuint64_t gdim[2] = {(cuuint64_t)kD, rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)kD};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, pool, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const cuuint64_t gdim[4] = {64, 8, 2, rows / 8};
   const cuuint64_t gstride[3] = {(cuuint64_t)kD * 2, 128, (cuuint64_t)kD * 2 * 8};
   const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)box_rows / 8};
@@ -857,8 +994,13 @@ bool make_map(CUtensorMap *map, void *pool, const KV &kv, int box_rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 6 stages of 16 KB; at most two CTAs fit an SM, which is what TMEM allows (2 x 256 columns)
+// 6 stages of 16 KB (E4M3: 4 code stages of 8 KB and 4 operand stages of 16 KB); at most two
+// CTAs fit an SM, which is what TMEM allows (2 x 256 columns)
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 32 * 8;
+static_assert(kCodeStages * kCodeStageBytes + kConvStages * kStageBytes <= kStages * kStageBytes,
+              "the E4M3 rings fit the bf16 ring's space");
+static_assert(2 * (kStages > kCodeStages ? kStages : kCodeStages) + 2 * kConvStages + 7 <= 31,
+              "barriers and the TMEM slot fit 256 B");
 static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "a third CTA per SM would wait for TMEM");
 
 struct UmmaLayout {
@@ -886,7 +1028,7 @@ UmmaLayout umma_layout(const KV &kv, int num_q_heads, int max_q, int max_seq_len
 bool attn_umma_supported(const KV &kv) {
   // TMA row coordinates are 32-bit: the pool's rows (blocks x KV heads x block_size) must fit
   const long long rows = (long long)kv.num_blocks * kv.num_kv_heads * kv.block_size;
-  return kv.elem_bytes == 2 && kv.head_dim == kD && kv.block_size >= 16 && kv.block_size <= 256 &&
+  return (kv.elem_bytes == 2 || kv.fp8) && kv.head_dim == kD && kv.block_size >= 16 && kv.block_size <= 256 &&
          (kv.block_size & (kv.block_size - 1)) == 0 && rows < (1LL << 31) &&
          encode_fn() != nullptr && ((uintptr_t)kv.k_pool % 16 == 0) && ((uintptr_t)kv.v_pool % 16 == 0);
 }
@@ -920,9 +1062,11 @@ cudaError_t launch_attn_umma(const AttnArgs &a, void *workspace, size_t workspac
   CUtensorMap mk, mv;
   if (!make_map(&mk, a.kv.k_pool, a.kv, p.box_rows) || !make_map(&mv, a.kv.v_pool, a.kv, p.box_rows))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  auto kernel = a.kv.fp8 ? attn_umma_kernel<true> : attn_umma_kernel<false>;
+  const int threads = a.kv.fp8 ? kThreads + kConvWarps * 32 : kThreads;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(attn_umma_kernel, dim3(p.ctas), dim3(kThreads), kSmemBytes, st, mk, mv, p);
+  e = launch_pdl(kernel, dim3(p.ctas), dim3(threads), kSmemBytes, st, mk, mv, p);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_umma_combine, dim3(a.kv.batch, a.kv.num_kv_heads * p.rb_max), dim3(128), 0, st, p);
 }

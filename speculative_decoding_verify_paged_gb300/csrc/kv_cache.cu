@@ -15,10 +15,33 @@
 //
 // The bookkeeping runs in one CTA (a block-wide scan over the batch); the row
 // scatter and the tree-path compaction run one CTA per row / per sequence.
+#include <cuda_fp8.h>
+
 #include "sv_internal.cuh"
 
 namespace sv {
 namespace {
+
+// 16 bf16 values (two 16-byte vectors) -> 16 E4M3 codes of x / scale (fp32
+// division; nearest, ties to even; saturating), element j in byte j.
+__device__ __forceinline__ uint4 quantize16(const uint4 &a, const uint4 &b, float scale) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t v = w[2 * q + h];
+      const float x0 = __fdiv_rn(__uint_as_float(v << 16), scale);
+      const float x1 = __fdiv_rn(__uint_as_float(v & 0xffff0000u), scale);
+      const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+      word |= (uint32_t)c << (16 * h);
+    }
+    out[q] = word;
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
 
 constexpr int kBookThreads = 1024;
 
@@ -237,11 +260,17 @@ __global__ void __launch_bounds__(kScatterThreads) kv_scatter_kernel(KV kv, cons
   const int row_bytes = kv.head_dim * kv.elem_bytes;  // a multiple of 16
   const int vec_per_row = row_bytes / 16;
   const int total = kv.num_kv_heads * vec_per_row;
-  const size_t src_row = (size_t)row * kv.num_kv_heads * row_bytes;
-  uint4 kk0 = make_uint4(0, 0, 0, 0), vv0 = kk0;  // the thread's first vector
+  // an fp8 pool's 16-byte vector (16 codes) comes from 32 bytes of bf16 input
+  const int src_vec = kv.fp8 ? 32 : 16;
+  const size_t src_row = (size_t)row * total * src_vec;
+  uint4 kk0 = make_uint4(0, 0, 0, 0), vv0 = kk0, kk1 = kk0, vv1 = kk0;  // the thread's first vector
   if ((int)threadIdx.x < total) {
-    kk0 = *reinterpret_cast<const uint4 *>(new_k + src_row + (size_t)threadIdx.x * 16);
-    vv0 = *reinterpret_cast<const uint4 *>(new_v + src_row + (size_t)threadIdx.x * 16);
+    kk0 = *reinterpret_cast<const uint4 *>(new_k + src_row + (size_t)threadIdx.x * src_vec);
+    vv0 = *reinterpret_cast<const uint4 *>(new_v + src_row + (size_t)threadIdx.x * src_vec);
+    if (kv.fp8) {
+      kk1 = *reinterpret_cast<const uint4 *>(new_k + src_row + (size_t)threadIdx.x * src_vec + 16);
+      vv1 = *reinterpret_cast<const uint4 *>(new_v + src_row + (size_t)threadIdx.x * src_vec + 16);
+    }
   }
   const bool staged = B + 1 <= kCuCache;
   if (staged)
@@ -289,10 +318,18 @@ __global__ void __launch_bounds__(kScatterThreads) kv_scatter_kernel(KV kv, cons
   }
   for (int x = threadIdx.x; x < total; x += blockDim.x) {
     const int h = x / vec_per_row, v = x % vec_per_row;
-    uint4 kk = kk0, vv = vv0;
+    uint4 kk = kk0, vv = vv0, kb = kk1, vb = vv1;
     if (x >= (int)blockDim.x) {
-      kk = *reinterpret_cast<const uint4 *>(new_k + src_row + (size_t)x * 16);
-      vv = *reinterpret_cast<const uint4 *>(new_v + src_row + (size_t)x * 16);
+      kk = *reinterpret_cast<const uint4 *>(new_k + src_row + (size_t)x * src_vec);
+      vv = *reinterpret_cast<const uint4 *>(new_v + src_row + (size_t)x * src_vec);
+      if (kv.fp8) {
+        kb = *reinterpret_cast<const uint4 *>(new_k + src_row + (size_t)x * src_vec + 16);
+        vb = *reinterpret_cast<const uint4 *>(new_v + src_row + (size_t)x * src_vec + 16);
+      }
+    }
+    if (kv.fp8) {
+      kk = quantize16(kk, kb, kv.k_scale);
+      vv = quantize16(vv, vb, kv.v_scale);
     }
     const size_t dst = (((size_t)blk * kv.num_kv_heads + h) * kv.block_size + slot) * row_bytes + (size_t)v * 16;
     *reinterpret_cast<uint4 *>((uint8_t *)kv.k_pool + dst) = kk;

@@ -66,7 +66,11 @@ sv_status check_kv(const sv_paged_kv *kv, bool need_free) {
     return SV_ERR_INVALID_ARG;
   if (!pow2(kv->block_size) || kv->block_size > 256) return SV_ERR_INVALID_ARG;
   if (kv->head_dim < 8 || kv->head_dim > 256 || kv->head_dim % 8 != 0) return SV_ERR_INVALID_ARG;
-  if (kv->dtype != SV_DTYPE_BF16 && kv->dtype != SV_DTYPE_F32) return SV_ERR_INVALID_ARG;
+  if (kv->dtype != SV_DTYPE_BF16 && kv->dtype != SV_DTYPE_F32 && kv->dtype != SV_DTYPE_E4M3) return SV_ERR_INVALID_ARG;
+  if (kv->dtype == SV_DTYPE_E4M3 &&
+      (kv->head_dim % 16 != 0 || !(kv->k_scale > 0.f) || !(kv->v_scale > 0.f) || kv->k_scale == INFINITY ||
+       kv->v_scale == INFINITY))
+    return SV_ERR_INVALID_ARG;
   if (kv->batch > 0 && (kv->block_table == nullptr || kv->seq_lens == nullptr)) return SV_ERR_INVALID_ARG;
   if (kv->k_pool == nullptr || kv->v_pool == nullptr) return SV_ERR_INVALID_ARG;
   if (!aligned16(kv->k_pool) || !aligned16(kv->v_pool)) return SV_ERR_INVALID_ARG;
@@ -78,13 +82,13 @@ sv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_
 
 // Whether the tcgen05 kernel can take these sizes.
 bool umma_usable(const sv_paged_kv *kv, int32_t num_q_heads, int32_t max_q, int32_t max_seq_len) {
-  return kv->dtype == SV_DTYPE_BF16 && attn_umma_supported(make_kv(*kv)) &&
+  return (kv->dtype == SV_DTYPE_BF16 || kv->dtype == SV_DTYPE_E4M3) && attn_umma_supported(make_kv(*kv)) &&
          attn_umma_fits(make_kv(*kv), num_q_heads, max_q, max_seq_len);
 }
 
 // Whether the keys-major tcgen05 kernel can (units of at most 32 query rows).
 bool keys_usable(const sv_paged_kv *kv, int32_t num_q_heads, int32_t max_q, int32_t max_seq_len) {
-  return umma_usable(kv, num_q_heads, max_q, max_seq_len) &&
+  return kv->dtype == SV_DTYPE_BF16 && umma_usable(kv, num_q_heads, max_q, max_seq_len) &&
          attn_keys_fits(make_kv(*kv), num_q_heads, max_q, max_seq_len);
 }
 

@@ -106,6 +106,8 @@ struct KV {
   int32_t *ref_count;  // null: no sharing
   int num_blocks, block_size, max_blocks, num_kv_heads, head_dim, batch;
   int elem_bytes;
+  bool fp8;                // E4M3 pool: 1-byte codes, bf16 rows in and out
+  float k_scale, v_scale;  // E4M3 dequantisation scales
 };
 
 inline KV make_kv(const sv_paged_kv &p) {
@@ -123,7 +125,10 @@ inline KV make_kv(const sv_paged_kv &p) {
   k.num_kv_heads = p.num_kv_heads;
   k.head_dim = p.head_dim;
   k.batch = p.batch;
-  k.elem_bytes = p.dtype == SV_DTYPE_BF16 ? 2 : 4;
+  k.elem_bytes = p.dtype == SV_DTYPE_BF16 ? 2 : (p.dtype == SV_DTYPE_E4M3 ? 1 : 4);
+  k.fp8 = p.dtype == SV_DTYPE_E4M3;
+  k.k_scale = p.k_scale;
+  k.v_scale = p.v_scale;
   return k;
 }
 

@@ -52,7 +52,8 @@ def device_kv(state, device="cuda", ref_count=None) -> L.PagedKV:
         seq_lens=_dev(state.seq_lens.astype(np.int32), device),
         free_list=_dev(state.free_list.astype(np.int32), device),
         free_top=torch.tensor([state.free_top], dtype=torch.int32, device=device),
-        ref_count=None if ref_count is None else _dev(np.asarray(ref_count, np.int32), device))
+        ref_count=None if ref_count is None else _dev(np.asarray(ref_count, np.int32), device),
+        k_scale=float(getattr(state, "k_scale", 1.0)), v_scale=float(getattr(state, "v_scale", 1.0)))
 
 
 @dataclass

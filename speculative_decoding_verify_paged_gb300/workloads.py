@@ -415,7 +415,7 @@ def tree(seed: int = 5, *, batch: int = 16, ctx: int = 8192, block_size: int = 6
          branching=(4, 3, 2, 2, 1, 1), keep: int = 60, vocab: int = 32000,
          num_q_heads: int = 32, num_kv_heads: int = 8, head_dim: int = 128,
          target_sigma: float = 3.0, draft_coef: float = 0.8, draft_sigma: float = 1.0,
-         temperature: float = 0.0) -> Case:
+         temperature: float = 0.0, kv_dtype: str = "bf16") -> Case:
     """EAGLE/Medusa-style draft trees at long context, greedy acceptance (or, at
     temperature > 0, the lossless tree rule with seeded uniforms).
 
@@ -432,7 +432,7 @@ def tree(seed: int = 5, *, batch: int = 16, ctx: int = 8192, block_size: int = 6
     ctx_lens = np.full(batch, ctx, np.int32)
     rows_per_seq = keep + 1
     state = make_kv_state(seed, ctx_lens, block_size=block_size, num_kv_heads=num_kv_heads,
-                          head_dim=head_dim, dtype="bf16", growth_tokens=rows_per_seq)
+                          head_dim=head_dim, dtype=kv_dtype, growth_tokens=rows_per_seq)
     bank = _Bank(seed)
     tgt_rows, drf_rows, toks, parents, masks = [], [], [], [], []
     for b in range(batch):
