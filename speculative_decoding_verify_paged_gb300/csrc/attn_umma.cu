@@ -857,17 +857,16 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
-// Merges the partial results of every unit that two or more CTAs shared.
-// First one thread per query row takes the maximum and the denominator of the
-// pieces' log-sum-exps; then the CTA's threads sweep the (row, 4 head_dim
-// elements) outputs, loading four pieces at a time.
+// Merges the partial results of every unit that two or more CTAs shared. A
+// thread takes one (row, 32 head_dim elements) item and issues the loads of
+// every piece's log-sum-exp and 32 partial outputs before it uses any (up to
+// four pieces; more go four at a time), so a merge costs about one round trip.
 __global__ void __launch_bounds__(128) attn_umma_combine(const UmmaParams P) {
   grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   grid_dependents_launch();
   const AttnArgs &a = P.a;
   const int b = blockIdx.x, kvh = blockIdx.y / P.rb_max, rb = blockIdx.y % P.rb_max;
   const int tid = threadIdx.x;
-  __shared__ float row_max[kRowsMax], row_inv[kRowsMax];
   const int W = P.prefix[a.kv.batch], base = P.prefix[b];  // loaded together with the sequence
   bool bad;
   const Seq s = load_seq(P, b, &bad);
@@ -882,64 +881,57 @@ __global__ void __launch_bounds__(128) attn_umma_combine(const UmmaParams P) {
   auto slot_of = [&](int cc, int row) -> size_t {
     return ((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * P.rows_cap + row;
   };
+  constexpr int kPc = 4;  // pieces in flight
   const int rows = min(kRowsMax, P.G * s.n - rb * kRowsMax);
-  for (int row = tid; row < rows; row += blockDim.x) {
-    float M = -INFINITY;
-    for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, P.part_lse[slot_of(cc, row)]);
-    float den = 0.f;
-    if (M != -INFINITY)
-      for (int cc = c0; cc <= c1; ++cc) den += exp2f(P.part_lse[slot_of(cc, row)] - M);
-    row_max[row] = M;
-    row_inv[row] = den > 0.f ? 1.f / den : 0.f;
-  }
-  __syncthreads();
-  // outputs (row, 4 head_dim elements): each thread takes up to kUnroll of them at once,
-  // with every piece's loads issued before any is used
-  constexpr int kUnroll = 4;
-  const int outs = rows * (kD / 4);
-  for (int x0 = tid; x0 < outs; x0 += blockDim.x * kUnroll) {
-    float4 acc[kUnroll];
-    int xr[kUnroll];
+  for (int x = tid; x < rows * (kD / 32); x += blockDim.x) {
+    const int row = x / (kD / 32), c32 = (x % (kD / 32)) * 32;
+    float M = -INFINITY, den = 0.f;
+    float acc[32];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      xr[u] = x0 + u * blockDim.x;
-    }
-    for (int cc = c0; cc <= c1; ++cc) {
-      float lse[kUnroll];
-      float4 o[kUnroll];
+    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+    for (int cb = c0; cb <= c1; cb += kPc) {
+      float lse[kPc];
+      float4 v[kPc][8];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        lse[u] = -INFINITY;
-        o[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (xr[u] < outs) {
-          const int row = xr[u] / (kD / 4), c4 = (xr[u] % (kD / 4)) * 4;
-          const size_t sl = slot_of(cc, row);
-          lse[u] = P.part_lse[sl];
-          o[u] = *reinterpret_cast<const float4 *>(P.part_o + sl * kD + c4);
+      for (int k = 0; k < kPc; ++k) {
+        const bool in = cb + k <= c1;
+        const size_t sl = slot_of(in ? cb + k : cb, row);
+        lse[k] = in ? __ldcg(P.part_lse + sl) : -INFINITY;
+        const float4 *src = reinterpret_cast<const float4 *>(P.part_o + sl * kD + c32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[k][j] = in ? __ldcg(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float mn = M;
+#pragma unroll
+      for (int k = 0; k < kPc; ++k) mn = fmaxf(mn, lse[k]);
+      if (mn == -INFINITY) continue;
+      const float f = exp2f(M - mn);  // 0 while nothing was taken yet
+      den *= f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) acc[k] *= f;
+#pragma unroll
+      for (int k = 0; k < kPc; ++k) {
+        const float w = exp2f(lse[k] - mn);
+        den += w;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          acc[4 * j] = fmaf(w, v[k][j].x, acc[4 * j]);
+          acc[4 * j + 1] = fmaf(w, v[k][j].y, acc[4 * j + 1]);
+          acc[4 * j + 2] = fmaf(w, v[k][j].z, acc[4 * j + 2]);
+          acc[4 * j + 3] = fmaf(w, v[k][j].w, acc[4 * j + 3]);
         }
       }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (xr[u] >= outs) continue;
-        const float M = row_max[xr[u] / (kD / 4)];
-        const float wk = M == -INFINITY ? 0.f : exp2f(lse[u] - M);
-        acc[u].x = fmaf(wk, o[u].x, acc[u].x);
-        acc[u].y = fmaf(wk, o[u].y, acc[u].y);
-        acc[u].z = fmaf(wk, o[u].z, acc[u].z);
-        acc[u].w = fmaf(wk, o[u].w, acc[u].w);
-      }
+      M = mn;
     }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int r = rb * kRowsMax + row, i = r / P.G, g = r - i * P.G;
+    const size_t qrow = (size_t)(s.row0 + i) * a.num_q_heads + kvh * P.G + g;
+    uint4 *op = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + qrow * kD + c32);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (xr[u] >= outs) continue;
-      const int row = xr[u] / (kD / 4), c4 = (xr[u] % (kD / 4)) * 4;
-      const float inv = row_inv[row];
-      const int r = rb * kRowsMax + row, i = r / P.G, g = r - i * P.G;
-      const size_t qrow = (size_t)(s.row0 + i) * a.num_q_heads + kvh * P.G + g;
-      *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + qrow * kD + c4) =
-          make_uint2(pack_bf16(acc[u].x * inv, acc[u].y * inv), pack_bf16(acc[u].z * inv, acc[u].w * inv));
-    }
+    for (int j = 0; j < 4; ++j)
+      op[j] = make_uint4(pack_bf16(acc[8 * j] * inv, acc[8 * j + 1] * inv), pack_bf16(acc[8 * j + 2] * inv, acc[8 * j + 3] * inv),
+                         pack_bf16(acc[8 * j + 4] * inv, acc[8 * j + 5] * inv),
+                         pack_bf16(acc[8 * j + 6] * inv, acc[8 * j + 7] * inv));
   }
 }
 

@@ -531,59 +531,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
   }
   bool ok = true;  // false after a bounded wait gave up: the remaining work is skipped, barriers are kept
 
-  // ---------------- row statistics from the partials: one warp per row ----------------
-  for (int r = warp; r < rows; r += kWarps) {
-    const int gr = r < n ? t0 + r : args.total_q + d0 + (r - n);  // row of the statistics kernel
-    const size_t p0 = (size_t)gr * nchunk * kStatWarps;
-    const int np = nchunk * kStatWarps;
-    if constexpr (STOCH) {
-      float m = -INFINITY, s = 0.f;
-      for (int q0 = 0; q0 < np; q0 += 128) {  // four loads of each array in flight per lane
-        float lm[4], lsum[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int q = q0 + 32 * j + lane;
-          lm[j] = q < np ? pm[p0 + q] : -INFINITY;
-          lsum[j] = q < np ? ps[p0 + q] : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) ms_combine(m, s, lm[j], lsum[j], coef);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        ms_combine(m, s, m2, s2, coef);
-      }
-      if (lane == 0) {
-        sm.M[r] = m;
-        sm.Z[r] = s;
-      }
-    } else {
-      float best = 0.f;
-      int bi = -1;
-      for (int q0 = 0; q0 < np; q0 += 128) {
-        float lv[4];
-        int li[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int q = q0 + 32 * j + lane;
-          lv[j] = q < np ? pm[p0 + q] : 0.f;
-          li[j] = q < np ? __float_as_int(ps[p0 + q]) : -1;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) am_combine(best, bi, lv[j], li[j]);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-        am_combine(best, bi, v2, i2);
-      }
-      if (lane == 0) sm.am[r] = bi;
-    }
-  }
-  // the sequence's small inputs into shared memory, so the serial scans below read no global memory
+  // the sequence's small inputs into shared memory, so the serial scans below read no global memory;
+  // issued first, so that their latency overlaps the partials' below
   if (tid < K) sm.tok[tid] = args.draft_tok[d0 + tid];
   if ((MODE == kTree || MODE == kTreeStochastic) && tid < n) sm.par[tid] = args.parent[t0 + tid];
   if constexpr (MODE == kTreeStochastic) {
@@ -609,6 +558,100 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
       } else {
         sm.gtl[tid] = to_f32(tgt[(size_t)(t0 + tid) * V + x]);
         sm.gdl[tid] = to_f32(drf[(size_t)(d0 + tid) * V + x]);
+      }
+    }
+  }
+  // ---------------- row statistics from the partials: one warp per row ----------------
+  const int np = nchunk * kStatWarps;
+  if constexpr (STOCH) {
+    // four rows per warp at a time, every load of them in flight before any is used
+    constexpr int kRB = 4;
+    for (int r0 = warp; r0 < rows; r0 += kRB * kWarps) {
+      size_t p0[kRB];
+#pragma unroll
+      for (int h = 0; h < kRB; ++h) {
+        const int r = r0 + h * kWarps;
+        const int gr = r < n ? t0 + r : args.total_q + d0 + (r - n);  // row of the statistics kernel
+        p0[h] = (size_t)gr * np;
+      }
+      float m[kRB], sum[kRB];
+#pragma unroll
+      for (int h = 0; h < kRB; ++h) {
+        m[h] = -INFINITY;
+        sum[h] = 0.f;
+      }
+      for (int q0 = 0; q0 < np; q0 += 64) {  // two loads of each array per row in flight per lane
+        float lm[kRB][2], lsum[kRB][2];
+#pragma unroll
+        for (int h = 0; h < kRB; ++h)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int q = q0 + 32 * j + lane;
+            const bool in = q < np && r0 + h * kWarps < rows;
+            lm[h][j] = in ? pm[p0[h] + q] : -INFINITY;
+            lsum[h][j] = in ? ps[p0[h] + q] : 0.f;
+          }
+#pragma unroll
+        for (int h = 0; h < kRB; ++h)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) ms_combine(m[h], sum[h], lm[h][j], lsum[h][j], coef);
+      }
+#pragma unroll
+      for (int h = 0; h < kRB; ++h) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m[h], o);
+          const float s2 = __shfl_xor_sync(0xffffffffu, sum[h], o);
+          ms_combine(m[h], sum[h], m2, s2, coef);
+        }
+        const int r = r0 + h * kWarps;
+        if (lane == 0 && r < rows) {
+          sm.M[r] = m[h];
+          sm.Z[r] = sum[h];
+        }
+      }
+    }
+  } else {
+    // argmax rows, four per warp at a time (tree rows are many), every load in flight first
+    constexpr int kRB = 4;
+    for (int r0 = warp; r0 < rows; r0 += kRB * kWarps) {
+      size_t p0[kRB];
+#pragma unroll
+      for (int h = 0; h < kRB; ++h) p0[h] = (size_t)(t0 + r0 + h * kWarps) * np;  // rows < n: target rows
+      float best[kRB];
+      int bi[kRB];
+#pragma unroll
+      for (int h = 0; h < kRB; ++h) {
+        best[h] = 0.f;
+        bi[h] = -1;
+      }
+      for (int q0 = 0; q0 < np; q0 += 64) {  // two loads of each array per row in flight per lane
+        float lv[kRB][2];
+        int li[kRB][2];
+#pragma unroll
+        for (int h = 0; h < kRB; ++h)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int q = q0 + 32 * j + lane;
+            const bool in = q < np && r0 + h * kWarps < rows;
+            lv[h][j] = in ? pm[p0[h] + q] : 0.f;
+            li[h][j] = in ? __float_as_int(ps[p0[h] + q]) : -1;
+          }
+#pragma unroll
+        for (int h = 0; h < kRB; ++h)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) am_combine(best[h], bi[h], lv[h][j], li[h][j]);
+      }
+#pragma unroll
+      for (int h = 0; h < kRB; ++h) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float v2 = __shfl_xor_sync(0xffffffffu, best[h], o);
+          const int i2 = __shfl_xor_sync(0xffffffffu, bi[h], o);
+          am_combine(best[h], bi[h], v2, i2);
+        }
+        const int r = r0 + h * kWarps;
+        if (lane == 0 && r < rows) sm.am[r] = bi[h];
       }
     }
   }
@@ -785,7 +828,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
       const bool excl_pass = nexcl > 0 && pass == 0;
       // the eight weights of group g, in [0, 1]: proportional to max(0, p_v - q_v)
       // (scaled by Z_t), or to p_v
-      auto weights8 = [&](int g, long long (&w)[kGroup]) {
+      auto weightsf8 = [&](int g, float (&w)[kGroup]) {
         float xt[kGroup];
         group8<T>(bt, g, len, xt);
         if (res_pass) {
@@ -795,29 +838,52 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
           for (int k = 0; k < kGroup; ++k) {
             const float et = exp2_acc(xt[k] - Mt, chi, clo);
             const float ed = exp2_acc(xd[k] - Md, chi, clo);
-            w[k] = to_fix(fmaxf(et - fmaf(ed, rho_hi, ed * rho_lo), 0.f));
+            w[k] = fmaxf(et - fmaf(ed, rho_hi, ed * rho_lo), 0.f);
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < kGroup; ++k) w[k] = to_fix(exp2_acc(xt[k] - Mt, chi, clo));
+          for (int k = 0; k < kGroup; ++k) w[k] = exp2_acc(xt[k] - Mt, chi, clo);
           if (excl_pass) {  // the rejected children's tokens carry no mass
             const int v0 = lo + g * kGroup;
             for (int e = 0; e < nexcl; ++e) {
               const int d = sm.excl[e] - v0;
-              if (d >= 0 && d < kGroup) w[d] = 0;
+              if (d >= 0 && d < kGroup) w[d] = 0.f;
             }
           }
         }
+      };
+      // ... as fixed point, one by one
+      auto weights8 = [&](int g, long long (&w)[kGroup]) {
+        float f[kGroup];
+        weightsf8(g, f);
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) w[k] = to_fix(f[k]);
+      };
+      // ... and their fixed-point sum, equal to the sum of the values above: the 20-bit
+      // halves of to_fix summed as float bit patterns (2^23 + integer, eight of them:
+      // no carry leaves 32 bits), the offsets taken off once
+      auto mass8 = [&](int g) -> long long {
+        float f[kGroup];
+        weightsf8(g, f);
+        uint32_t sh = 0u, sl = 0u;
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+          const float t = f[k] * 1048576.0f;
+          const float h = __fadd_rd(t, 8388608.0f);
+          const float r = (t - (h - 8388608.0f)) * 1048576.0f;
+          const float l = __fadd_rn(r, 8388608.0f);
+          sh += __float_as_uint(h);
+          sl += __float_as_uint(l);
+        }
+        sh -= static_cast<uint32_t>(kGroup) * 0x4B000000u;
+        sl -= static_cast<uint32_t>(kGroup) * 0x4B000000u;
+        return (static_cast<long long>(sh) << 20) + static_cast<long long>(sl);
       };
       // ---- pass B: each group's mass and this CTA's total ----
       long long mass = 0;
       if (ok) {
         for (int g = tid; g < ngroups; g += kThreads) {
-          long long w[kGroup];
-          weights8(g, w);
-          long long m8 = 0;
-#pragma unroll
-          for (int k = 0; k < kGroup; ++k) m8 += w[k];
+          const long long m8 = mass8(g);
           gmass[g] = m8;
           mass += m8;
         }
