@@ -672,73 +672,111 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
       args.num_out[b] = a + 1;
     }
   } else if constexpr (MODE == kTree) {
-    if (rank == 0 && tid == 0) {
+    // the walk with one warp: at each node the lanes look for the first child (in row
+    // order) whose token is the node's argmax
+    if (rank == 0 && warp == 0) {
       int32_t *o = args.out_tok + (size_t)b * args.max_q;
       int32_t *path = args.path + (size_t)b * args.max_q;
-      for (int j = 0; j < args.max_q; ++j) {
+      for (int j = lane; j < args.max_q; j += 32) {
         o[j] = -1;
         path[j] = -1;
       }
-      int cur = 0, a = 0, am = sm.am[0];
-      bool good = true;
-      for (int j = 1; j < n; ++j) {
+      bool g_l = true;
+      for (int j = 1 + lane; j < n; j += 32) {
         const int p = sm.par[j];
-        good &= (p >= 0 && p < n && p != j);
+        g_l &= (p >= 0 && p < n && p != j);
       }
-      if (!good) record(args.status, SV_ERR_BAD_LENGTH);
+      const bool good = __all_sync(0xffffffffu, g_l);
+      if (!good && lane == 0) record(args.status, SV_ERR_BAD_LENGTH);
+      __syncwarp();  // the -1 fill lands before the path entries below
+      int cur = 0, a = 0;
       while (good && a < n - 1) {
-        am = sm.am[cur];
+        const int am = sm.am[cur];
         int next = -1;
-        for (int j = 1; j < n; ++j)
-          if (sm.par[j] == cur && sm.tok[j - 1] == am) {
-            next = j;
-            break;
-          }
+        for (int j0 = 1; j0 < n && next < 0; j0 += 32) {
+          const int j = j0 + lane;
+          const unsigned m = __ballot_sync(0xffffffffu, j < n && sm.par[j] == cur && sm.tok[j - 1] == am);
+          if (m) next = j0 + __ffs(m) - 1;
+        }
         if (next < 0) break;
-        path[a] = next;
-        o[a] = am;
+        if (lane == 0) {
+          path[a] = next;
+          o[a] = am;
+        }
         ++a;
         cur = next;
       }
-      am = sm.am[cur];
-      o[a] = am;
-      args.accept[b] = a;
-      args.num_out[b] = a + 1;
+      if (lane == 0) {
+        o[a] = sm.am[cur];
+        args.accept[b] = a;
+        args.num_out[b] = a + 1;
+      }
     }
   } else {
     if constexpr (MODE == kTreeStochastic) {
-      // ---------------- the tree walk (identical in every CTA, one thread) ----------------
+      // ---------------- the tree walk (identical in every CTA, one warp) ----------------
       // at the current node, children in row order: child x is accepted iff u < p'(x), p'
-      // the node's p without the tokens of the siblings rejected before, renormalised
-      if (tid == 0) {
-        bool good = true;
-        for (int j = 1; j < n; ++j) good &= sm.par[j] >= 0 && sm.par[j] < j;
-        bool nz = false;
-        for (int r = 0; r < n; ++r) nz |= !(sm.Z[r] > 0.f);
-        if (nz && rank == 0) record(args.status, SV_ERR_NONFINITE);
-        if (!good && rank == 0) record(args.status, SV_ERR_BAD_LENGTH);
-        int cur = 0, a = 0, nexcl = 0;
-        float removed = 0.f;
-        for (int j = 1; good && j < n; ++j) {
-          if (sm.par[j] != cur) continue;
-          const int x = sm.tok[j - 1];
-          bool dup = false;
-          for (int e = 0; e < nexcl; ++e) dup |= sm.excl[e] == x;
-          const float px = dup ? 0.f : exp2f((sm.gtl[j - 1] - sm.M[cur]) * coef) / sm.Z[cur];
-          const float thr = removed < 1.f ? px / (1.f - removed) : 0.f;
-          if (sm.uacc[j - 1] < thr) {  // accepted: the walk goes on from this child
-            sm.path[a++] = j;
-            cur = j;
-            nexcl = 0;
-            removed = 0.f;
-          } else {
-            removed += px;
-            if (!dup) sm.excl[nexcl++] = x;
+      // the node's p without the tokens of the siblings rejected before, renormalised. The
+      // lanes find the node's children and their p(x) (a child whose token an earlier
+      // sibling had weighs 0: that sibling was rejected); lane order then adds the rejected
+      // mass one child at a time, as a single thread would.
+      if (warp == 0) {
+        bool g_l = true, nz_l = false;
+        for (int j = 1 + lane; j < n; j += 32) g_l &= sm.par[j] >= 0 && sm.par[j] < j;
+        for (int r = lane; r < n; r += 32) nz_l |= !(sm.Z[r] > 0.f);
+        const bool good = __all_sync(0xffffffffu, g_l);
+        if (__any_sync(0xffffffffu, nz_l) && rank == 0 && lane == 0) record(args.status, SV_ERR_NONFINITE);
+        if (!good && rank == 0 && lane == 0) record(args.status, SV_ERR_BAD_LENGTH);
+        int cur = 0, a = 0;
+        bool moved = good;
+        while (moved) {  // one node per pass; children of cur lie after cur (checked above)
+          moved = false;
+          float removed = 0.f;
+          for (int j0 = cur + 1; j0 < n && !moved; j0 += 32) {
+            const int j = j0 + lane;
+            const bool child = j < n && sm.par[j] == cur;
+            unsigned m = __ballot_sync(0xffffffffu, child);
+            float px = 0.f;
+            if (child) {
+              const int x = sm.tok[j - 1];
+              bool dup = false;
+              for (int k = cur + 1; k < j; ++k) dup |= sm.par[k] == cur && sm.tok[k - 1] == x;
+              px = dup ? 0.f : exp2f((sm.gtl[j - 1] - sm.M[cur]) * coef) / sm.Z[cur];
+            }
+            while (m) {  // warp-uniform: the children of this chunk in row order
+              const int k = __ffs(m) - 1;
+              m &= m - 1;
+              const float pk = __shfl_sync(0xffffffffu, px, k);
+              const float thr = removed < 1.f ? pk / (1.f - removed) : 0.f;
+              if (sm.uacc[j0 + k - 1] < thr) {  // accepted: the walk goes on from this child
+                if (lane == 0) sm.path[a] = j0 + k;
+                ++a;
+                cur = j0 + k;
+                moved = true;
+                break;
+              }
+              removed += pk;
+            }
           }
         }
-        sm.a = a;
-        sm.cur = cur;
-        sm.nexcl = nexcl;
+        // the final node's children were all rejected: their distinct tokens, in row order
+        int nexcl = 0;
+        for (int j0 = cur + 1; good && j0 < n; j0 += 32) {
+          const int j = j0 + lane;
+          bool keep = j < n && sm.par[j] == cur;
+          if (keep) {
+            const int x = sm.tok[j - 1];
+            for (int k = cur + 1; k < j; ++k) keep &= !(sm.par[k] == cur && sm.tok[k - 1] == x);
+          }
+          const unsigned m = __ballot_sync(0xffffffffu, keep);
+          if (keep) sm.excl[nexcl + __popc(m & ((1u << lane) - 1u))] = sm.tok[j - 1];
+          nexcl += __popc(m);
+        }
+        if (lane == 0) {
+          sm.a = a;
+          sm.cur = cur;
+          sm.nexcl = nexcl;
+        }
       }
     } else {
     // ---------------- accept scan (identical in every CTA): one lane per draft, first rejection by ballot ----------------
