@@ -242,7 +242,9 @@ def run_native(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    steps_total = args.steps + args.warmup + 2
+    # every step this run takes (warm-up, the timed pass, the per-call pass, the path timings, the
+    # end-to-end leg): each keeps at most K + 1 = 6 tokens a sequence, and the cache is sized for it
+    steps_total = args.warmup + 2 * args.steps + 2 + max(3, args.warmup) + max(10, args.steps // 2) + 2
     case, desc = make_case(args.config, args.temperature, steps_total, seed_offset=rank)
     st, sp = case.state, case.step
     G = sp.num_q_heads // st.num_kv_heads
@@ -273,7 +275,9 @@ def run_native(args):
     assert int(buf.status.item()) == 0, "device status set during warm-up"
     start_lens = kv.seq_lens.clone()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # the timed pass: K steps back to back, nothing recorded between the calls (an event
+    # between two kernels ends the programmatic dependent launch that lets each kernel's
+    # start overlap the previous one's end)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = Clocks(local, not args.no_clocks and rank == 0)
     if world > 1:
@@ -281,7 +285,7 @@ def run_native(args):
     torch.cuda.synchronize()
     t_start.record(stream)
     for s in range(args.steps):
-        one_step(evs[s])
+        one_step()
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -289,18 +293,25 @@ def run_native(args):
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
     assert int(buf.status.item()) == 0, "device status set during the timed steps"
-    attn_ms = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
-    samp_ms = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
-
     end_lens = kv.seq_lens.cpu().numpy().astype(np.int64)
     sl = start_lens.cpu().numpy().astype(np.int64)
     per_step_keep = (end_lens - sl) // args.steps  # a_b + 1, identical every step
     emitted = int((end_lens - sl).sum())
+
+    # the per-call pass: K more steps with events around the attention and sampler calls
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for s in range(args.steps):
+        one_step(evs[s])
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0, "device status set during the per-call steps"
+    attn_ms = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
+    samp_ms = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
+    sl_b = end_lens
     # attention bytes, exactly, step by step: c_b(s) = c_b(start) + s * (a_b + 1)
     ab = 0
     fl = 0.0
     for s in range(args.steps):
-        ctx = sl + s * per_step_keep
+        ctx = sl_b + s * per_step_keep
         ab += attn_bytes(ctx + sp.n_q, sp, st)
         fl += attn_flops(ctx, sp, G)
     attn_bytes_avg = ab / args.steps
@@ -323,7 +334,10 @@ def run_native(args):
         "data": "synthetic (seeded numpy PCG64; no dataset or weights)",
         "config": {"workload": desc, "global_batch": B * world, "scored_tokens_per_step": sp.total_q,
                    "l2": "inputs larger than L2: each step streams the whole KV prefix (>300 MB) and the "
-                         "logits; L2 is 129 MB", "state": "cache evolves across steps (a_b+1 tokens kept)"},
+                         "logits; L2 is 129 MB", "state": "cache evolves across steps (a_b+1 tokens kept)",
+                   "timing": "value: K steps with nothing recorded between the calls; roofline and "
+                             "sampler_roofline per-call times: K further steps with CUDA events around "
+                             "each call (the events cut the programmatic overlap between kernels)"},
         "tokens_per_s": emitted * world / (elapsed_ms / 1e3),
         "scored_tokens_per_s": sp.total_q * args.steps * world / (elapsed_ms / 1e3),
         "mean_tokens_per_seq_step": emitted / (B * args.steps),
@@ -598,6 +612,7 @@ def run_e2e(args, kv, d, buf, msl, sp, dev, stream, world):
         step_e2e()
     b.record(stream)
     torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0, "device status set during the end-to-end steps"
     ms = a.elapsed_time(b)
     t = torch.tensor([ms], dtype=torch.float64, device=dev)
     if world > 1:
