@@ -188,8 +188,8 @@ __device__ __forceinline__ void group8(const T *buf, int g, int n, float (&x)[kG
 
 // ===========================================================================
 // Row statistics: every target row (and, for T > 0, every draft row) cut into
-// items of 32 KB, the items of the launch cut into equal contiguous ranges,
-// one per CTA. A producer warp streams a CTA's items through a 3-stage ring of
+// items of 32 KB, the items of the launch cut into contiguous ranges that
+// differ by one item at most, one per CTA. A producer warp streams a CTA's items through a 3-stage ring of
 // 1-D bulk copies; eight consumer warps each reduce an eighth of every item.
 // A lane keeps a running (max, sum of 2^(x c - max c)) or argmax of the
 // current row; where a warp's run of items leaves a row the warp reduces it and
@@ -201,7 +201,7 @@ struct StatsArgs {
   const void *tgt, *drf;
   float *pm, *ps;  // [items][kStatWarps]: max (or best value), sum (or best index bits)
   int32_t *status;
-  int vocab, total_q, rows, nchunk, items, per;
+  int vocab, total_q, rows, nchunk, items, per, extra;  // CTA c: per items, one more when c < extra
   float coef;
 };
 
@@ -214,7 +214,8 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
   extern __shared__ __align__(128) uint8_t ring[];  // kStatStages x kPartBytes
   __shared__ uint64_t full[kStatStages], empty[kStatStages];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i0 = blockIdx.x * A.per, i1 = min(A.items, i0 + A.per);
+  const int i0 = blockIdx.x * A.per + min((int)blockIdx.x, A.extra);
+  const int i1 = min(A.items, i0 + A.per + ((int)blockIdx.x < A.extra ? 1 : 0));
   const int V = A.vocab;
   const T *tgt = reinterpret_cast<const T *>(A.tgt);
   const T *drf = reinterpret_cast<const T *>(A.drf);
@@ -1043,9 +1044,11 @@ template <typename T, bool VEC, int MODE>
 cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int rows, cudaStream_t st) {
   // ---- statistics ----
   const int items = rows * nchunk;
-  const int want = std::max(1, std::min(items, 2 * num_sms()));
-  const int per = (items + want - 1) / want;
-  const int grid = (items + per - 1) / per;
+  // every CTA of the launch takes floor(items / grid) items, the first (items mod grid) one
+  // more: the CTAs of one SM (c and c + SMs when the blocks go round the SMs) differ by one
+  // item at most
+  const int grid = std::max(1, std::min(items, 2 * num_sms()));
+  const int per = items / grid, extra = items - per * grid;
   StatsArgs sa;
   sa.tgt = a.tgt;
   sa.drf = a.drf;
@@ -1058,6 +1061,7 @@ cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int
   sa.nchunk = nchunk;
   sa.items = items;
   sa.per = per;
+  sa.extra = extra;
   sa.coef = a.coef;
   constexpr int SMODE = MODE == kTreeStochastic ? kStochastic : MODE;  // statistics of the target rows
   auto skern = stats_kernel<T, VEC, SMODE>;
