@@ -306,6 +306,9 @@ def run_native(args):
     assert int(buf.status.item()) == 0, "device status set during the per-call steps"
     attn_ms = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
     samp_ms = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
+    # near-ties of the last step's decisions (every step takes the same ones): sequences whose
+    # smallest |uniform - threshold| is below 1e-4 (+inf at T = 0 or for greedy trees)
+    near_ties = int((buf.margin < 1e-4).sum().item()) if sp.temperature > 0 else 0
     sl_b = end_lens
     # attention bytes, exactly, step by step: c_b(s) = c_b(start) + s * (a_b + 1)
     ab = 0
@@ -353,6 +356,8 @@ def run_native(args):
                              "unit": "GB/s", "frac": sampler_bytes(sp) / (samp_ms_avg / 1e3) / 1e9 / hbm_peak,
                              "algorithmic_bytes_per_launch": sampler_bytes(sp), "avg_launch_ms": samp_ms_avg},
         "hbm_gbs_step": (attn_bytes_avg + sampler_bytes(sp)) / (elapsed_ms / args.steps / 1e3) / 1e9,
+        "near_ties": {"sequences_per_step": near_ties, "of": B, "threshold": 1e-4,
+                      "note": "sampler margin output: decisions within 1e-4 of their threshold"},
         "attn_paths_ms": paths,
         "gpu_launches": S.launches_per_step(d, msl, kv) * args.steps,
         "clocks": clk,

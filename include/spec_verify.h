@@ -263,6 +263,15 @@ sv_status sv_spec_verify_attn_no_alloc(const sv_paged_kv *kv, const void *q, voi
  *   accept_count   int32 [batch] out: a_b
  *   out_tokens     int32 [batch, max_q_per_seq] out: x_1..x_a, y, then -1
  *   num_out        int32 [batch] out: a_b + 1
+ *   margin         float [batch] out, or NULL: the smallest distance, over
+ *                  the comparisons that decided the sequence, between a
+ *                  uniform and the threshold it was compared with:
+ *                  |u - min(1, p/q)| for each draft tested, and for the draw
+ *                  the distance of u' from the chosen token's interval edges
+ *                  on the normalised CDF (from the fixed-point sums; 0 when
+ *                  rounding left no crossing); +inf at T = 0. Below 1e-4 it
+ *                  marks a near-tie, where the fp32 decision may differ from
+ *                  an exact one.
  *   workspace      device scratch of at least
  *                  sv_spec_rejection_sample_workspace_bytes(...) bytes,
  *                  256-byte aligned, owned by the caller; its contents need no
@@ -279,8 +288,8 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
                                    int32_t vocab, int32_t batch, const int32_t *cu_q, int32_t total_q,
                                    int32_t max_q_per_seq, const int32_t *draft_tokens, const float *u_accept,
                                    const float *u_resample, float temperature, int32_t *accept_count,
-                                   int32_t *out_tokens, int32_t *num_out, void *workspace, size_t workspace_bytes,
-                                   int32_t *status_dev, void *stream);
+                                   int32_t *out_tokens, int32_t *num_out, float *margin, void *workspace,
+                                   size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /*
  * Workspace bytes of sv_spec_rejection_sample for these sizes (temperature 0:
@@ -330,8 +339,10 @@ sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype,
  * as p at its position. Node rows are in BFS order (parent row < row), else
  * SV_ERR_BAD_LENGTH.
  *   arguments and outputs as sv_tree_greedy_accept, plus u_accept (float
- *   [total_q - batch]) and u_resample (float [batch]) in [0, 1); the workspace
- *   is sized with sv_spec_rejection_sample_workspace_bytes(..., temperature 0)
+ *   [total_q - batch]) and u_resample (float [batch]) in [0, 1), and margin
+ *   (float [batch] out, or NULL) as for sv_spec_rejection_sample (each child
+ *   tested against p'(x), then the draw; +inf at T = 0); the workspace is
+ *   sized with sv_spec_rejection_sample_workspace_bytes(..., temperature 0)
  *   (target rows only); no draft logits are read.
  * Arithmetic as sv_spec_rejection_sample: p'(x) in fp32 from the row
  * statistics, the draw exact in 64-bit fixed point.
@@ -340,8 +351,8 @@ sv_status sv_tree_rejection_sample(const void *target_logits, int32_t logits_dty
                                    const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq,
                                    const int32_t *node_tokens, const int32_t *parent, const float *u_accept,
                                    const float *u_resample, float temperature, int32_t *accept_count,
-                                   int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, void *workspace,
-                                   size_t workspace_bytes, int32_t *status_dev, void *stream);
+                                   int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, float *margin,
+                                   void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /*
  * sv_kv_rollback -- keep each sequence's accepted prefix, give back the rest.

@@ -91,9 +91,9 @@ def load(path: Optional[str] = None, build_if_missing: bool = True) -> ctypes.CD
             "sv_spec_verify_attn": (I, [KVP, P, P, P, I, I, I, I, F, I, P, P, S, P, P]),
             "sv_spec_verify_attn_no_alloc": (I, [KVP, P, P, P, I, I, I, I, F, I, P, P, P]),
             "sv_spec_rejection_sample_workspace_bytes": (S, [I, I, I, I, F]),
-            "sv_spec_rejection_sample": (I, [P, P, I, I, I, P, I, I, P, P, P, F, P, P, P, P, S, P, P]),
+            "sv_spec_rejection_sample": (I, [P, P, I, I, I, P, I, I, P, P, P, F, P, P, P, P, P, S, P, P]),
             "sv_tree_greedy_accept": (I, [P, I, I, I, P, I, I, P, P, P, P, P, P, P, S, P, P]),
-            "sv_tree_rejection_sample": (I, [P, I, I, I, P, I, I, P, P, P, P, F, P, P, P, P, P, S, P, P]),
+            "sv_tree_rejection_sample": (I, [P, I, I, I, P, I, I, P, P, P, P, F, P, P, P, P, P, P, S, P, P]),
             "sv_kv_rollback": (I, [KVP, P, P, P, I, P, P]),
             "sv_kv_fork": (I, [KVP, P, P, I, P, P]),
             "sv_kv_release": (I, [KVP, P, I, P, P]),
@@ -249,14 +249,15 @@ def spec_rejection_sample(target_logits: torch.Tensor, draft_logits: Optional[to
                           draft_tokens: Optional[torch.Tensor], u_accept: Optional[torch.Tensor],
                           u_resample: Optional[torch.Tensor], temperature: float, accept_count: torch.Tensor,
                           out_tokens: torch.Tensor, num_out: torch.Tensor, *, workspace: Optional[torch.Tensor] = None,
-                          status: Optional[torch.Tensor] = None, stream=None) -> None:
+                          status: Optional[torch.Tensor] = None, margin: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
     batch = int(cu_q.shape[0]) - 1
     ws, ws_bytes = _sampler_workspace(workspace, target_logits, batch, temperature)
     _check(load().sv_spec_rejection_sample(
         _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), int(target_logits.shape[1]), batch,
         _ptr(cu_q), int(target_logits.shape[0]), int(out_tokens.shape[1]), _ptr(draft_tokens), _ptr(u_accept),
-        _ptr(u_resample), float(temperature), _ptr(accept_count), _ptr(out_tokens), _ptr(num_out), _ptr(ws),
-        ws_bytes, _ptr(status), _stream(stream)), "sv_spec_rejection_sample")
+        _ptr(u_resample), float(temperature), _ptr(accept_count), _ptr(out_tokens), _ptr(num_out), _ptr(margin),
+        _ptr(ws), ws_bytes, _ptr(status), _stream(stream)), "sv_spec_rejection_sample")
 
 
 def tree_greedy_accept(target_logits: torch.Tensor, cu_q: torch.Tensor, node_tokens: torch.Tensor,
@@ -276,7 +277,8 @@ def tree_rejection_sample(target_logits: torch.Tensor, cu_q: torch.Tensor, node_
                           parent: torch.Tensor, u_accept: torch.Tensor, u_resample: torch.Tensor, temperature: float,
                           accept_count: torch.Tensor, path_nodes: torch.Tensor, out_tokens: torch.Tensor,
                           num_out: torch.Tensor, *, workspace: Optional[torch.Tensor] = None,
-                          status: Optional[torch.Tensor] = None, stream=None) -> None:
+                          status: Optional[torch.Tensor] = None, margin: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
     """Lossless tree verification at T > 0 (children as point-mass proposals)."""
     batch = int(cu_q.shape[0]) - 1
     ws, ws_bytes = _sampler_workspace(workspace, target_logits, batch, 0.0)
@@ -284,7 +286,7 @@ def tree_rejection_sample(target_logits: torch.Tensor, cu_q: torch.Tensor, node_
         _ptr(target_logits), _dtype_code(target_logits), int(target_logits.shape[1]), batch, _ptr(cu_q),
         int(target_logits.shape[0]), int(out_tokens.shape[1]), _ptr(node_tokens), _ptr(parent), _ptr(u_accept),
         _ptr(u_resample), float(temperature), _ptr(accept_count), _ptr(path_nodes), _ptr(out_tokens), _ptr(num_out),
-        _ptr(ws), ws_bytes, _ptr(status), _stream(stream)), "sv_tree_rejection_sample")
+        _ptr(margin), _ptr(ws), ws_bytes, _ptr(status), _stream(stream)), "sv_tree_rejection_sample")
 
 
 def kv_rollback(kv: PagedKV, cu_q: torch.Tensor, accept_count: torch.Tensor, status: torch.Tensor, *,

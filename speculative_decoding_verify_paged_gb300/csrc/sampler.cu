@@ -487,6 +487,8 @@ struct Smem {
   long long ll_buf[kWarps];
   long long P_owner, target;
   float rho_hi, rho_lo;
+  float m1, m2;       // margins: of the accept tests, and of the draw's CDF crossing
+  long long Stot;     // the draw's total fixed-point mass
   int a;
   int owner, fallback;
   int y_hit, y_last;
@@ -671,6 +673,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
       o[a] = sm.am[a];
       args.accept[b] = a;
       args.num_out[b] = a + 1;
+      if (args.margin) args.margin[b] = INFINITY;
     }
   } else if constexpr (MODE == kTree) {
     // the walk with one warp: at each node the lanes look for the first child (in row
@@ -711,6 +714,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
         o[a] = sm.am[cur];
         args.accept[b] = a;
         args.num_out[b] = a + 1;
+        if (args.margin) args.margin[b] = INFINITY;
       }
     }
   } else {
@@ -729,6 +733,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
         if (__any_sync(0xffffffffu, nz_l) && rank == 0 && lane == 0) record(args.status, SV_ERR_NONFINITE);
         if (!good && rank == 0 && lane == 0) record(args.status, SV_ERR_BAD_LENGTH);
         int cur = 0, a = 0;
+        float mmin = INFINITY;  // the accept tests' margin
         bool moved = good;
         while (moved) {  // one node per pass; children of cur lie after cur (checked above)
           moved = false;
@@ -749,6 +754,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
               m &= m - 1;
               const float pk = __shfl_sync(0xffffffffu, px, k);
               const float thr = removed < 1.f ? pk / (1.f - removed) : 0.f;
+              mmin = fminf(mmin, fabsf(sm.uacc[j0 + k - 1] - thr));
               if (sm.uacc[j0 + k - 1] < thr) {  // accepted: the walk goes on from this child
                 if (lane == 0) sm.path[a] = j0 + k;
                 ++a;
@@ -777,23 +783,34 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
           sm.a = a;
           sm.cur = cur;
           sm.nexcl = nexcl;
+          sm.m1 = mmin;
         }
       }
     } else {
     // ---------------- accept scan (identical in every CTA): one lane per draft, first rejection by ballot ----------------
     if (warp == 0) {
       unsigned rej[2];
+      float dist[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int i = lane + 32 * h;
         bool r = false;
+        dist[h] = INFINITY;
         if (i < K) {
           const float p = exp2f((sm.gtl[i] - sm.M[i]) * coef) / sm.Z[i];
           const float q = exp2f((sm.gdl[i] - sm.M[n + i]) * coef) / sm.Z[n + i];
           const float thr = q > 0.f ? fminf(1.f, p / q) : 1.f;
           r = !(sm.uacc[i] < thr);
+          dist[h] = fabsf(sm.uacc[i] - thr);
         }
         rej[h] = __ballot_sync(0xffffffffu, r);
+      }
+      {  // the accept tests' margin: the drafts up to the first rejection
+        const int a_all = rej[0] ? __ffs(rej[0]) - 1 : rej[1] ? 31 + __ffs(rej[1]) : K;
+        float m = fminf(lane <= a_all ? dist[0] : INFINITY, lane + 32 <= a_all ? dist[1] : INFINITY);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) sm.m1 = m;
       }
       bool nz = false;
       for (int r = lane; r < rows; r += 32) nz |= !(sm.Z[r] > 0.f);
@@ -955,6 +972,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
             sm.P_owner = -1;
           }
           sm.target = target;
+          sm.Stot = S;
+          sm.m2 = 0.f;  // stays 0 when rounding leaves no crossing
           sm.y_hit = INT_MAX;
           sm.y_last = -1;
         }
@@ -987,6 +1006,9 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
                 c2 += w[k];
                 if (c2 > target) {
                   y = g * kGroup + k;
+                  // distance of u' S from the chosen interval's edges, on the normalised CDF
+                  const long long below = target - (c2 - w[k]), above = c2 - target;
+                  sm.m2 = (float)((double)(below < above ? below : above) / (double)sm.Stot);
                   break;
                 }
               }
@@ -1022,6 +1044,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
           o[a] = y;
           args.accept[b] = a;
           args.num_out[b] = a + 1;
+          if (args.margin) args.margin[b] = fminf(sm.m1, sm.m2);
         }
       }
       break;

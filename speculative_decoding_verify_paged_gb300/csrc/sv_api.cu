@@ -139,7 +139,7 @@ const char *sv_status_string(int32_t status) {
   }
 }
 
-int32_t sv_version(void) { return 30000; }
+int32_t sv_version(void) { return 30100; }
 
 sv_status sv_set_option(int32_t option, int32_t value) {
   if (option == SV_OPT_ATTN_PATH && value >= SV_ATTN_AUTO && value <= SV_ATTN_KEYS_MAJOR) {
@@ -244,8 +244,8 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
                                    int32_t vocab, int32_t batch, const int32_t *cu_q, int32_t total_q,
                                    int32_t max_q_per_seq, const int32_t *draft_tokens, const float *u_accept,
                                    const float *u_resample, float temperature, int32_t *accept_count,
-                                   int32_t *out_tokens, int32_t *num_out, void *workspace, size_t workspace_bytes,
-                                   int32_t *status_dev, void *stream) {
+                                   int32_t *out_tokens, int32_t *num_out, float *margin, void *workspace,
+                                   size_t workspace_bytes, int32_t *status_dev, void *stream) {
   if (logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F32) return SV_ERR_INVALID_ARG;
   if (vocab < 1 || batch < 0 || batch > 65535 || total_q < batch || max_q_per_seq < 1 || max_q_per_seq > kMaxQ)
     return SV_ERR_INVALID_ARG;
@@ -273,6 +273,7 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
   a.accept = accept_count;
   a.out_tok = out_tokens;
   a.num_out = num_out;
+  a.margin = margin;
   a.status = status_dev;
   a.vocab = vocab;
   a.batch = batch;
@@ -286,11 +287,12 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
   return cuda_status(launch_sampler(a, logits_dtype, greedy ? kGreedy : kStochastic, workspace, (cudaStream_t)stream));
 }
 
-sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype, int32_t vocab, int32_t batch,
-                                const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq,
-                                const int32_t *node_tokens, const int32_t *parent, int32_t *accept_count,
-                                int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, void *workspace,
-                                size_t workspace_bytes, int32_t *status_dev, void *stream) {
+namespace {
+sv_status tree_greedy(const void *target_logits, int32_t logits_dtype, int32_t vocab, int32_t batch,
+                      const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq, const int32_t *node_tokens,
+                      const int32_t *parent, int32_t *accept_count, int32_t *path_nodes, int32_t *out_tokens,
+                      int32_t *num_out, float *margin, void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                      void *stream) {
   if (logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F32) return SV_ERR_INVALID_ARG;
   if (vocab < 1 || batch < 0 || batch > 65535 || total_q < batch || max_q_per_seq < 1 || max_q_per_seq > kMaxQ)
     return SV_ERR_INVALID_ARG;
@@ -312,6 +314,7 @@ sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype,
   a.out_tok = out_tokens;
   a.num_out = num_out;
   a.path = path_nodes;
+  a.margin = margin;
   a.status = status_dev;
   a.vocab = vocab;
   a.batch = batch;
@@ -319,17 +322,28 @@ sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype,
   a.total_q = total_q;
   return cuda_status(launch_sampler(a, logits_dtype, kTree, workspace, (cudaStream_t)stream));
 }
+}  // namespace
+
+sv_status sv_tree_greedy_accept(const void *target_logits, int32_t logits_dtype, int32_t vocab, int32_t batch,
+                                const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq,
+                                const int32_t *node_tokens, const int32_t *parent, int32_t *accept_count,
+                                int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, void *workspace,
+                                size_t workspace_bytes, int32_t *status_dev, void *stream) {
+  return tree_greedy(target_logits, logits_dtype, vocab, batch, cu_q, total_q, max_q_per_seq, node_tokens, parent,
+                     accept_count, path_nodes, out_tokens, num_out, nullptr, workspace, workspace_bytes, status_dev,
+                     stream);
+}
 
 sv_status sv_tree_rejection_sample(const void *target_logits, int32_t logits_dtype, int32_t vocab, int32_t batch,
                                    const int32_t *cu_q, int32_t total_q, int32_t max_q_per_seq,
                                    const int32_t *node_tokens, const int32_t *parent, const float *u_accept,
                                    const float *u_resample, float temperature, int32_t *accept_count,
-                                   int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, void *workspace,
-                                   size_t workspace_bytes, int32_t *status_dev, void *stream) {
+                                   int32_t *path_nodes, int32_t *out_tokens, int32_t *num_out, float *margin,
+                                   void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream) {
   if (temperature == 0.f)
-    return sv_tree_greedy_accept(target_logits, logits_dtype, vocab, batch, cu_q, total_q, max_q_per_seq,
-                                 node_tokens, parent, accept_count, path_nodes, out_tokens, num_out, workspace,
-                                 workspace_bytes, status_dev, stream);
+    return tree_greedy(target_logits, logits_dtype, vocab, batch, cu_q, total_q, max_q_per_seq, node_tokens, parent,
+                       accept_count, path_nodes, out_tokens, num_out, margin, workspace, workspace_bytes,
+                       status_dev, stream);
   if (logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F32) return SV_ERR_INVALID_ARG;
   if (vocab < 1 || batch < 0 || batch > 65535 || total_q < batch || max_q_per_seq < 1 || max_q_per_seq > kMaxQ)
     return SV_ERR_INVALID_ARG;
@@ -355,6 +369,7 @@ sv_status sv_tree_rejection_sample(const void *target_logits, int32_t logits_dty
   a.out_tok = out_tokens;
   a.num_out = num_out;
   a.path = path_nodes;
+  a.margin = margin;
   a.status = status_dev;
   a.vocab = vocab;
   a.batch = batch;

@@ -190,6 +190,7 @@ struct SamplerArgs {
   int32_t *out_tok;
   int32_t *num_out;
   int32_t *path;
+  float *margin;  // nullable: per sequence, the smallest |uniform - threshold| of the decisions (+inf greedy)
   int32_t *status;
   int vocab, batch, max_q, chunk, total_q;
   float coef;     // log2(e) / temperature, rounded to fp32

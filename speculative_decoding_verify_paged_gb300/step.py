@@ -113,6 +113,7 @@ class StepBuffers:
     num_out: torch.Tensor
     path: torch.Tensor
     status: torch.Tensor
+    margin: torch.Tensor  # per sequence: the decisions' smallest distance to a threshold (near-ties < 1e-4)
 
     @classmethod
     def make(cls, kv: L.PagedKV, dstep: DeviceStep, max_seq_len: int, device="cuda") -> "StepBuffers":
@@ -129,7 +130,8 @@ class StepBuffers:
             out_tok=torch.empty((B, dstep.max_q), dtype=torch.int32, device=device),
             num_out=torch.empty(B, dtype=torch.int32, device=device),
             path=torch.empty((B, dstep.max_q), dtype=torch.int32, device=device),
-            status=torch.zeros(1, dtype=torch.int32, device=device))
+            status=torch.zeros(1, dtype=torch.int32, device=device),
+            margin=torch.empty(B, dtype=torch.float32, device=device))
 
 
 def append(kv, d: DeviceStep, buf: StepBuffers, stream=None):
@@ -146,7 +148,7 @@ def sample(d: DeviceStep, buf: StepBuffers, stream=None):
     if d.mask_kind == L.SV_MASK_TREE and d.temperature > 0.0:
         L.tree_rejection_sample(d.target_logits, d.cu_q, d.draft_tokens, d.parent, d.u_accept, d.u_resample,
                                 d.temperature, buf.accept, buf.path, buf.out_tok, buf.num_out,
-                                workspace=buf.sampler_ws, status=buf.status, stream=stream)
+                                workspace=buf.sampler_ws, status=buf.status, margin=buf.margin, stream=stream)
     elif d.mask_kind == L.SV_MASK_TREE:
         L.tree_greedy_accept(d.target_logits, d.cu_q, d.draft_tokens, d.parent, buf.accept, buf.path, buf.out_tok,
                              buf.num_out, workspace=buf.sampler_ws, status=buf.status, stream=stream)
@@ -155,7 +157,7 @@ def sample(d: DeviceStep, buf: StepBuffers, stream=None):
         L.spec_rejection_sample(d.target_logits, None if greedy else d.draft_logits, d.cu_q, d.draft_tokens,
                                 None if greedy else d.u_accept, None if greedy else d.u_resample, d.temperature,
                                 buf.accept, buf.out_tok, buf.num_out, workspace=buf.sampler_ws, status=buf.status,
-                                stream=stream)
+                                margin=buf.margin, stream=stream)
 
 
 def rollback(kv, d: DeviceStep, buf: StepBuffers, stream=None):

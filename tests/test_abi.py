@@ -58,9 +58,9 @@ def test_host_validation_without_gpu(lib):
     s.block_size, s.head_dim, s.num_kv_heads, s.num_blocks, s.max_blocks_per_seq = 3, 128, 8, 16, 4
     assert lib.sv_kv_rollback(ctypes.byref(s), None, None, None, 6, None, None) == 1
     assert lib.sv_spec_rejection_sample(None, None, 7, 100, 1, None, 2, 2, None, None, None, 1.0,
-                                        None, None, None, None, 0, None, None) == 1
+                                        None, None, None, None, None, 0, None, None) == 1
     assert lib.sv_spec_rejection_sample(None, None, 0, 100, 1, None, 2, 2, None, None, None, float("nan"),
-                                        None, None, None, None, 0, None, None) == 1
+                                        None, None, None, None, None, 0, None, None) == 1
     # the sampler's workspace: 32 KB items x 8 warps x (max, sum); target (+ draft) rows
     assert lib.sv_spec_rejection_sample_workspace_bytes(0, 128256, 32, 256, 1.0) == (2 * 256 - 32) * 8 * 64
     assert lib.sv_spec_rejection_sample_workspace_bytes(0, 128256, 32, 256, 0.0) == 256 * 8 * 64
@@ -70,7 +70,7 @@ def test_host_validation_without_gpu(lib):
     # a workspace that is missing: refused on the host before anything is read
     fake = ctypes.c_void_p(256)
     assert lib.sv_spec_rejection_sample(fake, fake, 0, 100, 1, fake, 2, 2, fake, fake, fake, 1.0,
-                                        fake, fake, fake, None, 0, None, None) == 10
+                                        fake, fake, fake, None, None, 0, None, None) == 10
     assert lib.sv_tree_greedy_accept(fake, 0, 100, 1, fake, 2, 2, fake, fake, fake, fake, fake, fake,
                                      ctypes.c_void_p(512), 16, None, None) == 10
 

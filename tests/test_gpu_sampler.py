@@ -27,17 +27,38 @@ def _sample(case):
 
 
 def _check(case):
-    got = _sample(case)
+    kv, d, buf = upload(case)
+    buf.margin.fill_(-1.0)
+    S.sample(d, buf)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    got = gpu_sample_result(buf)
     if case.step.mask_kind == "tree" and case.step.temperature > 0:
         ref = oracle.tree_sample(case.step)
         compare_samples(case.step, got, ref)  # near-ties as for chains
+        _check_margins(got, ref, buf.margin.cpu().numpy())
     elif case.step.mask_kind == "tree":
         ref = oracle.tree_greedy(case.step)
         compare_samples(case.step, got, ref, tree=True)
     else:
         ref = oracle.rejection_sample(case.step)
         compare_samples(case.step, got, ref)
+        _check_margins(got, ref, buf.margin.cpu().numpy())
     return got, ref
+
+
+def _check_margins(got, ref, margin):
+    """The kernel's per-sequence margin (smallest |uniform - threshold| of its
+    decisions) against the oracle's fp64 one, where the decisions agree: +inf
+    for greedy, else within 1e-5 (fp32 thresholds, fixed-point CDF)."""
+    acc, tok, num = got
+    same = (acc == ref.accept_cnt) & (num == ref.num_out) & np.all(tok == ref.out_tok, axis=1)
+    assert same.sum() > 0
+    m, r = margin[same].astype(np.float64), ref.margin[same]
+    np.testing.assert_array_equal(np.isinf(m), np.isinf(r))
+    fin = ~np.isinf(r)
+    assert np.all(m[fin] >= 0.0)
+    np.testing.assert_allclose(m[fin], r[fin], rtol=0, atol=1e-5)
 
 
 @pytest.mark.parametrize("T", [1.0, 0.0])
