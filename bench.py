@@ -393,7 +393,8 @@ def tree_sampler_timing(hbm_peak, reps=20):
     (sv_tree_rejection_sample). Device time per call, CUDA events; before each
     call the L2 is emptied of the logits by reading a 256 MB buffer ("read"),
     and, as a second figure, by writing it ("write": the call then also pays for
-    evicting 129 MB of dirty lines); bytes = every target row once."""
+    evicting 129 MB of dirty lines); the median of the reps; bytes = every
+    target row once."""
     import torch
     from speculative_decoding_verify_paged_gb300 import step as S
     from speculative_decoding_verify_paged_gb300 import workloads as W
@@ -419,7 +420,7 @@ def tree_sampler_timing(hbm_peak, reps=20):
                 b.record()
                 torch.cuda.synchronize()
                 ms.append(a.elapsed_time(b))
-            times[how] = float(np.mean(ms))
+            times[how] = float(np.median(ms))  # median: a rep can catch the flush's own tail
         t = times["read"]
         nbytes = case.step.target_logits.shape[0] * case.step.vocab * 2
         out[name] = {"us": t * 1e3, "us_after_dirty_flush": times["write"] * 1e3, "bytes": int(nbytes),
