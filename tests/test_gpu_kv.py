@@ -110,10 +110,12 @@ def test_tree_rollback_compacts_path():
     assert_kv_equal(kv, okv, rows=rows)
 
 
-def test_tree_step_at_temperature():
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_tree_step_at_temperature(kv_dtype):
     """The whole step with a stochastic tree: append, attention, tree rejection
-    sample, rollback with the accepted path, against the oracle."""
-    case = W.tree(batch=4, ctx=1000, vocab=512, temperature=1.0)
+    sample, rollback with the accepted path (the path's rows moved as bf16 rows
+    or as E4M3 codes), against the oracle."""
+    case = W.tree(batch=4, ctx=1000, vocab=512, temperature=1.0, kv_dtype=kv_dtype)
     kv, d, buf = upload(case)
     okv = oracle.OracleKV(case.state)
     c0 = list(okv.seq_lens)
