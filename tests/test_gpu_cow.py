@@ -56,13 +56,14 @@ def _verify(kv, okv, step, msl, attn_seqs):
     _assert_same(kv, okv)
 
 
-def test_parallel_sampling_fork_step_release():
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_parallel_sampling_fork_step_release(kv_dtype):
     seed, P, C = 11, 8, 3
     B = P * (C + 1)
     rng = np.random.default_rng(seed)
     ctx = np.zeros(B, np.int32)
     ctx[:P] = rng.integers(40, 200, size=P)  # partial last blocks (block size 16) in most parents
-    st = W.make_kv_state(seed, ctx, block_size=16, num_kv_heads=8, head_dim=128, dtype="bf16",
+    st = W.make_kv_state(seed, ctx, block_size=16, num_kv_heads=8, head_dim=128, dtype=kv_dtype,
                          growth_tokens=200 + 40, pool_factor=1.2)
     okv = oracle.OracleKV(st)
     okv.enable_sharing()
