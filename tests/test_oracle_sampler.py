@@ -269,3 +269,30 @@ def test_nonfinite_logits_are_an_error():
     step.u_accept[:] = 0.0  # accept position 0 so that row 1 is read
     with pytest.raises(oracle.OracleError):
         oracle.rejection_sample(step)
+
+
+def test_margin_hand_worked():
+    """The margin, worked by hand on four-token rows: the smallest of |u - min(1, p/q)| over the
+    drafts tested and the draw's distance to its interval edges on the normalised CDF."""
+    V = 4
+    p0 = np.array([0.1, 0.2, 0.3, 0.4])
+    q0 = np.array([0.4, 0.3, 0.2, 0.1])
+    p1 = np.array([0.25, 0.25, 0.25, 0.25])
+    dummy = np.zeros((2, 1, 1), np.float32)
+
+    def run(u, ur):
+        step = W.StepInputs(np.array([2], np.int32), np.array([0, 2], np.int32), 1, dummy, dummy, dummy, V, "f32",
+                            np.log(np.array([p0, p1])).astype(np.float32), np.log(np.array([q0])).astype(np.float32),
+                            np.array([0], np.int32), np.array([u], np.float32), np.array([ur], np.float32), 1.0)
+        return oracle.rejection_sample(step)
+
+    # rejected (u = 0.7 against 0.1 / 0.4 = 0.25): residual (0, 0, 0.1, 0.3), u' S = 0.2 falls in
+    # token 3's interval [0.1, 0.4): edges 0.25 and 0.5 of the mass 0.4 away; margin min(0.45, 0.25)
+    r = run(0.7, 0.5)
+    assert r.accept_cnt[0] == 0 and r.out_tok[0, 0] == 3
+    np.testing.assert_allclose(r.margin[0], 0.25, rtol=1e-6)
+    # accepted (u = 0.1 < 0.25, distance 0.15); the bonus draw from p1 at 0.6 lands in token 2's
+    # interval [0.5, 0.75): edges 0.1 and 0.15 away; margin 0.1
+    r = run(0.1, 0.6)
+    assert r.accept_cnt[0] == 1 and list(r.out_tok[0, :2]) == [0, 2]
+    np.testing.assert_allclose(r.margin[0], 0.1, rtol=1e-6)
