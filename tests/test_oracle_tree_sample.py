@@ -127,3 +127,18 @@ def test_certain_and_impossible_children():
     r = oracle.tree_sample(step)
     assert (r.accept_cnt >= 1).all()
     assert (r.path_nodes[:, 0] == 2).all() and (r.out_tok[:, 0] == 5).all()
+
+
+def test_margin_hand_worked():
+    """Root p = (0.1, 0.2, 0.3, 0.4); child 1 carries token 3 (p' = 0.4, u = 0.5: rejected, 0.1
+    away), child 2 token 2 (p' = 0.3 / 0.6 = 0.5, u = 0.42: accepted, 0.08 away); child 2 is a
+    leaf with a uniform row, and u' = 0.3 lands in token 1's interval [0.25, 0.5): 0.05 from its
+    edge. The margin is the smallest of the three, 0.05."""
+    dummy = np.zeros((3, 1, 1), np.float32)
+    tgt = np.log(np.array([[0.1, 0.2, 0.3, 0.4], [0.25] * 4, [0.25] * 4])).astype(np.float32)
+    step = W.StepInputs(np.array([3], np.int32), np.array([0, 3], np.int32), 1, dummy, dummy, dummy, 4, "f32", tgt,
+                        np.zeros((2, 4), np.float32), np.array([3, 2], np.int32), np.array([0.5, 0.42], np.float32),
+                        np.array([0.3], np.float32), 1.0, mask_kind="tree", parent=np.array([-1, 0, 0], np.int32))
+    r = oracle.tree_sample(step)
+    assert r.accept_cnt[0] == 1 and r.path_nodes[0, 0] == 2 and list(r.out_tok[0, :2]) == [2, 1]
+    np.testing.assert_allclose(r.margin[0], 0.05, rtol=1e-6)
