@@ -32,7 +32,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks_aggregate():
     port = _free_port()
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of a process that may hold threads
         out = m.dict()
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
