@@ -12,17 +12,22 @@
 //   Greedy: accept while x_i == argmax p_i; y = argmax p_a.
 //   Tree greedy: walk from the root to the child whose token is the argmax of
 //   the current node's row; y = argmax of the last node's row.
+//   Tree at T > 0: children are point-mass proposals, accepted with p'(x) (p
+//   without the siblings rejected before, renormalised); y drawn from p'.
+//   Optional margin: the smallest |uniform - threshold| of a sequence's
+//   decisions, the draw's included (near-ties below 1e-4).
 //
 // How:
 //   statistics  every row of the batch (target rows, then draft rows) is cut
-//               into 32 KB items; the launch's items are cut into equal
-//               contiguous ranges, one per persistent CTA, so the whole batch
+//               into 32 KB items; the launch's items are cut into contiguous
+//               ranges (one item apart at most), one per persistent CTA, so the whole batch
 //               streams through every SM at once whatever the number of
 //               sequences. A producer warp keeps three items in flight with 1-D
 //               bulk copies; eight consumer warps reduce each item to a
 //               (max, sum of 2^((l - max) log2(e)/T)) pair, or to an argmax,
 //               per warp, into a workspace of per-(item, warp) partials.
-//   decisions   one cluster per sequence (one CTA for greedy and tree). Every
+//   decisions   one cluster per sequence (8 or 16 CTAs; one for greedy and
+//               greedy tree). The tree walks run on one warp. Every
 //               CTA combines its sequence's partials in the same fixed order,
 //               so all CTAs hold identical row statistics and take identical
 //               accept decisions. For T > 0 the row pair of the draw (target
