@@ -224,9 +224,11 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
  * the workspace. The scratch is a static device array of
  * SV_ATTN_NO_ALLOC_SCRATCH_BYTES that every device loading the library holds
  * until the process exits. Sizes whose sv_spec_verify_attn_workspace_bytes
- * exceeds it return SV_ERR_WORKSPACE and launch nothing.
- *   - The first call on each device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ * exceeds it return SV_ERR_WORKSPACE and launch nothing; that check comes
+ * before any other CUDA runtime call of this entry point.
+ *   - The first call on each device that launches work looks up the array's
+ *     device address (with that device current; this may load the library's
+ *     module there); make that first call before any stream capture.
  *   - Every call on a device uses the same array and leaves its contents
  *     behind; nothing in it needs to start at zero, since each value the
  *     kernels read was written earlier in the same call.
@@ -458,7 +460,8 @@ sv_status sv_adaptive_k_current(const void *state, int32_t *k);
 
 /*
  * Process-wide options (no counterpart on the pages; they select between
- * complete implementations of the same operation, for measurement).
+ * complete implementations of the same operation, for measurement, and set
+ * the failure-detection limits).
  *   SV_OPT_ATTN_PATH:
  *     SV_ATTN_AUTO (default): 5th-generation tensor cores (tcgen05, TMEM) for
  *       bf16 and E4M3 caches with head_dim 128 and blocks of 16..256 tokens
@@ -472,10 +475,31 @@ sv_status sv_adaptive_k_current(const void *state, int32_t *k);
  *       on the MMA's M dimension; units of at most 32 query rows, i.e. query
  *       heads per KV head x max_q_per_seq <= 32; bf16 caches), else
  *       SV_ERR_UNSUPPORTED. SV_ATTN_TENSOR_CORES is the query-major one.
+ *   SV_OPT_WAIT_BUDGET_US (value in microseconds, 1000 .. 2000000; default
+ *     500000): how long a pipeline wait (a consumer waiting for the data its
+ *     producer brings, a producer waiting for a free stage) of the tcgen05
+ *     attention kernels and of the sampler's statistics kernel may take before
+ *     the kernel gives up, records SV_ERR_TIMEOUT in the status word and ends.
+ *     A kernel that gives up still waits for the copies and matrix operations
+ *     it has issued (at most 0.5 s each, whatever this option says) before it
+ *     releases its shared memory and tensor memory, so that nothing lands in
+ *     memory it no longer owns. The mma.sync attention kernel
+ *     (SV_ATTN_WARP_MMA) keeps 0.5 s for every wait. A budget shorter than the
+ *     time the memory system needs to deliver a stage makes healthy calls
+ *     fail, hence the 1 ms floor.
+ *   SV_OPT_STALL_FOR_TEST (SV_STALL_NONE, the default; SV_STALL_ATTENTION;
+ *     SV_STALL_SAMPLER): for tests of the failure path only. The producer warp
+ *     of the tensor-core attention kernel, or of the sampler's statistics
+ *     kernel, first waits on a barrier that nothing ever completes, as a
+ *     producer whose data never arrives would; that wait runs out after the
+ *     wait budget, the producer issues nothing, and every pipeline wait of its
+ *     consumers runs out in turn. The call then records SV_ERR_TIMEOUT and its
+ *     outputs are undefined; it faults and traps nothing.
  * Returns SV_ERR_INVALID_ARG for an unknown option or value. Not thread-safe
  * with respect to calls in flight on other host threads.
  */
-typedef enum sv_option { SV_OPT_ATTN_PATH = 1 } sv_option;
+typedef enum sv_option { SV_OPT_ATTN_PATH = 1, SV_OPT_WAIT_BUDGET_US = 2, SV_OPT_STALL_FOR_TEST = 3 } sv_option;
+typedef enum sv_stall { SV_STALL_NONE = 0, SV_STALL_ATTENTION = 1, SV_STALL_SAMPLER = 2 } sv_stall;
 typedef enum sv_attn_path {
   SV_ATTN_AUTO = 0,
   SV_ATTN_CUDA_CORES = 1,

@@ -121,6 +121,24 @@ def set_attn_path(path: str) -> None:
     _check(load().sv_set_option(SV_OPT_ATTN_PATH, ATTN_PATHS[path]), "sv_set_option")
 
 
+SV_OPT_WAIT_BUDGET_US = 2
+SV_OPT_STALL_FOR_TEST = 3
+SV_ERR_TIMEOUT = 5
+STALLS = {"none": 0, "attention": 1, "sampler": 2}
+DEFAULT_WAIT_BUDGET_US = 500_000
+
+
+def set_wait_budget_us(us: int) -> None:
+    """Budget of the kernels' pipeline waits, in microseconds (1000 .. 2000000)."""
+    _check(load().sv_set_option(SV_OPT_WAIT_BUDGET_US, int(us)), "sv_set_option")
+
+
+def set_stall_for_test(which: str) -> None:
+    """Failure-path test hook: "attention" or "sampler" makes that kernel's
+    producer wait on a barrier nothing completes; "none" turns it off."""
+    _check(load().sv_set_option(SV_OPT_STALL_FOR_TEST, STALLS[which]), "sv_set_option")
+
+
 def status_string(code: int) -> str:
     try:
         return load().sv_status_string(int(code)).decode()

@@ -63,7 +63,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
+// budget: the launch's pipeline budget, or kDrainBudgetNs for copies and MMAs already issued
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long budget) {
+  return mbar_wait_bounded(bar, parity, budget);
+}
 // One box of the (64 elements, 8 rows, 2 halves, row groups) view of a pool.
 __device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap *map, int y, uint32_t bar) {
   asm volatile(
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
         }
         const int ks = issued % kKSlots, vs = issued % kVSlots;
         if (issued >= kKSlots)
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&k_empty[ks]), ((issued / kKSlots) - 1) & 1));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&k_empty[ks]), ((issued / kKSlots) - 1) & 1, a.wait_ns));
         if (!ok) break;
         if (lane == 0) {
           const uint32_t fb = smem_u32(&k_full[ks]);
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
         }
         __syncwarp();
         if (issued >= kVSlots)
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&v_empty[vs]), ((issued / kVSlots) - 1) & 1));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&v_empty[vs]), ((issued / kVSlots) - 1) & 1, a.wait_ns));
         if (!ok) break;
         if (lane == 0) {
           const uint32_t fb = smem_u32(&v_full[vs]);
@@ -438,8 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
     int pend = -1;  // P V of tile t - 1 still to issue: -1 none, 0 overwrite O, 1 accumulate
     Piece p;
     auto finish_pv = [&](int u, int mode) -> bool {  // P(u) written and V(u) landed, then P V(u)
-      bool w = mbar_wait(smem_u32(&p_ready[u & 1]), (u >> 1) & 1);
-      if (w) w = mbar_wait(smem_u32(&v_full[u % kVSlots]), (u / kVSlots) & 1);
+      bool w = mbar_wait(smem_u32(&p_ready[u & 1]), (u >> 1) & 1, a.wait_ns);
+      if (w) w = mbar_wait(smem_u32(&v_full[u % kVSlots]), (u / kVSlots) & 1, a.wait_ns);
       if (!__all_sync(0xffffffffu, w)) return false;
       tc_fence_after();
       if (lane == 0) issue_pv(u, mode == 1);
@@ -449,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
     while (ok && walker.next(P, p)) {
       for (int kt = p.kt0; kt < p.kt1; ++kt, ++t) {
         const int ks = t % kKSlots;
-        bool w = mbar_wait(smem_u32(&k_full[ks]), (t / kKSlots) & 1);
-        if (w && kt == p.kt0) w = mbar_wait(smem_u32(&q_ready), piece & 1);
+        bool w = mbar_wait(smem_u32(&k_full[ks]), (t / kKSlots) & 1, a.wait_ns);
+        if (w && kt == p.kt0) w = mbar_wait(smem_u32(&q_ready), piece & 1, a.wait_ns);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         tc_fence_after();
@@ -476,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
     // every MMA issued finishes before TMEM is released
     if (lane == 0) mma_commit(smem_u32(&mma_done));
     __syncwarp();
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&mma_done), 0))) ok = false;
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&mma_done), 0, kDrainBudgetNs))) ok = false;
   } else {
     // ================= softmax: one key per thread, 32 query rows =================
     const int q4 = warp & 3;                           // TMEM lane quarter: keys 32 q4 .. 32 q4 + 31
@@ -529,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
         const bool handoff = kt == cur.kt1 - 1 && has_nxt;
         const int k0 = kt * kTileK;
         const int valid = min(kTileK, ke - k0);
-        bool w = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t & 1]), (t >> 1) & 1));
+        bool w = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t & 1]), (t >> 1) & 1, a.wait_ns));
         tc_fence_after();
         uint32_t sr[kRowsK];
         if (w) {
@@ -537,10 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
           tmem_wait_ld();
         }
         if (w && kt == cur.kt1 - 1 && t >= 1)  // P V(t-1) done before P(t) goes out (o_bar phase, see attn_umma.cu)
-          w = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_bar), (t - 1) & 1));
+          w = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_bar), (t - 1) & 1, a.wait_ns));
         if (w && valid < kTileK) {
           // zero this tile's V rows past the unit's end before P V reads them
-          w = __all_sync(0xffffffffu, mbar_wait(smem_u32(&v_full[t % kVSlots]), (t / kVSlots) & 1));
+          w = __all_sync(0xffffffffu, mbar_wait(smem_u32(&v_full[t % kVSlots]), (t / kVSlots) & 1, a.wait_ns));
           uint8_t *vst = vring + (t % kVSlots) * kTileBytes;
           for (int x = tsoft; w && x < (kTileK - valid) * 16; x += kSoftWarps * 32) {
             const int rr = valid + (x >> 4), ch = x & 15;
@@ -602,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
           for (int r = 0; r < kRowsK; ++r) lsum[r] *= __shfl_sync(0xffffffffu, f, r);
           if (owner) {
             // O row `lane`: wait for P(t-1) V(t-1) (S^T(t) done means P V up to t-2 is)
-            if (!mbar_wait(smem_u32(&o_bar), (t - 1) & 1)) ok = false;
+            if (!mbar_wait(smem_u32(&o_bar), (t - 1) & 1, a.wait_ns)) ok = false;
             tc_fence_after();
 #pragma unroll
             for (int cb = 0; cb < kD / 32; ++cb) {
@@ -645,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
       }
       // ---- end of the piece: wait for its last P V, then write ----
       const int tl = t - 1;
-      const bool w = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_bar), tl & 1));
+      const bool w = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_bar), tl & 1, a.wait_ns));
       tc_fence_after();
       // each row's sum over the warp's keys: lane l ends with row l's (transpose-reduction)
 #pragma unroll
@@ -712,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_keys_kernel(const __grid_con
   tc_fence_after();
   if (sh_err != 0 && warp == 0 && lane == 0) {
     // after a failed wait, let this CTA's copies in flight land before its shared memory is released
-    for (int k = max(0, issued - kKSlots); k < issued; ++k) mbar_wait(smem_u32(&k_full[k % kKSlots]), (k / kKSlots) & 1);
-    for (int k = max(0, issued - kVSlots); k < issued; ++k) mbar_wait(smem_u32(&v_full[k % kVSlots]), (k / kVSlots) & 1);
+    for (int k = max(0, issued - kKSlots); k < issued; ++k) mbar_wait(smem_u32(&k_full[k % kKSlots]), (k / kKSlots) & 1, kDrainBudgetNs);
+    for (int k = max(0, issued - kVSlots); k < issued; ++k) mbar_wait(smem_u32(&v_full[k % kVSlots]), (k / kVSlots) & 1, kDrainBudgetNs);
   }
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }

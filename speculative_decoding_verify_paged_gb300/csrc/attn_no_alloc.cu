@@ -5,9 +5,11 @@
 //
 // The array is SV_ATTN_NO_ALLOC_SCRATCH_BYTES long and lives on every device
 // that loads this library until the process exits. Its device address is
-// looked up once per device, on that device's first call, with the device
-// current (host code cannot hand the array's name to a kernel: on the host it
-// names a stand-in, not device memory).
+// looked up once per device, on the first call there that launches work, with
+// the device current (host code cannot hand the array's name to a kernel: on
+// the host it names a stand-in, not device memory). Sizes are checked before
+// that look-up, so a refused call, or one with nothing to launch, makes no
+// call into the CUDA runtime that could load the module or create a context.
 #include <mutex>
 
 #include "sv_internal.cuh"
@@ -48,11 +50,17 @@ extern "C" sv_status sv_spec_verify_attn_no_alloc(const sv_paged_kv *kv, const v
                                                   int32_t max_q_per_seq, int32_t max_seq_len, float scale,
                                                   int32_t mask_kind, const uint64_t *tree_mask, int32_t *status_dev,
                                                   void *stream) {
+  if (kv == nullptr) return SV_ERR_INVALID_ARG;
+  const size_t need = sv_spec_verify_attn_workspace_bytes(kv, num_q_heads, total_q, max_q_per_seq, max_seq_len);
+  if (need > SV_ATTN_NO_ALLOC_SCRATCH_BYTES) return SV_ERR_WORKSPACE;
+  // invalid sizes (need == 0 then), an empty batch or no scratch needed: the workspace
+  // entry point decides, and launches nothing that would read a workspace
+  if (need == 0 || kv->batch == 0 || total_q == 0)
+    return sv_spec_verify_attn(kv, q, out, cu_q, num_q_heads, total_q, max_q_per_seq, max_seq_len, scale,
+                               mask_kind, tree_mask, nullptr, 0, status_dev, stream);
   void *scratch = nullptr;
   const sv_status s = scratch_address(&scratch);
   if (s != SV_OK) return s;
-  const size_t need = sv_spec_verify_attn_workspace_bytes(kv, num_q_heads, total_q, max_q_per_seq, max_seq_len);
-  if (need > SV_ATTN_NO_ALLOC_SCRATCH_BYTES) return SV_ERR_WORKSPACE;
   return sv_spec_verify_attn(kv, q, out, cu_q, num_q_heads, total_q, max_q_per_seq, max_seq_len, scale, mask_kind,
                              tree_mask, scratch, SV_ATTN_NO_ALLOC_SCRATCH_BYTES, status_dev, stream);
 }

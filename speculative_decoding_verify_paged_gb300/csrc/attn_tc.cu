@@ -67,7 +67,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 // Bounded wait for the phase with the given parity; false after the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
+// This kernel's consumers leave without draining the copies still in flight when a wait gives
+// up, so every wait keeps the long budget kDrainBudgetNs (the pipeline budget option does not
+// apply here): a wait gives up only when a copy has not landed after half a second.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long budget) {
+  return mbar_wait_bounded(bar, parity, budget);
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
     int nxt = load_id(wbase + 32 + lane);
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % kStages;
-      if (t >= kStages && !mbar_wait(smem_u32(&empty[s]), ((t / kStages) - 1) & 1)) {
+      if (t >= kStages && !mbar_wait(smem_u32(&empty[s]), ((t / kStages) - 1) & 1, kDrainBudgetNs)) {
         if (lane == 0) record(a.status, SV_ERR_TIMEOUT);
         break;
       }
@@ -288,7 +293,7 @@ __global__ void __launch_bounds__(kThreads) attn_tc_kernel(const __grid_constant
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % kStages;
-    const bool got = mbar_wait(smem_u32(&full[s]), (t / kStages) & 1);
+    const bool got = mbar_wait(smem_u32(&full[s]), (t / kStages) & 1, kDrainBudgetNs);
     const int kt = kb + t * kTile;
     const int valid = min(kTile, ke - kt);
     uint8_t *kst = stages + s * kStageBytes;

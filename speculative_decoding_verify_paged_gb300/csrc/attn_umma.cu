@@ -96,7 +96,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
+// budget: the launch's pipeline budget, or kDrainBudgetNs for copies and MMAs already issued
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long budget) {
+  return mbar_wait_bounded(bar, parity, budget);
+}
 // One box of an E4M3 pool's (128 codes, rows) view: R rows starting at row y, 128 B each.
 __device__ __forceinline__ void tma_load_codes(uint32_t dst, const CUtensorMap *map, int y, uint32_t bar) {
   asm volatile(
@@ -341,6 +344,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
   const KV &kv = a.kv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = kv.batch;
+  const unsigned long long wns = a.wait_ns;  // budget of the pipeline waits
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -355,7 +359,8 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
   uint64_t *mma_done = q_ready + 1;    // every MMA issued has finished
   uint64_t *cfull = mma_done + 1;      // [kConvStages] F8: operand stage converted
   uint64_t *cempty = cfull + kConvStages;  // [kConvStages] F8: operand stage read by its last MMA
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cempty + kConvStages);
+  uint64_t *stall_bar = cempty + kConvStages;  // failure-path test: a barrier nothing arrives on
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(stall_bar + 1);
   uint64_t *mfull = F8 ? cfull : full;    // the MMA waits on these ...
   uint64_t *mempty = F8 ? cempty : empty;  // ... and frees its stages through these
   __shared__ int sh_scan[kNT / 32];
@@ -378,6 +383,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
     mbar_init(smem_u32(o_bar), 1);
     mbar_init(smem_u32(q_ready), kSoftWarps);
     mbar_init(smem_u32(mma_done), 1);
+    mbar_init(smem_u32(stall_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     sh_first_b = 0;
     sh_first_base = 0;
@@ -444,6 +450,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
     const int bs_shift = __ffs(bs) - 1;
     const uint32_t row_bytes = F8 ? 128u : 256u;  // one key's row of K (or V) as the TMA brings it
     const uint32_t box_bytes = static_cast<uint32_t>(box) * row_bytes;
+    if (a.stall == SV_STALL_ATTENTION) ok = __all_sync(0xffffffffu, wait_on_nothing(smem_u32(stall_bar), wns));
     Piece p;
     while (ok && walker.next(P, p)) {
       const int kb = p.kt0 * kTile, ke = min(p.L, p.kt1 * kTile);
@@ -464,7 +471,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
       int nxt = load_y(wbase + 32 + lane);
       for (int kt = p.kt0; kt < p.kt1; ++kt, ++issued) {
         const int s = issued % kLS;
-        if (issued >= kLS) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), ((issued / kLS) - 1) & 1));
+        if (issued >= kLS) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), ((issued / kLS) - 1) & 1, wns));
         if (!ok) break;
         const int k0 = kt * kTile;
         int ys[kTile / 16];
@@ -530,8 +537,8 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
     while (ok && walker.next(P, p)) {
       for (int kt = p.kt0; kt < p.kt1; ++kt, ++t) {
         const int s = t % kMS;
-        bool w = mbar_wait(smem_u32(&mfull[s]), (t / kMS) & 1);
-        if (w && kt == p.kt0) w = mbar_wait(smem_u32(q_ready), piece & 1);
+        bool w = mbar_wait(smem_u32(&mfull[s]), (t / kMS) & 1, wns);
+        if (w && kt == p.kt0) w = mbar_wait(smem_u32(q_ready), piece & 1, wns);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         tc_fence_after();
@@ -546,7 +553,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
         __syncwarp();
         if (pend >= 0) {
           const int u = t - 1;
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_ready[u & 1]), (u >> 1) & 1));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_ready[u & 1]), (u >> 1) & 1, wns));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) issue_pv(u, pend == 1);
@@ -558,7 +565,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
     }
     if (ok && pend >= 0) {
       const int u = t - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_ready[u & 1]), (u >> 1) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_ready[u & 1]), (u >> 1) & 1, wns));
       if (ok) {
         tc_fence_after();
         if (lane == 0) issue_pv(u, pend == 1);
@@ -568,7 +575,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
     // every MMA issued finishes before TMEM is released
     if (lane == 0) mma_commit(smem_u32(mma_done));
     __syncwarp();
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(mma_done), 0))) ok = false;
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(mma_done), 0, kDrainBudgetNs))) ok = false;
   } else if (warp >= kSoft0 && warp < kSoft0 + kSoftWarps) {
     // ================= softmax, one query row per thread =================
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
@@ -646,7 +653,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
         if (handoff) prefetch_q(nxt);
         const int k0 = kt * kTile;
         const int valid = min(kTile, ke - k0);
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t & 1]), (t >> 1) & 1));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t & 1]), (t >> 1) & 1, wns));
         if (!ok) break;
         tc_fence_after();
         // S(t) was this unit's last product with its Q: the next unit's rows can take its place
@@ -655,7 +662,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
           // last tile of the piece: P(t-1) V(t-1) must be done before P(t) goes out. Here
           // P V(t) cannot have started, so o_bar is in the phase of t-1 or t and the parity
           // wait is unambiguous; the end of the piece then waits for phase t alone.
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_bar), (t - 1) & 1));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_bar), (t - 1) & 1, wns));
           if (!ok) break;
         }
         if (!F8 && valid < kTile) {
@@ -708,7 +715,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
           if (__any_sync(0xffffffffu, move && l_run > 0.f)) {
             // O must be rescaled: wait for P(t-1) V(t-1) (S(t) done means P V up to t-2 is),
             // then scale this lane's row
-            if (!mbar_wait(smem_u32(o_bar), (t - 1) & 1)) ok = false;
+            if (!mbar_wait(smem_u32(o_bar), (t - 1) & 1, wns)) ok = false;
             tc_fence_after();
             const float f = (move && l_run > 0.f) ? exp2f(m_run - mx) : 1.f;
 #pragma unroll
@@ -753,7 +760,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
       // P V(tl-1) finished before P(tl) went out, and P V(tl+1) cannot start before
       // this warp's next p_ready: o_bar is in the phase of tl or tl+1.
       const int tl = t - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_bar), tl & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_bar), tl & 1, wns));
       if (!ok) break;
       tc_fence_after();
       if (warp_live) {
@@ -804,7 +811,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
       const int ke = min(p.L, p.kt1 * kTile);
       for (int kt = p.kt0; kt < p.kt1; ++kt, ++t) {
         const int cs = t % kLS, ms = t % kMS;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[cs]), (t / kLS) & 1));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[cs]), (t / kLS) & 1, wns));
         if (!ok) break;
         const int valid = min(kTile, ke - kt * kTile);
         const uint8_t *src = stages + cs * kCodeStageBytes;
@@ -817,7 +824,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[cs]));  // the codes are in registers: the stage can refill
-        if (t >= kMS) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&cempty[ms]), ((t / kMS) - 1) & 1));
+        if (t >= kMS) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&cempty[ms]), ((t / kMS) - 1) & 1, wns));
         if (!ok) break;
         tc_fence_after();
         uint8_t *dst = mstages + ms * kStageBytes;
@@ -852,7 +859,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
   tc_fence_after();
   if (sh_err != 0 && warp == 0 && lane == 0) {
     // after a failed wait, let this CTA's copies in flight land before its shared memory is released
-    for (int k = max(0, issued - kLS); k < issued; ++k) mbar_wait(smem_u32(&full[k % kLS]), (k / kLS) & 1);
+    for (int k = max(0, issued - kLS); k < issued; ++k) mbar_wait(smem_u32(&full[k % kLS]), (k / kLS) & 1, kDrainBudgetNs);
   }
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
@@ -991,7 +998,7 @@ bool make_map(CUtensorMap *map, void *pool, const KV &kv, int box_rows) {
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 32 * 8;
 static_assert(kCodeStages * kCodeStageBytes + kConvStages * kStageBytes <= kStages * kStageBytes,
               "the E4M3 rings fit the bf16 ring's space");
-static_assert(2 * (kStages > kCodeStages ? kStages : kCodeStages) + 2 * kConvStages + 7 <= 31,
+static_assert(2 * (kStages > kCodeStages ? kStages : kCodeStages) + 2 * kConvStages + 8 <= 31,
               "barriers and the TMEM slot fit 256 B");
 static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "a third CTA per SM would wait for TMEM");
 

@@ -101,11 +101,14 @@ __device__ __forceinline__ void am_combine(float &v, int &i, float v2, int i2) {
 
 // 2^(d * c) for d <= 0 with c = c_hi + c_lo: the product is carried to about
 // 2^-40 before exp2f, so no rounding of c or of d*c shifts all weights alike.
+// A weight below 2^-200 is returned as exactly zero; so is the weight of a
+// -inf logit (and of the -inf padding past a chunk's end) at any temperature,
+// as the statistics kernel gives it (to_fix rounds anything below 2^-41 to 0).
 __device__ __forceinline__ float exp2_acc(float d, float c_hi, float c_lo) {
-  d = fmaxf(d, -200.f);  // -inf logits: 2^(d c) flushes to zero below 2^-126 either way
-  const float xh = d * c_hi;
+  const float xh = d * c_hi;  // -inf for d = -inf
   const float xe = fmaf(d, c_hi, -xh) + d * c_lo;
-  return fast_exp2(xh) * fmaf(xe, 0.69314718055994531f, 1.0f);
+  const float w = fast_exp2(xh) * fmaf(xe, 0.69314718055994531f, 1.0f);  // NaN for d = -inf
+  return xh > -200.f ? w : 0.f;
 }
 
 // Weights in [0, 1] as 64-bit fixed point with 40 fractional bits: sums of up
@@ -208,6 +211,8 @@ struct StatsArgs {
   int32_t *status;
   int vocab, total_q, rows, nchunk, items, per, extra;  // CTA c: per items, one more when c < extra
   float coef;
+  unsigned long long wait_ns;  // budget of the pipeline waits
+  int stall;                   // SV_STALL_SAMPLER: the producer waits on nothing (failure-path test)
 };
 
 template <typename T, bool VEC, int MODE>
@@ -218,6 +223,7 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
   constexpr int SL = CH / kStatWarps;              // elements of a warp's slice
   extern __shared__ __align__(128) uint8_t ring[];  // kStatStages x kPartBytes
   __shared__ uint64_t full[kStatStages], empty[kStatStages];
+  __shared__ uint64_t stall_bar;  // failure-path test: a barrier nothing arrives on
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i0 = blockIdx.x * A.per + min((int)blockIdx.x, A.extra);
   const int i1 = min(A.items, i0 + A.per + ((int)blockIdx.x < A.extra ? 1 : 0));
@@ -233,17 +239,22 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[s])), "r"(kStatWarps)
                    : "memory");
     }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&stall_bar)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   bool ok = true;
+  int issued = 0;  // producer: items whose copies were issued
 
   if (warp == kStatWarps) {
     // ---------------- producer ----------------
     if (VEC && lane == 0) {
-      for (int it = i0, j = 0; it < i1; ++it, ++j) {
+      if (A.stall == SV_STALL_SAMPLER) ok = wait_on_nothing(smem_addr(&stall_bar), A.wait_ns);
+      for (int it = i0, j = 0; ok && it < i1; ++it, ++j) {
         const int s = j % kStatStages;
-        if (j >= kStatStages && !mbar_wait_bounded(smem_addr(&empty[s]), ((j / kStatStages) - 1) & 1)) {
+        // a stage is refilled only after all eight consumer warps read its last item (they stop
+        // arriving once one of their waits gave up, so nothing is copied over a stage in flight)
+        if (j >= kStatStages && !mbar_wait_bounded(smem_addr(&empty[s]), ((j / kStatStages) - 1) & 1, A.wait_ns)) {
           ok = false;
           break;
         }
@@ -256,6 +267,7 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
                          smem_addr(ring + s * kPartBytes)),
                      "l"(row_ptr(r) + e0), "r"(bytes), "r"(smem_addr(&full[s]))
                      : "memory");
+        ++issued;
       }
     }
   } else {
@@ -308,7 +320,7 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
       }
       const T *src;
       if constexpr (VEC) {
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[s]), (j / kStatStages) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[s]), (j / kStatStages) & 1, A.wait_ns));
         src = reinterpret_cast<const T *>(ring + s * kPartBytes);
       } else {
         src = row_ptr(r) + e0;  // rows not 16-byte aligned: scalar loads straight from memory
@@ -452,19 +464,21 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
       }
       if constexpr (VEC) {
         __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty[s])) : "memory");
+        if (lane == 0 && ok)
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty[s])) : "memory");
       }
     }
     if (cur_row >= 0) flush();
     if (bad) record(A.status, SV_ERR_NONFINITE);
     if (!ok) record(A.status, SV_ERR_TIMEOUT);
   }
-  // after a failed wait, let the producer's copies in flight land before shared memory is released
+  // after a failed wait, let the producer's copies in flight land before shared memory is released:
+  // a copy older than the last kStatStages issued was read by every consumer before its stage
+  // was refilled, so only those can still be in flight
   const bool any_fail = __syncthreads_or(!ok);
   if (VEC && any_fail && tid == kStatWarps * 32) {
-    const int n = i1 - i0;
-    for (int j = max(0, n - kStatStages); j < n; ++j)
-      mbar_wait_bounded(smem_addr(&full[j % kStatStages]), (j / kStatStages) & 1);
+    for (int j = max(0, issued - kStatStages); j < issued; ++j)
+      mbar_wait_bounded(smem_addr(&full[j % kStatStages]), (j / kStatStages) & 1, kDrainBudgetNs);
   }
 }
 
@@ -1093,6 +1107,8 @@ cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int
   sa.per = per;
   sa.extra = extra;
   sa.coef = a.coef;
+  sa.wait_ns = a.wait_ns;
+  sa.stall = a.stall;
   constexpr int SMODE = MODE == kTreeStochastic ? kStochastic : MODE;  // statistics of the target rows
   auto skern = stats_kernel<T, VEC, SMODE>;
   const int sdyn = VEC ? kStatStages * kPartBytes : 0;

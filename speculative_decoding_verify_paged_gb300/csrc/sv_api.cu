@@ -56,6 +56,8 @@ namespace {
 constexpr int kMaxQ = 64;
 constexpr int kGranule = 64;
 int g_attn_path = SV_ATTN_AUTO;
+unsigned long long g_wait_ns = kDefaultWaitNs;  // budget of the kernels' pipeline waits
+int g_stall = SV_STALL_NONE;                    // failure-path test hook
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -146,6 +148,14 @@ sv_status sv_set_option(int32_t option, int32_t value) {
     g_attn_path = value;
     return SV_OK;
   }
+  if (option == SV_OPT_WAIT_BUDGET_US && value >= 1000 && value <= 2000000) {
+    g_wait_ns = (unsigned long long)value * 1000ull;
+    return SV_OK;
+  }
+  if (option == SV_OPT_STALL_FOR_TEST && value >= SV_STALL_NONE && value <= SV_STALL_SAMPLER) {
+    g_stall = value;
+    return SV_OK;
+  }
   return SV_ERR_INVALID_ARG;
 }
 
@@ -208,6 +218,8 @@ sv_status sv_spec_verify_attn(const sv_paged_kv *kv, const void *q, void *out, c
   a.max_splits = p.max_splits;
   a.mask_kind = mask_kind;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_ns = g_wait_ns;
+  a.stall = g_stall;
   cudaStream_t st = (cudaStream_t)stream;
   const bool umma_ok = umma_usable(kv, num_q_heads, max_q_per_seq, max_seq_len);
   const bool keys_ok = keys_usable(kv, num_q_heads, max_q_per_seq, max_seq_len);
@@ -279,6 +291,8 @@ sv_status sv_spec_rejection_sample(const void *target_logits, const void *draft_
   a.batch = batch;
   a.max_q = max_q_per_seq;
   a.total_q = total_q;
+  a.wait_ns = g_wait_ns;
+  a.stall = g_stall;
   if (!greedy) {
     const double c = 1.4426950408889634 / (double)temperature;
     a.coef = (float)c;
@@ -320,6 +334,8 @@ sv_status tree_greedy(const void *target_logits, int32_t logits_dtype, int32_t v
   a.batch = batch;
   a.max_q = max_q_per_seq;
   a.total_q = total_q;
+  a.wait_ns = g_wait_ns;
+  a.stall = g_stall;
   return cuda_status(launch_sampler(a, logits_dtype, kTree, workspace, (cudaStream_t)stream));
 }
 }  // namespace
@@ -375,6 +391,8 @@ sv_status sv_tree_rejection_sample(const void *target_logits, int32_t logits_dty
   a.batch = batch;
   a.max_q = max_q_per_seq;
   a.total_q = total_q;
+  a.wait_ns = g_wait_ns;
+  a.stall = g_stall;
   const double c = 1.4426950408889634 / (double)temperature;
   a.coef = (float)c;
   a.coef_lo = (float)(c - (double)a.coef);

@@ -63,10 +63,17 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // ---------------------------------------------------------------------------
 // bounded mbarrier wait: gives up (returns false) once it has waited about
-// kWaitBudgetNs of wall-clock time (globaltimer), so that a kernel whose
-// barrier phase never completes ends within a second instead of spinning on
+// `budget_ns` of wall-clock time (globaltimer), so that a kernel whose
+// barrier phase never completes ends instead of spinning on. Two budgets:
+//  - pipeline waits (a consumer waiting for its producer, a producer for a
+//    free stage) take the launch's budget (sv_set_option SV_OPT_WAIT_BUDGET_US,
+//    0.5 s unless set);
+//  - drain waits (for copies or MMAs this CTA has already issued, before its
+//    shared memory or TMEM is released) always take kDrainBudgetNs, so that
+//    nothing lands in memory the CTA no longer owns, whatever the option says.
 // ---------------------------------------------------------------------------
-constexpr unsigned long long kWaitBudgetNs = 500ull * 1000 * 1000;
+constexpr unsigned long long kDrainBudgetNs = 500ull * 1000 * 1000;
+constexpr unsigned long long kDefaultWaitNs = 500ull * 1000 * 1000;
 
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
@@ -74,7 +81,8 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long budget_ns = kDrainBudgetNs) {
   unsigned long long deadline = 0;
   for (uint32_t i = 0; i < (1u << 30); ++i) {
     uint32_t done;
@@ -86,11 +94,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     if (done) return true;
     if ((i & 63u) == 63u) {
       const unsigned long long now = global_ns();
-      if (deadline == 0) deadline = now + kWaitBudgetNs;
+      if (deadline == 0) deadline = now + budget_ns;
       else if (now > deadline) return false;
     }
   }
   return false;
+}
+
+// The failure-path test hook (sv_set_option SV_OPT_STALL_FOR_TEST): a
+// producer waits, with the pipeline budget, on a barrier of its own that no
+// thread ever arrives on, as a producer would whose data never comes. The wait
+// runs out, so the producer issues nothing and its consumers' waits run out in
+// turn. Returns false (always). `bar` is an initialised mbarrier of count 1.
+__device__ __forceinline__ bool wait_on_nothing(uint32_t bar, unsigned long long budget_ns) {
+  return mbar_wait_bounded(bar, 0, budget_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -145,6 +162,8 @@ struct AttnArgs {
   int num_q_heads, total_q, max_q, max_seq_len, chunk, max_splits;
   int mask_kind;
   float scale_log2;  // scale * log2(e)
+  unsigned long long wait_ns;  // budget of the pipeline waits
+  int stall;                   // failure-path test: SV_STALL_ATTENTION makes the producer wait on nothing
 };
 
 // How the key range of every sequence is split across CTAs.
@@ -195,6 +214,8 @@ struct SamplerArgs {
   int vocab, batch, max_q, chunk, total_q;
   float coef;     // log2(e) / temperature, rounded to fp32
   float coef_lo;  // log2(e) / temperature - coef
+  unsigned long long wait_ns;  // budget of the pipeline waits
+  int stall;                   // failure-path test: SV_STALL_SAMPLER makes the statistics producer wait on nothing
 };
 enum SamplerMode { kStochastic = 0, kGreedy = 1, kTree = 2, kTreeStochastic = 3 };
 // Bytes of the partials workspace: rows (total_q target rows, plus total_q - batch

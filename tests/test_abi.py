@@ -87,3 +87,34 @@ def test_oracle_and_library_share_no_code():
             text = open(path).read()
             assert "speculative_decoding_verify_paged_gb300" not in text, path
             assert "spec_verify.h" not in text, path
+
+
+def test_no_alloc_scratch_size_matches_the_header():
+    """The binding's copy of SV_ATTN_NO_ALLOC_SCRATCH_BYTES is the header's value."""
+    text = open(os.path.join(ROOT, "include", "spec_verify.h")).read()
+    m = re.search(r"#define\s+SV_ATTN_NO_ALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", text)
+    assert m, "SV_ATTN_NO_ALLOC_SCRATCH_BYTES not found in the header"
+    assert L.ATTN_NO_ALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_no_alloc_refusals_on_the_host(lib):
+    """sv_spec_verify_attn_no_alloc checks its arguments before any CUDA call:
+    a NULL cache and an empty batch answer here, where there is no GPU."""
+    assert lib.sv_spec_verify_attn_no_alloc(None, None, None, None, 8, 4, 4, 64, 0.1, 0, None, None, None) == 1
+    s = L.sv_paged_kv()
+    s.num_blocks, s.block_size, s.max_blocks_per_seq, s.num_kv_heads, s.head_dim, s.batch = 16, 16, 4, 2, 128, 0
+    s.k_pool = s.v_pool = 256  # never read: nothing is launched for an empty batch
+    assert lib.sv_spec_verify_attn_no_alloc(ctypes.byref(s), None, None, None, 8, 0, 4, 64, 0.1, 0, None, None,
+                                            None) == 0
+
+
+def test_failure_options_are_checked(lib):
+    """The wait budget takes 1 ms .. 2 s (in microseconds); the stall hook three values."""
+    for bad in (0, 999, 2_000_001, -5):
+        assert lib.sv_set_option(L.SV_OPT_WAIT_BUDGET_US, bad) == L.SV_ERR_INVALID_ARG
+    assert lib.sv_set_option(L.SV_OPT_STALL_FOR_TEST, 3) == L.SV_ERR_INVALID_ARG
+    assert lib.sv_set_option(L.SV_OPT_STALL_FOR_TEST, -1) == L.SV_ERR_INVALID_ARG
+    assert lib.sv_set_option(99, 0) == L.SV_ERR_INVALID_ARG
+    assert lib.sv_set_option(L.SV_OPT_WAIT_BUDGET_US, 1000) == 0
+    assert lib.sv_set_option(L.SV_OPT_WAIT_BUDGET_US, L.DEFAULT_WAIT_BUDGET_US) == 0
+    assert lib.sv_set_option(L.SV_OPT_STALL_FOR_TEST, 0) == 0

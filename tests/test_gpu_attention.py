@@ -2,9 +2,11 @@
 
 Bar: max-abs error <= 1e-2 * max|out| for bf16 KV with fp32 accumulation
 (the stated tolerance), 1e-4 for fp32 KV. Small cases are compared in full
-(several key tiles, several splits, ragged tails, every block size); the
-full-size workloads are compared on sampled sequences in the launch
-configuration the benchmark uses.
+(several key tiles, several splits, ragged tails, every block size); so are
+the full-size workloads, every query row of every sequence, in the launch
+configuration the benchmark uses: the persistent kernel's split of the key
+tiles (and so which units two CTAs share and merge) depends on the whole
+batch, so a sample of sequences could miss a wrong merge.
 """
 import numpy as np
 import pytest
@@ -135,24 +137,38 @@ def test_tree_small(path):
     _run(case, path=path)
 
 
-@pytest.mark.parametrize("name,seqs,path", [("llama8b", [0, 5, 17, 31], "auto"),
-                                            ("llama8b", [2, 9, 26], "keys_major"),
-                                            ("llama8b", [3, 30], "cuda_cores"),
-                                            ("llama8b", [1, 20], "warp_mma"),
-                                            ("llama70b", [0, 63, 127], "auto")])
-def test_full_size_sampled(name, seqs, path):
-    _run(W.CONFIGS[name](), seqs=seqs, path=path)
+FULL_PATHS = {
+    "llama8b": ["auto", "keys_major", "cuda_cores", "warp_mma"],
+    "llama70b": ["auto", "warp_mma", "cuda_cores"],  # 8 query heads x 5 rows per KV head: too wide for keys-major
+    "contbatch": ["auto"],
+    "tree": ["auto", "warp_mma", "cuda_cores"],
+}
 
 
-def test_contbatch_sampled():
-    case = W.contbatch()
-    lens = case.state.seq_lens
-    seqs = sorted({int(np.argmax(lens)), int(np.argmin(lens)), 7, 128, 255})
-    _run(case, seqs=seqs)
-
-
-def test_tree_full_size_sampled():
-    _run(W.tree(), seqs=[0, 15])
+@pytest.mark.parametrize("name", list(FULL_PATHS))
+def test_full_size_every_sequence(name):
+    """Every query row of every sequence of the full-size workload, on each
+    attention path that covers it; the oracle's reference is computed once."""
+    case = W.CONFIGS[name]()
+    kv, d, buf = upload(case)
+    okv = oracle.OracleKV(case.state)
+    assert okv.append(case.step) is None
+    S.append(kv, d, buf)
+    msl = max_seq_len(case.state, case.step)
+    ref = oracle.paged_attention(okv.as_state(), case.step)
+    del okv
+    for path in FULL_PATHS[name]:
+        L.set_attn_path(path)
+        try:
+            buf.attn_out.fill_(float("nan"))
+            S.attention(kv, d, buf, msl)
+            torch.cuda.synchronize()
+        finally:
+            L.set_attn_path("auto")
+        assert status_of(buf) == 0, path
+        got = attn_as_f64(buf.attn_out)
+        assert np.isfinite(got).all(), f"{path}: rows left unwritten"
+        assert_attn_close(got, ref)
 
 
 def test_bad_block_id_is_reported():

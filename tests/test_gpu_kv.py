@@ -119,22 +119,31 @@ def test_tree_step_at_temperature(kv_dtype):
     kv, d, buf = upload(case)
     okv = oracle.OracleKV(case.state)
     c0 = list(okv.seq_lens)
-    S.run_step(kv, d, buf, max_seq_len(case.state, case.step))
+    msl = max_seq_len(case.state, case.step)
+    S.append(kv, d, buf)
+    S.attention(kv, d, buf, msl)
+    S.sample(d, buf)
     okv.append(case.step)
     ref = oracle.tree_sample(case.step)
     torch.cuda.synchronize()
     assert status_of(buf) == 0
     got = gpu_sample_result(buf)
-    compare_samples(case.step, got, ref)
-    if np.array_equal(got[0], ref.accept_cnt):
-        np.testing.assert_array_equal(buf.path.cpu().numpy(), ref.path_nodes)
-        okv.rollback(case.step, ref.accept_cnt, path_nodes=ref.path_nodes)
-        rows = []
-        for b in range(case.state.batch):
-            for j in range(ref.accept_cnt[b] + 1):
-                pos = c0[b] + j
-                rows.append((okv.bt[b][pos // okv.bs], pos % okv.bs))
-        assert_kv_equal(kv, okv, rows=rows)
+    compare_samples(case.step, got, ref)  # a divergence only at a flagged near-tie
+    same = got[0] == ref.accept_cnt
+    np.testing.assert_array_equal(buf.path.cpu().numpy()[same], ref.path_nodes[same])
+    if not same.all():  # the rollback then takes the oracle's decisions, so the caches stay comparable
+        buf.accept.copy_(torch.from_numpy(ref.accept_cnt))
+        buf.path.copy_(torch.from_numpy(ref.path_nodes))
+    S.rollback(kv, d, buf)
+    okv.rollback(case.step, ref.accept_cnt, path_nodes=ref.path_nodes)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    rows = []
+    for b in range(case.state.batch):
+        for j in range(ref.accept_cnt[b] + 1):
+            pos = c0[b] + j
+            rows.append((okv.bt[b][pos // okv.bs], pos % okv.bs))
+    assert_kv_equal(kv, okv, rows=rows)
 
 
 def test_out_of_blocks_is_all_or_nothing():

@@ -66,7 +66,7 @@ def test_tiny(T):
     _check(W.tiny(temperature=T))
 
 
-@pytest.mark.parametrize("name,T", [("llama8b", 1.0), ("llama8b", 0.0), ("llama70b", 1.0)])
+@pytest.mark.parametrize("name,T", [("llama8b", 1.0), ("llama8b", 0.0), ("llama70b", 1.0), ("llama70b", 0.0)])
 def test_full_size(name, T):
     _check(W.CONFIGS[name](temperature=T))
 
@@ -142,6 +142,36 @@ def test_vocab_sizes(V, dtype):
     _check(case)
     case.step.temperature = 0.0
     _check(case)
+
+
+@pytest.mark.parametrize("V,dtype", [(1004, "f32"), (1001, "bf16"), (4099, "bf16"), (2052, "f32")])
+def test_high_temperature_with_neg_inf_logits(V, dtype):
+    """T = 10 with -inf logits scattered over target and draft rows and a
+    vocabulary that is not a multiple of 8 (the last group of a chunk is padded
+    with -inf): a -inf logit has p = 0 (or q = 0), so no emitted token may carry
+    one, every token is < V, and the decisions equal the oracle's."""
+    case = W.custom(61, batch=24, ctx_lens=[4] * 24, n_q=[1, 2, 3, 6] * 6, num_q_heads=1, num_kv_heads=1,
+                    head_dim=8, block_size=16, vocab=V, dtype=dtype, temperature=10.0, target_sigma=2.0,
+                    draft_coef=0.8, draft_sigma=1.0, use_bank=False)
+    sp = case.step
+    rng = np.random.default_rng(62)
+    ninf = np.uint16(0xFF80) if dtype == "bf16" else np.float32(-np.inf)
+    tgt, drf = sp.target_logits.copy(), sp.draft_logits.copy()
+    for rows in (tgt, drf):
+        hit = rng.random(rows.shape) < 0.3  # 30% of each row is -inf
+        hit[:, 0] = False  # every row keeps a finite logit
+        rows[hit] = ninf
+    sp.target_logits, sp.draft_logits = tgt, drf
+    # the draft model's tokens, drawn again from the draft rows that now hold -inf
+    drf_f = W.bf16_bits_to_f32(drf) if dtype == "bf16" else drf
+    sp.draft_tokens = W._draft_sample(np.random.default_rng(63), drf_f, sp.temperature)
+    got, ref = _check(case)
+    acc, tok, num = got
+    tgt_f = W.bf16_bits_to_f32(tgt) if dtype == "bf16" else tgt
+    for b in range(case.state.batch):
+        y = int(tok[b][acc[b]])
+        assert 0 <= y < V
+        assert np.isfinite(tgt_f[sp.cu_q[b] + acc[b], y]), f"sequence {b} emitted token {y} with p = 0"
 
 
 def test_temperature_half():

@@ -3,7 +3,8 @@ workload (256 sequences, lognormal contexts, K_b ~ U{2..8} redrawn every
 iteration, 128-token blocks from a fragmented free list) runs 10 iterations of
 append -> attention -> rejection sample -> rollback on the GPU and in the
 oracle. Block tables, seq_lens, the free list and every emitted token must be
-bit-exact at every iteration; attention is compared on sampled sequences.
+bit-exact at every iteration; attention is compared on every sequence at the
+first and the last iteration.
 
 A decision may differ from the oracle only at an oracle-flagged near-tie, and
 such divergences, counted over the whole run, must stay below 0.01% of the
@@ -19,7 +20,7 @@ from speculative_decoding_verify_paged_gb300 import step as S
 from speculative_decoding_verify_paged_gb300 import workloads as W
 
 from _helpers import (MAX_TIE_FRACTION, assert_attn_close, assert_kv_equal, attn_as_f64, compare_samples,
-                      gpu_sample_result, rows_of, status_of)
+                      gpu_sample_result, rows_of, status_of, upload)
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +43,7 @@ def _loop(case, iterations, steps_of, attn_check_iters, attn_seqs, with_pools, o
         if it in attn_check_iters:
             torch.cuda.synchronize()
             ref = oracle.paged_attention(okv.as_state(), step, seqs=attn_seqs)
-            assert_attn_close(attn_as_f64(buf.attn_out), ref, rows_of(step, attn_seqs))
+            assert_attn_close(attn_as_f64(buf.attn_out), ref, None if attn_seqs is None else rows_of(step, attn_seqs))
         ref = oracle.rejection_sample(step)
         got = gpu_sample_result(buf)
         diverged += compare_samples(step, got, ref, max_fraction=None)
@@ -66,9 +67,7 @@ def test_contbatch_ten_iterations():
     sig = case.meta["sigma_b"]
     steps = lambda it: case.step if it == 0 else W.contbatch_step(case.seed, it, batch=case.state.batch,
                                                                    vocab=case.step.vocab, sigma_b=sig)
-    lens = case.state.seq_lens
-    seqs = sorted({int(np.argmax(lens)), 3, 200})
-    kv, okv, accepted = _loop(case, W.CONTBATCH_ITERS, steps, {0, W.CONTBATCH_ITERS - 1}, seqs, with_pools=True)
+    kv, okv, accepted = _loop(case, W.CONTBATCH_ITERS, steps, {0, W.CONTBATCH_ITERS - 1}, None, with_pools=True)
     # acceptance spreads with the per-sequence draft noise
     rate = np.mean(np.stack(accepted), axis=0)
     assert rate[sig < 1.0].mean() > rate[sig > 2.5].mean()
@@ -122,3 +121,44 @@ def test_contbatch_adaptive_k():
     ks = np.stack(ks)
     assert (ks[:10] == 4).all()  # nothing moves before ten rates are held
     assert len(set(ks[-1].tolist())) > 1  # then low- and high-noise drafts part ways
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_tree_full_size_step(T):
+    """The draft-tree workload at full size (16 sequences of 8192 tokens in
+    64-token blocks, 61 rows per sequence): append, tree attention on every row,
+    the tree sampler (greedy walk, or the lossless tree rule at T = 1), and the
+    rollback that moves the accepted path's rows into place. Block tables,
+    lengths, the free list, the emitted tokens, the path and the compacted rows
+    must equal the oracle's."""
+    case = W.tree(temperature=T)
+    st, sp = case.state, case.step
+    kv, d, buf = upload(case)
+    okv = oracle.OracleKV(st)
+    c0 = list(okv.seq_lens)
+    msl = int((st.seq_lens + sp.n_q).max())
+    S.append(kv, d, buf)
+    S.attention(kv, d, buf, msl)
+    S.sample(d, buf)
+    assert okv.append(sp) is None
+    ref_attn = oracle.paged_attention(okv.as_state(), sp)
+    ref = oracle.tree_sample(sp) if T > 0 else oracle.tree_greedy(sp)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    assert_attn_close(attn_as_f64(buf.attn_out), ref_attn)
+    got = gpu_sample_result(buf)
+    compare_samples(sp, got, ref, tree=T == 0.0)
+    path = buf.path.cpu().numpy()
+    same = got[0] == ref.accept_cnt
+    np.testing.assert_array_equal(path[same], ref.path_nodes[same])
+    if not same.all():  # a flagged near-tie (T > 0): the rollback takes the oracle's decisions
+        buf.accept.copy_(torch.from_numpy(ref.accept_cnt))
+        buf.path.copy_(torch.from_numpy(ref.path_nodes))
+    assert ref.accept_cnt.max() >= 1
+    S.rollback(kv, d, buf)
+    okv.rollback(sp, ref.accept_cnt, path_nodes=ref.path_nodes)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    rows = [(okv.bt[b][(c0[b] + j) // okv.bs], (c0[b] + j) % okv.bs)
+            for b in range(st.batch) for j in range(int(ref.accept_cnt[b]) + 1)]
+    assert_kv_equal(kv, okv, rows=rows)
