@@ -6,12 +6,21 @@ spec_rejection_sample -> kv_rollback, four C-ABI calls on one stream.
 Default workload: the Llama-3-8B-shaped batch (32 sequences, contexts
 U[512, 4096], K = 5, 32 q / 8 kv heads of dim 128, bf16 KV in 16-token
 blocks, vocab 128256, T = 1). The cache state evolves from step to step like
-a decode loop (each step keeps a_b + 1 tokens per sequence); the step inputs
-(logits, drafts, uniforms) are the same every step, so every step makes the
-same decisions and the bytes each step reads are known exactly.
+a decode loop (each step keeps a_b + 1 tokens per sequence). Two input sets
+(logits, drafts, uniforms, new rows and queries) alternate from step to step,
+so a step's 92 MB of sampler inputs were last read two steps before, with more
+than 700 MB of other traffic in between (L2: 129 MB). A set's decisions depend
+on its inputs alone, so the tokens each step keeps, and the bytes each step
+reads, are known exactly.
+
+The line also carries `configs`: the same measurements on the other workloads
+(Llama-8B shape greedy, Llama-70B shape at T = 1 and greedy, the
+continuous-batching mix, the draft trees greedy and at T = 1).
 
 Prints one JSON line. `--impl reference` times the fp64 CPU oracle on the
-host cores instead (bounded samples of the same workload).
+host cores instead (bounded samples of the same workload). `--profile
+attention|sampler` runs only that call of the default workload six times (for
+a profiler's capture) and prints nothing else.
 """
 from __future__ import annotations
 
@@ -34,6 +43,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILES = os.path.join(ROOT, "profiles")
 ATTN_SOURCES = ["attn_umma.cu", "sv_internal.cuh"]  # the files that define attn_umma_kernel
+SAMPLER_SOURCES = ["sampler.cu", "sv_internal.cuh"]  # the files that define the sampler's kernels
 
 
 def parse():
@@ -47,6 +57,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-configs", action="store_true")
+    p.add_argument("--profile", choices=["attention", "sampler"], default=None)
     return p.parse_args()
 
 
@@ -69,6 +81,18 @@ def make_case(name, temperature, steps_total, seed_offset=0):
         case = W.tree(seed=5 + seed_offset)
         desc = "tree verify: B=16, ctx 8192, 61 rows (60-node tree), bs64, vocab 32000, greedy"
     return case, desc
+
+
+def second_inputs(name, case, temperature, seed_offset=0):
+    """Another input set of the workload's shapes (the main loop alternates the two);
+    None where the workload has one (the sets of the continuous-batching mix and of
+    the trees differ in shape)."""
+    from speculative_decoding_verify_paged_gb300 import workloads as W
+    if name == "llama8b":
+        return W.llama8b_step(1 + seed_offset, 1, temperature=temperature)
+    if name == "llama70b":
+        return W.llama70b_step(2 + seed_offset, 1, temperature=temperature)
+    return None
 
 
 def attn_bytes(ctx_plus_n, step, state):
@@ -202,16 +226,16 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def attn_traffic_record():
-    """DRAM traffic of the attention kernel from a committed ncu summary, valid
-    only while the kernel sources are unchanged (matching hash)."""
-    path = os.path.join(PROFILES, "attn_traffic.json")
+def traffic_record(name, sources):
+    """A kernel's DRAM traffic from a committed ncu summary, valid only while the
+    kernel's sources are unchanged (matching hash)."""
+    path = os.path.join(PROFILES, name)
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
     h = hashlib.sha256()
-    for name in ATTN_SOURCES:
-        h.update(open(os.path.join(ROOT, "speculative_decoding_verify_paged_gb300", "csrc", name), "rb").read())
+    for src in sources:
+        h.update(open(os.path.join(ROOT, "speculative_decoding_verify_paged_gb300", "csrc", src), "rb").read())
     return rec if rec.get("sources_sha256") == h.hexdigest() else None
 
 
@@ -229,10 +253,95 @@ def aggregate(elapsed_ms: float, seqs_local: int, world: int, device=None):
     return float(n.item()) / (ms / 1e3), ms
 
 
+class StepLoop:
+    """The verify step of one workload on the device, with its input sets: the
+    cache state, one DeviceStep per input set (used in turn), shared buffers,
+    and the tokens each set keeps per sequence (a_b + 1, from a first run: a
+    set's decisions depend on its inputs alone), so that the context lengths,
+    and the bytes every step reads, are known without reading the device."""
+
+    def __init__(self, state, sets, growth, dev):
+        from speculative_decoding_verify_paged_gb300 import step as S
+        self.S = S
+        self.state, self.sets = state, sets
+        self.kv = S.device_kv(state, dev)
+        self.ds = [S.DeviceStep.from_host(x, dev) for x in sets]
+        self.msl = int(max((state.seq_lens + x.n_q).max() for x in sets)) + growth + 16
+        big = max(range(len(sets)), key=lambda k: (sets[k].max_q, sets[k].total_q))
+        self.buf = S.StepBuffers.make(self.kv, self.ds[big], self.msl, dev)
+        self.keep = [None] * len(sets)
+        self.lens = state.seq_lens.astype(np.int64).copy()  # the host's copy of the committed lengths
+        self.count = 0  # steps run
+
+    def step(self, stream, ev=None):
+        """One step with the next input set; `ev` (three events) brackets attention and sampler."""
+        S, k = self.S, self.count % len(self.ds)
+        d, buf = self.ds[k], self.buf
+        S.append(self.kv, d, buf, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        S.attention(self.kv, d, buf, self.msl, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        S.sample(d, buf, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        S.rollback(self.kv, d, buf, stream)
+        self.count += 1
+        return k
+
+    def learn(self, stream):
+        """One step with every set, reading back the tokens each keeps."""
+        import torch
+        for _ in range(len(self.ds)):
+            before = self.kv.seq_lens.clone()
+            k = self.step(stream)
+            torch.cuda.synchronize()
+            assert int(self.buf.status.item()) == 0, "device status set"
+            self.keep[k] = (self.kv.seq_lens - before).cpu().numpy().astype(np.int64)
+            self.lens += self.keep[k]
+
+    def advance(self, k):
+        """The host's lengths after a step of set k; returns the lengths that step started from."""
+        c = self.lens.copy()
+        self.lens += self.keep[k]
+        return c
+
+    def attn_bytes_flops(self, c, k):
+        x = self.sets[k]
+        G = x.num_q_heads // self.state.num_kv_heads
+        return attn_bytes(c + x.n_q, x, self.state), attn_flops(c, x, G)
+
+
+def timed_loop(loop, steps, stream, per_call):
+    """`steps` steps back to back (per_call: with events around attention and the
+    sampler); returns the total ms, the per-call ms lists, and per step the
+    attention bytes and flops, the sampler bytes and the emitted tokens."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)] if per_call else None
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ab, fl, sb, em = [], [], [], []
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for s in range(steps):
+        k = loop.step(stream, evs[s] if per_call else None)
+        c = loop.advance(k)
+        b, f = loop.attn_bytes_flops(c, k)
+        ab.append(b)
+        fl.append(f)
+        sb.append(sampler_bytes(loop.sets[k]))
+        em.append(int(loop.keep[k].sum()))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    assert int(loop.buf.status.item()) == 0, "device status set during the timed steps"
+    attn_ms = [e[0].elapsed_time(e[1]) for e in evs] if per_call else None
+    samp_ms = [e[1].elapsed_time(e[2]) for e in evs] if per_call else None
+    return t0.elapsed_time(t1), attn_ms, samp_ms, ab, fl, sb, em
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
-    from speculative_decoding_verify_paged_gb300 import step as S
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -242,85 +351,59 @@ def run_native(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    # every step this run takes (warm-up, the timed pass, the per-call pass, the path timings, the
-    # end-to-end leg): each keeps at most K + 1 = 6 tokens a sequence, and the cache is sized for it
-    steps_total = args.warmup + 2 * args.steps + 2 + max(3, args.warmup) + max(10, args.steps // 2) + 2
+    # every step this run takes (the learning steps, warm-up, the timed pass, the per-call pass,
+    # the path timings, the end-to-end leg): each keeps at most K + 1 = 6 tokens a sequence,
+    # and the cache is sized for it
+    steps_total = 2 + args.warmup + 2 * args.steps + 2 + max(3, args.warmup) + max(10, args.steps // 2) + 2
     case, desc = make_case(args.config, args.temperature, steps_total, seed_offset=rank)
     st, sp = case.state, case.step
-    G = sp.num_q_heads // st.num_kv_heads
+    second = second_inputs(args.config, case, args.temperature, seed_offset=rank)
+    sets = [sp] if second is None else [sp, second]
     growth = 6 * steps_total if args.config == "llama8b" else 0
-    msl = int((st.seq_lens + sp.n_q).max()) + growth + 16
-
-    kv = S.device_kv(st, dev)
-    d = S.DeviceStep.from_host(sp, dev)
-    buf = S.StepBuffers.make(kv, d, msl, dev)
+    loop = StepLoop(st, sets, growth, dev)
+    kv, d, buf, msl = loop.kv, loop.ds[0], loop.buf, loop.msl
     stream = torch.cuda.current_stream(dev)
-    c0 = kv.seq_lens.clone()
-
-    def one_step(ev=None):
-        S.append(kv, d, buf, stream)
-        if ev is not None:
-            ev[0].record(stream)
-        S.attention(kv, d, buf, msl, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        S.sample(d, buf, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        S.rollback(kv, d, buf, stream)
-
+    loop.learn(stream)
     for _ in range(args.warmup):
-        one_step()
+        loop.advance(loop.step(stream) % len(sets))
     torch.cuda.synchronize()
     assert int(buf.status.item()) == 0, "device status set during warm-up"
-    start_lens = kv.seq_lens.clone()
+
+    if args.profile:
+        # only the one call, six times, on the state the warm-up left (the append of the
+        # attention's rows done once); nothing printed
+        S = loop.S
+        S.append(kv, d, buf, stream)
+        for _ in range(6):
+            if args.profile == "attention":
+                S.attention(kv, d, buf, msl, stream)
+            else:
+                S.sample(d, buf, stream)
+        torch.cuda.synchronize()
+        assert int(buf.status.item()) == 0
+        return
 
     # the timed pass: K steps back to back, nothing recorded between the calls (an event
     # between two kernels ends the programmatic dependent launch that lets each kernel's
     # start overlap the previous one's end)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = Clocks(local, not args.no_clocks and rank == 0)
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for s in range(args.steps):
-        one_step()
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    elapsed_ms, _, _, _, _, sb_t, em_t = timed_loop(loop, args.steps, stream, per_call=False)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    assert int(buf.status.item()) == 0, "device status set during the timed steps"
-    end_lens = kv.seq_lens.cpu().numpy().astype(np.int64)
-    sl = start_lens.cpu().numpy().astype(np.int64)
-    per_step_keep = (end_lens - sl) // args.steps  # a_b + 1, identical every step
-    emitted = int((end_lens - sl).sum())
+    emitted = int(np.sum(em_t))
 
     # the per-call pass: K more steps with events around the attention and sampler calls
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    for s in range(args.steps):
-        one_step(evs[s])
-    torch.cuda.synchronize()
-    assert int(buf.status.item()) == 0, "device status set during the per-call steps"
-    attn_ms = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
-    samp_ms = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
-    # near-ties of the last step's decisions (every step takes the same ones): sequences whose
-    # smallest |uniform - threshold| is below 1e-4 (+inf at T = 0 or for greedy trees)
+    _, attn_ms, samp_ms, ab, fl, sb, _ = timed_loop(loop, args.steps, stream, per_call=True)
+    # near-ties of the last step's decisions: sequences whose smallest |uniform - threshold| is below
+    # 1e-4 (+inf at T = 0 or for greedy trees)
     near_ties = int((buf.margin < 1e-4).sum().item()) if sp.temperature > 0 else 0
-    sl_b = end_lens
-    # attention bytes, exactly, step by step: c_b(s) = c_b(start) + s * (a_b + 1)
-    ab = 0
-    fl = 0.0
-    for s in range(args.steps):
-        ctx = sl_b + s * per_step_keep
-        ab += attn_bytes(ctx + sp.n_q, sp, st)
-        fl += attn_flops(ctx, sp, G)
-    attn_bytes_avg = ab / args.steps
-    attn_bytes_first = attn_bytes(sl + sp.n_q, sp, st)  # the first timed launch (what an ncu capture sees)
+    attn_bytes_avg = float(np.mean(ab))
     attn_ms_avg = float(np.mean(attn_ms))
     samp_ms_avg = float(np.mean(samp_ms))
+    samp_bytes_avg = float(np.mean(sb))
 
     B = st.batch
     value, elapsed_ms = aggregate(elapsed_ms, B * args.steps, world, dev)
@@ -329,15 +412,18 @@ def run_native(args):
     e2e = None if args.no_e2e else run_e2e(args, kv, d, buf, msl, sp, dev, stream, world)
     hbm_peak, peak_kind = peaks()
     achieved = attn_bytes_avg / (attn_ms_avg / 1e3) / 1e9
-    traffic = attn_traffic_record()
+    traffic = traffic_record("attn_traffic.json", ATTN_SOURCES)
+    samp_traffic = traffic_record("sampler_traffic.json", SAMPLER_SOURCES)
     line = {
         "metric": METRIC, "value": value, "unit": "seqs/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if st.dtype == "bf16" else "f32",
         "data": "synthetic (seeded numpy PCG64; no dataset or weights)",
         "config": {"workload": desc, "global_batch": B * world, "scored_tokens_per_step": sp.total_q,
-                   "l2": "inputs larger than L2: each step streams the whole KV prefix (>300 MB) and the "
-                         "logits; L2 is 129 MB", "state": "cache evolves across steps (a_b+1 tokens kept)",
+                   "l2": ("inputs larger than L2 (129 MB): each step streams the whole KV prefix (>300 MB) and "
+                          "the logits; %d input sets alternate, so a step's logits were last read %d steps "
+                          "before" % (len(sets), len(sets))),
+                   "input_sets": len(sets), "state": "cache evolves across steps (a_b+1 tokens kept)",
                    "timing": "value: K steps with nothing recorded between the calls; roofline and "
                              "sampler_roofline per-call times: K further steps with CUDA events around "
                              "each call (the events cut the programmatic overlap between kernels)"},
@@ -348,18 +434,20 @@ def run_native(args):
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS, "peak_source": peak_kind,
                      "traffic": (traffic["traffic_per_algorithmic_byte"] * attn_bytes_avg if traffic else None),
+                     "tensor_pipe_active": traffic.get("tensor_pipe_active_pct") if traffic else None,
                      "algorithmic_bytes_per_launch": attn_bytes_avg, "avg_launch_ms": attn_ms_avg,
-                     "algorithmic_bytes_first_timed_launch": attn_bytes_first,
-                     "tflops": fl / args.steps / (attn_ms_avg / 1e3) / 1e12},
-        "sampler_roofline": {"kernel": "spec_rejection_sample", "bound": "hbm",
-                             "achieved": sampler_bytes(sp) / (samp_ms_avg / 1e3) / 1e9, "peak": hbm_peak,
-                             "unit": "GB/s", "frac": sampler_bytes(sp) / (samp_ms_avg / 1e3) / 1e9 / hbm_peak,
-                             "algorithmic_bytes_per_launch": sampler_bytes(sp), "avg_launch_ms": samp_ms_avg},
-        "hbm_gbs_step": (attn_bytes_avg + sampler_bytes(sp)) / (elapsed_ms / args.steps / 1e3) / 1e9,
+                     "tflops": float(np.mean(fl)) / (attn_ms_avg / 1e3) / 1e12},
+        "sampler_roofline": {"kernel": "spec_rejection_sample (statistics + decisions)", "bound": "hbm",
+                             "achieved": samp_bytes_avg / (samp_ms_avg / 1e3) / 1e9, "peak": hbm_peak,
+                             "unit": "GB/s", "frac": samp_bytes_avg / (samp_ms_avg / 1e3) / 1e9 / hbm_peak,
+                             "traffic": (samp_traffic["traffic_per_algorithmic_byte"] * samp_bytes_avg
+                                         if samp_traffic else None),
+                             "algorithmic_bytes_per_launch": samp_bytes_avg, "avg_launch_ms": samp_ms_avg},
+        "hbm_gbs_step": (float(np.mean(ab)) + float(np.mean(sb_t))) / (elapsed_ms / args.steps / 1e3) / 1e9,
         "near_ties": {"sequences_per_step": near_ties, "of": B, "threshold": 1e-4,
                       "note": "sampler margin output: decisions within 1e-4 of their threshold"},
         "attn_paths_ms": paths,
-        "gpu_launches": S.launches_per_step(d, msl, kv) * args.steps,
+        "gpu_launches": S_launches(loop) * args.steps,
         "clocks": clk,
         "adaptive_k": adaptive_k_timing(),
         "cow": cow_timing(),
@@ -368,23 +456,104 @@ def run_native(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if not args.no_configs and rank == 0:
+        del loop, kv, d, buf
+        torch.cuda.empty_cache()
+        line["configs"] = config_records(hbm_peak, dev, stream)
     if rank == 0 and not args.no_cpu:
-        import oracle
-        cores = os.cpu_count() or 1
-        oracle.set_threads(1)
-        n, t1 = cpu_seqs_for(case, budget_s=10.0)
-        seqs = list(range(n))
-        t_one = oracle_sample_step(case, seqs)
-        used = oracle.set_threads(cores)  # OpenMP over (sequence, KV head) and sequences; same values
-        t_all = oracle_sample_step(case, seqs)
-        line["cpu_baseline"] = {"value": n / t_all, "unit": "seqs/s", "cores": used, "kind": "oracle",
-                                "sample": f"one verify step of {n} of the {B} sequences (fp64 C oracle: append, "
-                                          f"attention, sampler, rollback), {t_all:.1f} s on {used} threads",
-                                "single_thread": {"value": n / t_one, "cores": 1, "seconds": t_one}}
+        line["cpu_baseline"] = cpu_baseline(case, B)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
+
+
+def S_launches(loop):
+    return loop.S.launches_per_step(loop.ds[0], loop.msl, loop.kv)
+
+
+def cpu_baseline(case, B):
+    """The fp64 oracle's verify step on the host cores: a bounded sample of the bench's
+    workload on one thread and on every core, and, per workload, one timed step
+    (the continuous-batching mix: one of its ten iterations, times ten)."""
+    import oracle
+    from speculative_decoding_verify_paged_gb300 import workloads as W
+    cores = os.cpu_count() or 1
+    oracle.set_threads(1)
+    n, t1 = cpu_seqs_for(case, budget_s=10.0)
+    seqs = list(range(n))
+    t_one = oracle_sample_step(case, seqs)
+    used = oracle.set_threads(cores)  # OpenMP over (sequence, KV head) and sequences; same values
+    t_all = oracle_sample_step(case, seqs)
+    out = {"value": n / t_all, "unit": "seqs/s", "cores": used, "kind": "oracle",
+           "sample": f"one verify step of {n} of the {B} sequences (fp64 C oracle: append, "
+                     f"attention, sampler, rollback), {t_all:.1f} s on {used} threads",
+           "single_thread": {"value": n / t_one, "cores": 1, "seconds": t_one}}
+    per = {}
+    for name in ("tiny", "llama8b", "llama70b", "contbatch", "tree"):
+        c = W.CONFIGS[name]()
+        bsz = c.state.batch
+        secs = oracle_sample_step(c, list(range(bsz)))
+        rec = {"seqs_per_s": bsz / secs, "seconds": secs, "sequences": bsz, "threads": used}
+        if name == "contbatch":
+            rec["note"] = ("one iteration timed; the 10-iteration loop extrapolated: %.1f s" % (10 * secs))
+            rec["extrapolated_10_iterations_s"] = 10 * secs
+        per[name] = rec
+        del c
+    out["configs"] = per
+    return out
+
+
+CONFIG_RUNS = (("llama8b", 0.0), ("llama70b", 1.0), ("llama70b", 0.0), ("contbatch", 1.0), ("tree", 0.0),
+               ("tree", 1.0))
+
+
+def config_records(hbm_peak, dev, stream, steps=10, warmup=2):
+    """Per workload: `steps` steps back to back (seqs/s, tokens/s), then `steps` with
+    events around attention and the sampler (their HBM fractions); input sets in turn
+    (two for the fixed-shape workloads; three iterations of the continuous-batching
+    mix, whose K_b are redrawn each iteration; the trees have one)."""
+    import torch
+    from speculative_decoding_verify_paged_gb300 import workloads as W
+    out = {}
+    for name, T in CONFIG_RUNS:
+        total = 3 + warmup + 2 * steps
+        if name == "llama8b":
+            case = W.llama8b(temperature=T, growth_tokens=6 * total)
+            sets = [case.step, W.llama8b_step(1, 1, temperature=T)]
+        elif name == "llama70b":
+            case = W.llama70b(temperature=T, growth_tokens=5 * total)
+            sets = [case.step, W.llama70b_step(2, 1, temperature=T)]
+        elif name == "contbatch":
+            case = W.contbatch(iterations=total)
+            sig = case.meta["sigma_b"]
+            sets = [case.step] + [W.contbatch_step(3, it, batch=case.state.batch, vocab=case.step.vocab, sigma_b=sig)
+                                  for it in (1, 2)]
+        else:
+            case = W.tree(temperature=T, growth_tokens=7 * total)
+            sets = [case.step]
+        growth = {"llama8b": 6, "llama70b": 5, "contbatch": 9, "tree": 7}[name] * total
+        loop = StepLoop(case.state, sets, growth, dev)
+        loop.learn(stream)
+        for _ in range(warmup):
+            loop.advance(loop.step(stream) % len(sets))
+        ms, _, _, _, _, _, em = timed_loop(loop, steps, stream, per_call=False)
+        _, attn_ms, samp_ms, ab, fl, sb, _ = timed_loop(loop, steps, stream, per_call=True)
+        B = case.state.batch
+        a_ms, s_ms = float(np.mean(attn_ms)), float(np.mean(samp_ms))
+        a_gbs = float(np.mean(ab)) / (a_ms / 1e3) / 1e9
+        s_gbs = float(np.mean(sb)) / (s_ms / 1e3) / 1e9
+        rec = {"seqs_per_s": B * steps / (ms / 1e3), "tokens_per_s": float(np.sum(em)) / (ms / 1e3),
+               "scored_tokens_per_s": float(np.mean([x.total_q for x in sets])) * steps / (ms / 1e3),
+               "ms_per_step": ms / steps, "input_sets": len(sets), "steps": steps,
+               "attention": {"ms": a_ms, "bytes": float(np.mean(ab)), "achieved_gbs": a_gbs, "frac": a_gbs / hbm_peak,
+                             "tflops": float(np.mean(fl)) / (a_ms / 1e3) / 1e12},
+               "sampler": {"ms": s_ms, "bytes": float(np.mean(sb)), "achieved_gbs": s_gbs, "frac": s_gbs / hbm_peak},
+               "near_ties": (int((loop.buf.margin[:B] < 1e-4).sum().item()) if T > 0 else 0)}
+        out[f"{name}_T{T:g}"] = rec
+        del loop, case, sets
+        torch.cuda.empty_cache()
+    return out
 
 
 def tree_sampler_timing(hbm_peak, reps=20):

@@ -516,8 +516,6 @@ struct Smem {
 template <typename T, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, const float *__restrict__ pm,
                                                           const float *__restrict__ ps, int nchunk, int ring_bytes) {
-  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
-  grid_dependents_launch();
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -528,6 +526,11 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
   uint8_t *ring = dyn;                                                   // phase 3: the row pair
   long long *gmass = reinterpret_cast<long long *>(dyn + ring_bytes);  // phase 3: per-group mass
 
+  // Before the grid-dependency wait this kernel reads only the call's own inputs (cu_q, draft
+  // tokens, uniforms, parents and logits), which the statistics kernel does not write: the kernel
+  // before that one on the stream has completed (the statistics kernel let this one launch only
+  // after its own wait), so they are final. Their latency then overlaps the statistics kernel's
+  // tail. The status word, the partials and every output are touched only after the wait.
   const int V = args.vocab;
   const int t0 = args.cu_q[b];
   const int n = args.cu_q[b + 1] - t0;
@@ -540,49 +543,54 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
   const T *tgt = reinterpret_cast<const T *>(args.tgt);
   const T *drf = reinterpret_cast<const T *>(args.drf);
   const float coef = args.coef;
-
-  // rows outside [0, total_q) or more than max_q rows: nothing is read or written.
+  // rows outside [0, total_q) or more than max_q rows: nothing is read or written
+  const bool valid = !(n < 1 || n > args.max_q || t0 < 0 || t0 + n > args.total_q);
+  bool bad_token = false;
+  if (valid) {
+    if (tid == 0) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pair)) : "memory");
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // the sequence's small inputs into shared memory, so the serial scans below read no global memory
+    if (tid < K) sm.tok[tid] = args.draft_tok[d0 + tid];
+    if ((MODE == kTree || MODE == kTreeStochastic) && tid < n) sm.par[tid] = args.parent[t0 + tid];
+    if constexpr (MODE == kTreeStochastic) {
+      if (tid < K) {  // node tid + 1: its accept uniform and its token's target logit in its parent's row
+        sm.uacc[tid] = args.u_acc[d0 + tid];
+        const int x = args.draft_tok[d0 + tid], pr = args.parent[t0 + tid + 1];
+        sm.gtl[tid] = 0.f;
+        if (x < 0 || x >= V) {
+          bad_token = true;
+        } else if (pr >= 0 && pr < n) {
+          sm.gtl[tid] = to_f32(tgt[(size_t)(t0 + pr) * V + x]);
+        }
+      }
+    }
+    if constexpr (MODE == kStochastic) {
+      if (tid < K) {  // the accept uniform and the target and draft logits of each draft token
+        sm.uacc[tid] = args.u_acc[d0 + tid];
+        const int x = args.draft_tok[d0 + tid];
+        if (x < 0 || x >= V) {
+          bad_token = true;
+          sm.gtl[tid] = 0.f;
+          sm.gdl[tid] = 0.f;
+        } else {
+          sm.gtl[tid] = to_f32(tgt[(size_t)(t0 + tid) * V + x]);
+          sm.gdl[tid] = to_f32(drf[(size_t)(d0 + tid) * V + x]);
+        }
+      }
+    }
+  }
+  grid_dependency_wait();  // the statistics kernel is complete and its partials visible
+  grid_dependents_launch();
   // Every CTA of the cluster takes this exit together (same b), before any barrier.
-  if (n < 1 || n > args.max_q || t0 < 0 || t0 + n > args.total_q) {
+  if (!valid) {
     if (rank == 0 && tid == 0) record(args.status, SV_ERR_BAD_LENGTH);
     return;
   }
-  if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pair)) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
+  if (bad_token && rank == 0) record(args.status, SV_ERR_BAD_TOKEN);
   bool ok = true;  // false after a bounded wait gave up: the remaining work is skipped, barriers are kept
 
-  // the sequence's small inputs into shared memory, so the serial scans below read no global memory;
-  // issued first, so that their latency overlaps the partials' below
-  if (tid < K) sm.tok[tid] = args.draft_tok[d0 + tid];
-  if ((MODE == kTree || MODE == kTreeStochastic) && tid < n) sm.par[tid] = args.parent[t0 + tid];
-  if constexpr (MODE == kTreeStochastic) {
-    if (tid < K) {  // node tid + 1: its accept uniform and its token's target logit in its parent's row
-      sm.uacc[tid] = args.u_acc[d0 + tid];
-      const int x = args.draft_tok[d0 + tid], pr = args.parent[t0 + tid + 1];
-      sm.gtl[tid] = 0.f;
-      if (x < 0 || x >= V) {
-        if (rank == 0) record(args.status, SV_ERR_BAD_TOKEN);
-      } else if (pr >= 0 && pr < n) {
-        sm.gtl[tid] = to_f32(tgt[(size_t)(t0 + pr) * V + x]);
-      }
-    }
-  }
-  if constexpr (MODE == kStochastic) {
-    if (tid < K) {  // the accept uniform and the target and draft logits of each draft token
-      sm.uacc[tid] = args.u_acc[d0 + tid];
-      const int x = args.draft_tok[d0 + tid];
-      if (x < 0 || x >= V) {
-        if (rank == 0) record(args.status, SV_ERR_BAD_TOKEN);
-        sm.gtl[tid] = 0.f;
-        sm.gdl[tid] = 0.f;
-      } else {
-        sm.gtl[tid] = to_f32(tgt[(size_t)(t0 + tid) * V + x]);
-        sm.gdl[tid] = to_f32(drf[(size_t)(d0 + tid) * V + x]);
-      }
-    }
-  }
   // ---------------- row statistics from the partials: one warp per row ----------------
   const int np = nchunk * kStatWarps;
   if constexpr (STOCH) {

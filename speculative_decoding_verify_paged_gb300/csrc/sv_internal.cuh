@@ -34,11 +34,14 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 // ---------------------------------------------------------------------------
 // programmatic dependent launch: every kernel of the library is launched with
 // launch_pdl, so its launch and set-up may overlap the end of the kernel
-// before it on the stream. Each kernel calls grid_dependency_wait() first,
-// before it reads or writes any memory and before any early return: the
-// earlier kernel has then completed and its writes are visible, and, since
-// every kernel waits before it can complete, completion stays transitive
-// along the stream. grid_dependents_launch() lets the next kernel launch.
+// before it on the stream. Each kernel calls grid_dependency_wait() before it
+// writes any memory, before it reads anything an earlier kernel of the library
+// may write, and before any return: the earlier kernel has then completed and
+// its writes are visible, and, since every kernel waits before it can
+// complete, completion stays transitive along the stream. (A kernel may read
+// the call's own inputs before the wait: the kernel before the earlier one has
+// completed by then, since the earlier one let this one launch only after its
+// own wait.) grid_dependents_launch() lets the next kernel launch.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependents_launch() {

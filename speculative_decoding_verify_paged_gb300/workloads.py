@@ -336,14 +336,21 @@ def llama8b(seed: int = 1, temperature: float = 1.0, *, batch: int = 32, ctx_ran
     n_q = np.full(batch, K + 1, np.int32)
     state = make_kv_state(seed, ctx, block_size=block_size, num_kv_heads=8, head_dim=128, dtype=kv_dtype,
                           growth_tokens=K + 1 + growth_tokens, pool_factor=pool_factor)
-    step = make_chain_step(seed, n_q, num_q_heads=32, num_kv_heads=8, head_dim=128, qkv_dtype="bf16",
-                           vocab=vocab, logits_dtype="bf16", target_sigma=3.0, draft_coef=0.8,
-                           draft_sigma=1.5, temperature=temperature)
+    step = llama8b_step(seed, 0, batch=batch, K=K, vocab=vocab, temperature=temperature)
     return Case("llama8b", seed, state, step, {"K": K})
 
 
+def llama8b_step(seed: int, stream: int, *, batch: int = 32, K: int = 5, vocab: int = 128256,
+                 temperature: float = 1.0) -> StepInputs:
+    """The Llama-8B-shaped step inputs; stream 0 is the workload's own, others are
+    further input sets of the same shapes and distributions."""
+    return make_chain_step(seed, np.full(batch, K + 1, np.int32), num_q_heads=32, num_kv_heads=8, head_dim=128,
+                           qkv_dtype="bf16", vocab=vocab, logits_dtype="bf16", target_sigma=3.0, draft_coef=0.8,
+                           draft_sigma=1.5, temperature=temperature, stream=stream)
+
+
 def llama70b(seed: int = 2, temperature: float = 1.0, *, batch: int = 128, ctx_range=(512, 640),
-             K: int = 4, vocab: int = 128256) -> Case:
+             K: int = 4, vocab: int = 128256, growth_tokens: int = 0) -> Case:
     """Llama-3-70B-shaped, input-512/output-128: 64 q / 8 kv heads of dim 128,
     bf16 KV in 16-token blocks, 128 sequences with contexts U[512, 640], K = 4,
     vocab 128256, target N(0, 3^2), draft = 0.7 target + N(0, 2^2)."""
@@ -351,11 +358,17 @@ def llama70b(seed: int = 2, temperature: float = 1.0, *, batch: int = 128, ctx_r
     ctx = rng.integers(ctx_range[0], ctx_range[1] + 1, size=batch).astype(np.int32)
     n_q = np.full(batch, K + 1, np.int32)
     state = make_kv_state(seed, ctx, block_size=16, num_kv_heads=8, head_dim=128, dtype="bf16",
-                          growth_tokens=K + 1)
-    step = make_chain_step(seed, n_q, num_q_heads=64, num_kv_heads=8, head_dim=128, qkv_dtype="bf16",
-                           vocab=vocab, logits_dtype="bf16", target_sigma=3.0, draft_coef=0.7,
-                           draft_sigma=2.0, temperature=temperature)
+                          growth_tokens=K + 1 + growth_tokens)
+    step = llama70b_step(seed, 0, batch=batch, K=K, vocab=vocab, temperature=temperature)
     return Case("llama70b", seed, state, step, {"K": K})
+
+
+def llama70b_step(seed: int, stream: int, *, batch: int = 128, K: int = 4, vocab: int = 128256,
+                  temperature: float = 1.0) -> StepInputs:
+    """The Llama-70B-shaped step inputs (stream 0: the workload's own)."""
+    return make_chain_step(seed, np.full(batch, K + 1, np.int32), num_q_heads=64, num_kv_heads=8, head_dim=128,
+                           qkv_dtype="bf16", vocab=vocab, logits_dtype="bf16", target_sigma=3.0, draft_coef=0.7,
+                           draft_sigma=2.0, temperature=temperature, stream=stream)
 
 
 CONTBATCH_ITERS = 10
@@ -415,7 +428,7 @@ def tree(seed: int = 5, *, batch: int = 16, ctx: int = 8192, block_size: int = 6
          branching=(4, 3, 2, 2, 1, 1), keep: int = 60, vocab: int = 32000,
          num_q_heads: int = 32, num_kv_heads: int = 8, head_dim: int = 128,
          target_sigma: float = 3.0, draft_coef: float = 0.8, draft_sigma: float = 1.0,
-         temperature: float = 0.0, kv_dtype: str = "bf16") -> Case:
+         temperature: float = 0.0, kv_dtype: str = "bf16", growth_tokens: int = 0) -> Case:
     """EAGLE/Medusa-style draft trees at long context, greedy acceptance (or, at
     temperature > 0, the lossless tree rule with seeded uniforms).
 
@@ -432,7 +445,7 @@ def tree(seed: int = 5, *, batch: int = 16, ctx: int = 8192, block_size: int = 6
     ctx_lens = np.full(batch, ctx, np.int32)
     rows_per_seq = keep + 1
     state = make_kv_state(seed, ctx_lens, block_size=block_size, num_kv_heads=num_kv_heads,
-                          head_dim=head_dim, dtype=kv_dtype, growth_tokens=rows_per_seq)
+                          head_dim=head_dim, dtype=kv_dtype, growth_tokens=rows_per_seq + growth_tokens)
     bank = _Bank(seed)
     tgt_rows, drf_rows, toks, parents, masks = [], [], [], [], []
     for b in range(batch):

@@ -60,9 +60,11 @@ def _no_alloc(kv, d, buf, msl, out):
 
 
 def _allocator():
+    """The caching allocator's cumulative counts of allocations and of segments it
+    took from the device (they only grow), and the bytes it holds (a garbage
+    collection between two snapshots may lower them, never raise them)."""
     st = torch.cuda.memory_stats()
-    return (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), st.get("allocation.all.allocated", 0),
-            st.get("segment.all.allocated", 0))
+    return st.get("allocation.all.allocated", 0), st.get("segment.all.allocated", 0), torch.cuda.memory_reserved()
 
 
 @pytest.mark.parametrize("path", ["auto", "tensor_cores", "cuda_cores", "warp_mma", "keys_major"])
@@ -78,7 +80,8 @@ def test_two_calls_match_the_workspace_entry_point(path):
         for p, out in zip(prepared, outs):  # back to back on one stream
             _no_alloc(*p, out)
         torch.cuda.synchronize()
-        assert _allocator() == before, "the caching allocator was used"
+        after = _allocator()
+        assert after[:2] == before[:2] and after[2] <= before[2], "the caching allocator was used"
         for (kv, d, buf, msl), out in zip(prepared, outs):
             assert int(buf.status.item()) == 0
             assert torch.equal(out, buf.attn_out)
