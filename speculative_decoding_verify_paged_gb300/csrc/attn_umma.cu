@@ -83,6 +83,10 @@ constexpr int kCodeHalf = kTile * 128;          // 32 keys x 128 one-byte codes
 constexpr int kCodeStageBytes = 2 * kCodeHalf;  // K and V codes
 constexpr int kConvStages = 3;
 constexpr int kConvWarps = 2;                   // warps 6-7, after the softmax warps
+// What starting and finishing a unit costs a CTA (the Q load, the pipeline refill, the last
+// P V and the epilogue), in tiles: the work order gives each unit this many lead-in positions,
+// so that ranges with more units hold fewer tiles.
+constexpr int kUnitLeadIn = 4;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -226,6 +230,7 @@ struct UmmaParams {
   int rows_cap;     // rows of a workspace slot: min(128, G * max_q)
   int rb_max;       // row blocks of the longest sequence: ceil(G * max_q / 128)
   int ctas;         // CTAs of the launch
+  int alpha;        // lead-in positions of a unit in the work order
   float *part_o;    // [ctas][2][rows_cap][128] normalised partial outputs
   float *part_lse;  // [ctas][2][rows_cap] their log-sum-exp (base 2)
   int *prefix;      // [batch + 1]: first tile of each sequence's units; [batch] = all tiles
@@ -255,8 +260,16 @@ __device__ __forceinline__ Seq load_seq(const UmmaParams &P, int b, bool *bad) {
   s.tiles = (ok && s.rbs > 0) ? (s.L + kTile - 1) / kTile : 0;
   return s;
 }
+// Positions a sequence takes in the launch's work order: per unit, a lead-in of alpha
+// positions (the cost of starting and finishing a unit, in tiles) and then its tiles.
 __device__ __forceinline__ int seq_work(const UmmaParams &P, const Seq &s) {
-  return P.a.kv.num_kv_heads * s.rbs * s.tiles;
+  return s.tiles > 0 ? P.a.kv.num_kv_heads * s.rbs * (s.tiles + P.alpha) : 0;
+}
+// CTA c's positions start at range_start(c): the W positions cut as evenly as integers allow
+__device__ __forceinline__ int range_start(int c, int W, int ctas) { return (int)(((long long)c * W) / ctas); }
+// the CTA whose positions hold position x (0 <= x < W)
+__device__ __forceinline__ int range_owner(int x, int W, int ctas) {
+  return (int)((((long long)x + 1) * ctas + W - 1) / W) - 1;
 }
 
 // Inclusive sum over the CTA's threads; *total gets the sum over all of them.
@@ -295,34 +308,39 @@ struct Walker {
   int b, base, g, end;
   Seq s;
   __device__ __forceinline__ bool next(const UmmaParams &P, Piece &p) {
-    if (g >= end) return false;
-    int work = seq_work(P, s);
-    while (g - base >= work) {
-      if (b + 1 >= P.a.kv.batch) {  // cannot happen while the lengths stay put; never read past the batch
-        g = end;
-        return false;
+    for (;;) {
+      if (g >= end) return false;
+      int work = seq_work(P, s);
+      while (g - base >= work) {
+        if (b + 1 >= P.a.kv.batch) {  // cannot happen while the lengths stay put; never read past the batch
+          g = end;
+          return false;
+        }
+        base += work;
+        ++b;
+        bool bad;
+        s = load_seq(P, b, &bad);
+        work = seq_work(P, s);
       }
-      base += work;
-      ++b;
-      bool bad;
-      s = load_seq(P, b, &bad);
-      work = seq_work(P, s);
+      const int U = s.tiles + P.alpha;  // a unit's positions: lead-in, then tiles
+      const int local = g - base;
+      const int j = local / U, off = local - j * U;
+      const int npos = min(U - off, end - g);
+      g += npos;
+      const int kt0 = max(0, off - P.alpha), kt1 = off + npos - P.alpha;
+      if (kt1 <= 0) continue;  // only the unit's lead-in lies in this range
+      p.b = b;
+      p.kvh = j / s.rbs;
+      p.rb = j - p.kvh * s.rbs;
+      p.c = s.c;
+      p.row0 = s.row0;
+      p.n = s.n;
+      p.L = s.L;
+      p.kt0 = kt0;
+      p.kt1 = kt1;
+      p.whole = kt0 == 0 && kt1 == s.tiles;
+      return true;
     }
-    const int local = g - base;
-    const int j = local / s.tiles, off = local - j * s.tiles;
-    const int len = min(s.tiles - off, end - g);
-    p.b = b;
-    p.kvh = j / s.rbs;
-    p.rb = j - p.kvh * s.rbs;
-    p.c = s.c;
-    p.row0 = s.row0;
-    p.n = s.n;
-    p.L = s.L;
-    p.kt0 = off;
-    p.kt1 = off + len;
-    p.whole = off == 0 && len == s.tiles;
-    g += len;
-    return true;
   }
 };
 
@@ -406,8 +424,7 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
   }
   int W;
   block_scan<kNT>(mine, sh_scan, &W);
-  const int per = max(1, (W + P.ctas - 1) / P.ctas);
-  const int g0 = min(W, (int)blockIdx.x * per), g1 = min(W, g0 + per);
+  const int g0 = range_start(blockIdx.x, W, P.ctas), g1 = range_start(blockIdx.x + 1, W, P.ctas);
   int run = 0;
   for (int b0 = 0; b0 < B; b0 += kNT) {  // the sequence holding tile g0; CTA 0 also stores the prefix
     const int b = b0 + tid;
@@ -445,70 +462,59 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
 
   if (warp == 0) {
     // ================= producer =================
+    // Lane j copies box j of a tile (box rows of one block), K and V. The block ids come from
+    // a 64-block window of the block table, two entries per lane, each loaded one window
+    // before it is used and checked only then, so no load latency sits in the issue loop.
     // block_size is a power of two: logical blocks and row offsets by shift and mask
     const int bs = kv.block_size, box = P.box_rows;
     const int bs_shift = __ffs(bs) - 1;
     const uint32_t row_bytes = F8 ? 128u : 256u;  // one key's row of K (or V) as the TMA brings it
     const uint32_t box_bytes = static_cast<uint32_t>(box) * row_bytes;
+    const int nboxes = kTile / box;  // 1 or 2
     if (a.stall == SV_STALL_ATTENTION) ok = __all_sync(0xffffffffu, wait_on_nothing(smem_u32(stall_bar), wns));
     Piece p;
     while (ok && walker.next(P, p)) {
-      const int kb = p.kt0 * kTile, ke = min(p.L, p.kt1 * kTile);
+      const int ke = min(p.L, p.kt1 * kTile);
       const int lb_last = (ke - 1) >> bs_shift;
       const int32_t *bt = kv.block_table + (size_t)p.b * kv.max_blocks;
-      // first pool row of logical block lb for this KV head; -1 past the piece or for a bad id
-      auto load_y = [&](int lb) -> int {
-        if (lb > lb_last) return -1;
-        const int id = bt[lb];
-        if (id < 0 || id >= kv.num_blocks) {
-          record(a.status, SV_ERR_BAD_BLOCK_ID);
-          return -1;
-        }
-        return (id * kv.num_kv_heads + p.kvh) << bs_shift;
-      };
-      int wbase = kb >> bs_shift;  // lane l holds logical block wbase + l (cur) and wbase + 32 + l (nxt)
-      int cur = load_y(wbase + lane);
-      int nxt = load_y(wbase + 32 + lane);
+      auto load_id = [&](int lb) -> int { return lb <= lb_last ? bt[lb] : -1; };
+      int wbase = (p.kt0 * kTile) >> bs_shift;  // lane l holds blocks wbase + l (cur) and wbase + 32 + l (nxt)
+      int cur = load_id(wbase + lane);
+      int nxt = load_id(wbase + 32 + lane);
       for (int kt = p.kt0; kt < p.kt1; ++kt, ++issued) {
         const int s = issued % kLS;
+        const int k0 = kt * kTile;
+        while ((k0 >> bs_shift) >= wbase + 32) {  // warp-uniform
+          wbase += 32;
+          cur = nxt;
+          nxt = load_id(wbase + 32 + lane);
+        }
+        const int tok = k0 + lane * box;
+        const bool want = lane < nboxes && tok < ke;
+        const int src = (tok >> bs_shift) - wbase;  // below 34 for a wanted box
+        const int idc = __shfl_sync(0xffffffffu, cur, src & 31);
+        const int idn = __shfl_sync(0xffffffffu, nxt, src & 31);
+        const int id = src < 32 ? idc : idn;
+        const bool bad = want && (id < 0 || id >= kv.num_blocks);
+        if (bad) record(a.status, SV_ERR_BAD_BLOCK_ID);
+        const bool go = want && !bad;
+        const int y = ((id * kv.num_kv_heads + p.kvh) << bs_shift) + (tok & (bs - 1));
+        const int nbox = __popc(__ballot_sync(0xffffffffu, go));
         if (issued >= kLS) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), ((issued / kLS) - 1) & 1, wns));
         if (!ok) break;
-        const int k0 = kt * kTile;
-        int ys[kTile / 16];
-        int nbox = 0;
-#pragma unroll
-        for (int j = 0; j < kTile / 16; ++j) {
-          const int tok = k0 + j * box;
-          int y = -1;
-          if (j * box < kTile && tok < ke) {
-            const int lb = tok >> bs_shift;
-            while (lb >= wbase + 32) {  // warp-uniform
-              wbase += 32;
-              cur = nxt;
-              nxt = load_y(wbase + 32 + lane);
-            }
-            const int yb = __shfl_sync(0xffffffffu, cur, lb - wbase);
-            y = yb < 0 ? -1 : yb + (tok & (bs - 1));
-          }
-          ys[j] = y;
-          nbox += y >= 0;
-        }
-        if (lane == 0) {
-          const uint32_t fb = smem_u32(&full[s]);
-          mbar_expect_tx(fb, static_cast<uint32_t>(nbox) * 2u * box_bytes);
-          const uint32_t kdst = smem_u32(stages + s * kLoadStageBytes);
-          const uint32_t vdst = kdst + (F8 ? kCodeHalf : 2 * kHalfBytes);
-#pragma unroll
-          for (int j = 0; j < kTile / 16; ++j) {
-            if (ys[j] < 0) continue;
-            const uint32_t off = static_cast<uint32_t>(j * box) * row_bytes;  // group of `box` rows
-            if (F8) {
-              tma_load_codes(kdst + off, &tmap_k, ys[j], fb);
-              tma_load_codes(vdst + off, &tmap_v, ys[j], fb);
-            } else {
-              tma_load_rows(kdst + off, &tmap_k, ys[j], fb);
-              tma_load_rows(vdst + off, &tmap_v, ys[j], fb);
-            }
+        const uint32_t fb = smem_u32(&full[s]);
+        if (lane == 0) mbar_expect_tx(fb, static_cast<uint32_t>(nbox) * 2u * box_bytes);
+        __syncwarp();
+        const uint32_t kdst = smem_u32(stages + s * kLoadStageBytes);
+        const uint32_t vdst = kdst + (F8 ? kCodeHalf : 2 * kHalfBytes);
+        const uint32_t off = static_cast<uint32_t>(lane * box) * row_bytes;  // group of `box` rows
+        if (go) {
+          if (F8) {
+            tma_load_codes(kdst + off, &tmap_k, y, fb);
+            tma_load_codes(vdst + off, &tmap_v, y, fb);
+          } else {
+            tma_load_rows(kdst + off, &tmap_k, y, fb);
+            tma_load_rows(vdst + off, &tmap_v, y, fb);
           }
         }
         __syncwarp();
@@ -878,13 +884,12 @@ __global__ void __launch_bounds__(128) attn_umma_combine(const UmmaParams P) {
   bool bad;
   const Seq s = load_seq(P, b, &bad);
   if (s.tiles == 0 || rb >= s.rbs) return;
-  const int per = max(1, (W + P.ctas - 1) / P.ctas);
-  const int T0 = base + (kvh * s.rbs + rb) * s.tiles, T1 = T0 + s.tiles;
-  const int c0 = T0 / per, c1 = (T1 - 1) / per;
+  const int T0 = base + (kvh * s.rbs + rb) * (s.tiles + P.alpha) + P.alpha, T1 = T0 + s.tiles;  // its tiles
+  const int c0 = range_owner(T0, W, P.ctas), c1 = range_owner(T1 - 1, W, P.ctas);
   if (c0 == c1) return;  // one CTA held the whole unit and wrote its rows
-  // CTA c0 holds the unit as its first piece (slot 0) only when the unit starts its range;
-  // every later CTA holds it as its first piece
-  const int slot0 = T0 == c0 * per ? 0 : 1;
+  // CTA c0 holds the unit as its first piece (slot 0) only when its range starts in the unit's
+  // lead-in (before that come tiles of an earlier unit); every later CTA holds it as its first piece
+  const int slot0 = range_start(c0, W, P.ctas) >= T0 - P.alpha ? 0 : 1;
   auto slot_of = [&](int cc, int row) -> size_t {
     return ((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * P.rows_cap + row;
   };
@@ -901,7 +906,8 @@ __global__ void __launch_bounds__(128) attn_umma_combine(const UmmaParams P) {
       float4 v[kPc][8];
 #pragma unroll
       for (int k = 0; k < kPc; ++k) {
-        const bool in = cb + k <= c1;
+        // a CTA between c0 and c1 whose range is empty (more CTAs than positions) holds nothing
+        const bool in = cb + k <= c1 && range_start(cb + k, W, P.ctas) < range_start(cb + k + 1, W, P.ctas);
         const size_t sl = slot_of(in ? cb + k : cb, row);
         lse[k] = in ? __ldcg(P.part_lse + sl) : -INFINITY;
         const float4 *src = reinterpret_cast<const float4 *>(P.part_o + sl * kD + c32);
@@ -1034,9 +1040,9 @@ bool attn_umma_supported(const KV &kv) {
 
 bool attn_umma_fits(const KV &kv, int num_q_heads, int max_q, int max_seq_len) {
   const int G = num_q_heads / kv.num_kv_heads;
-  const long long max_tiles =
-      (long long)kv.batch * kv.num_kv_heads * ((G * max_q + kRowsMax - 1) / kRowsMax) * ((max_seq_len + kTile - 1) / kTile);
-  return max_tiles < (1LL << 30);
+  const long long units = (long long)kv.batch * kv.num_kv_heads * ((G * max_q + kRowsMax - 1) / kRowsMax);
+  const long long positions = units * (((max_seq_len + kTile - 1) / kTile) + kUnitLeadIn);
+  return positions < (1LL << 30);
 }
 
 size_t attn_umma_workspace_bytes(const KV &kv, int num_q_heads, int max_q, int max_seq_len) {
@@ -1055,6 +1061,7 @@ cudaError_t launch_attn_umma(const AttnArgs &a, void *workspace, size_t workspac
   p.rows_cap = l.rows_cap;
   p.rb_max = l.rb_max;
   p.ctas = l.ctas;
+  p.alpha = kUnitLeadIn;
   p.part_o = reinterpret_cast<float *>(workspace);
   p.part_lse = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + l.lse_offset);
   p.prefix = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(workspace) + l.prefix_offset);
