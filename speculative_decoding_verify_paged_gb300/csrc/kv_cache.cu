@@ -251,12 +251,9 @@ constexpr int kCuCache = 2048;
 __global__ void __launch_bounds__(kScatterThreads) kv_scatter_kernel(KV kv, const uint8_t *new_k,
                                                                      const uint8_t *new_v, const int32_t *cu_q,
                                                                      int32_t *status) {
-  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
-  grid_dependents_launch();
   __shared__ int s_cu[kCuCache];
   const int row = blockIdx.x;
   const int B = kv.batch;
-  const bool failed = status_set(status);
   const int row_bytes = kv.head_dim * kv.elem_bytes;  // a multiple of 16
   const int vec_per_row = row_bytes / 16;
   const int total = kv.num_kv_heads * vec_per_row;
@@ -276,7 +273,11 @@ __global__ void __launch_bounds__(kScatterThreads) kv_scatter_kernel(KV kv, cons
   if (staged)
     for (int k = threadIdx.x; k <= B; k += blockDim.x) s_cu[k] = cu_q[k];
   __syncthreads();
-  if (failed) return;
+  // the row's vectors and cu_q are the call's own inputs, read above before the wait; the status,
+  // the lengths, the block table and the pool come after it
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  grid_dependents_launch();
+  if (status_set(status)) return;
   auto cu = [&](int k) { return staged ? s_cu[k] : cu_q[k]; };
   int lo = 0, hi = B;  // the last b with cu_q[b] <= row owns the row
   while (hi - lo > 1) {

@@ -26,7 +26,7 @@
 //               bulk copies; eight consumer warps reduce each item to a
 //               (max, sum of 2^((l - max) log2(e)/T)) pair, or to an argmax,
 //               per warp, into a workspace of per-(item, warp) partials.
-//   decisions   one cluster per sequence (8 or 16 CTAs; one for greedy and
+//   decisions   one cluster per sequence (4, 8 or 16 CTAs; one for greedy and
 //               greedy tree). The tree walks run on one warp. Every
 //               CTA combines its sequence's partials in the same fixed order,
 //               so all CTAs hold identical row statistics and take identical
@@ -64,11 +64,17 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kStatWarps = 8;                          // statistics kernel: consumer warps
 constexpr int kStatThreads = (kStatWarps + 1) * 32;   // + one producer warp
 constexpr int kStatStages = 3;
+constexpr int kMaxRuns = 64;                           // statistics kernel: runs a CTA keeps until its wait
 constexpr int kPartBytes = 32768;                      // one statistics item: 32 KB of one row
 constexpr int kMaxQ = 64;
 constexpr int kMaxRows = 2 * kMaxQ;  // target + draft rows of one sequence
-constexpr int kMaxChunk = 16384;     // vocabulary elements per CTA
+constexpr int kMaxChunk = 32768;     // vocabulary elements per CTA
 constexpr int kGroup = 8;            // consecutive elements of a group
+constexpr int kSub = 4096;           // decisions: elements of a sub-chunk of the row pair (two groups a thread)
+constexpr int kRingBytes = 65536;    // decisions: the sub-chunk ring (target and draft halves)
+template <typename T>
+constexpr int sub_stages() { return kRingBytes / (2 * kSub * (int)sizeof(T)); }  // bf16: 4, fp32: 2
+constexpr int kMaxSubStages = 4;
 
 // 2^x by the MUFU approximation (flush-to-zero; relative error about 2^-22)
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -165,31 +171,32 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 
 // The eight elements of group g of a shared-memory copy of a chunk, as floats;
 // -inf at and past element n (only the chunk's last group can reach it).
-template <typename T>
-__device__ __forceinline__ void group8(const T *buf, int g, int n, float (&x)[kGroup]) {
+// Group g (elements 8 g .. 8 g + 7) of a span of n elements, from global memory (GLOBAL) or
+// shared memory; elements past n read as -inf.
+template <typename T, bool VEC, bool GLOBAL>
+__device__ __forceinline__ void group8(const T *row, int g, int n, float (&x)[kGroup]) {
   const int e = g * kGroup;
-  if constexpr (sizeof(T) == 2) {
-    const uint4 r = *reinterpret_cast<const uint4 *>(buf + e);
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(&r);
+  auto ld16 = [](const void *q) -> uint4 {
+    return GLOBAL ? __ldg(reinterpret_cast<const uint4 *>(q)) : *reinterpret_cast<const uint4 *>(q);
+  };
+  if (VEC && e + kGroup <= n) {  // 16-byte aligned: the span starts at a multiple of 8 elements
+    if constexpr (sizeof(T) == 2) {
+      const uint4 r = ld16(row + e);
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      x[2 * k] = __uint_as_float(w[k] << 16);
-      x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+      for (int k = 0; k < 4; ++k) {
+        x[2 * k] = __uint_as_float(w[k] << 16);
+        x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+      }
+    } else {
+      const uint4 r0 = ld16(row + e), r1 = ld16(row + e + 4);
+      x[0] = __uint_as_float(r0.x), x[1] = __uint_as_float(r0.y), x[2] = __uint_as_float(r0.z);
+      x[3] = __uint_as_float(r0.w), x[4] = __uint_as_float(r1.x), x[5] = __uint_as_float(r1.y);
+      x[6] = __uint_as_float(r1.z), x[7] = __uint_as_float(r1.w);
     }
-  } else {
-    const uint4 r0 = *reinterpret_cast<const uint4 *>(buf + e);
-    const uint4 r1 = *reinterpret_cast<const uint4 *>(buf + e + 4);
-    const float *f0 = reinterpret_cast<const float *>(&r0), *f1 = reinterpret_cast<const float *>(&r1);
+  } else {  // the chunk's ragged end (elements past it read as -inf), or rows without alignment
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      x[k] = f0[k];
-      x[k + 4] = f1[k];
-    }
-  }
-  if (e + kGroup > n) {
-#pragma unroll
-    for (int k = 0; k < kGroup; ++k)
-      if (e + k >= n) x[k] = -INFINITY;
+    for (int k = 0; k < kGroup; ++k) x[k] = e + k < n ? to_f32(row[e + k]) : -INFINITY;
   }
 }
 
@@ -217,13 +224,18 @@ struct StatsArgs {
 
 template <typename T, bool VEC, int MODE>
 __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) {
-  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  // This kernel reads only the call's logits, which no kernel of the library writes: it streams
+  // them without waiting for the kernel before it (the end of the attention call), and waits
+  // only before its first write to global memory, which goes to a workspace another call may
+  // share. Its partials wait in shared memory until then (kMaxRuns runs; more are written after
+  // an early wait).
   grid_dependents_launch();
   constexpr int CH = kPartBytes / (int)sizeof(T);  // elements of an item
   constexpr int SL = CH / kStatWarps;              // elements of a warp's slice
   extern __shared__ __align__(128) uint8_t ring[];  // kStatStages x kPartBytes
   __shared__ uint64_t full[kStatStages], empty[kStatStages];
   __shared__ uint64_t stall_bar;  // failure-path test: a barrier nothing arrives on
+  __shared__ float2 runbuf[kMaxRuns][kStatWarps];  // consumers: each run's per-warp statistics
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i0 = blockIdx.x * A.per + min((int)blockIdx.x, A.extra);
   const int i1 = min(A.items, i0 + A.per + ((int)blockIdx.x < A.extra ? 1 : 0));
@@ -270,13 +282,30 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
         ++issued;
       }
     }
+    grid_dependency_wait();
   } else {
     // ---------------- consumers: warp w reduces elements [w SL, (w + 1) SL) of each item ----------------
     int bad = 0;
     float lm = -INFINITY, ls = 0.f;  // stochastic: running max, sum of 2^(x c - lm c)
     float lb = 0.f;                  // greedy: best value and index
     int lbi = -1;
-    int cur_row = -1, run_start = -1;
+    int cur_row = -1, run_start = -1, nrun = 0;
+    bool waited = false;
+    auto wait_once = [&]() {
+      if (!waited) grid_dependency_wait();
+      waited = true;
+    };
+    // the run's (max, sum) or (value, index bits) for item run_start: kept in shared memory, or
+    // (past kMaxRuns runs) written after the wait
+    auto put = [&](float a, float b) {
+      if (nrun < kMaxRuns) {
+        runbuf[nrun][warp] = make_float2(a, b);
+      } else {
+        wait_once();
+        A.pm[(size_t)run_start * kStatWarps + warp] = a;
+        A.ps[(size_t)run_start * kStatWarps + warp] = b;
+      }
+    };
     auto flush = [&]() {  // warp-uniform: the run's statistics into (run_start, warp)
       if constexpr (MODE == kStochastic) {
 #pragma unroll
@@ -285,10 +314,7 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
           const float s2 = __shfl_xor_sync(0xffffffffu, ls, o);
           ms_combine(lm, ls, m2, s2, A.coef);
         }
-        if (lane == 0) {
-          A.pm[(size_t)run_start * kStatWarps + warp] = lm;
-          A.ps[(size_t)run_start * kStatWarps + warp] = ls;
-        }
+        if (lane == 0) put(lm, ls);
         lm = -INFINITY;
         ls = 0.f;
       } else {
@@ -298,13 +324,11 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
           const int i2 = __shfl_xor_sync(0xffffffffu, lbi, o);
           am_combine(lb, lbi, v2, i2);
         }
-        if (lane == 0) {
-          A.pm[(size_t)run_start * kStatWarps + warp] = lb;
-          A.ps[(size_t)run_start * kStatWarps + warp] = __int_as_float(lbi);
-        }
+        if (lane == 0) put(lb, __int_as_float(lbi));
         lb = 0.f;
         lbi = -1;
       }
+      ++nrun;
     };
     for (int it = i0, j = 0; it < i1; ++it, ++j) {
       const int s = j % kStatStages;
@@ -314,9 +338,6 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
         if (cur_row >= 0) flush();
         cur_row = r;
         run_start = it;
-      } else if (lane == 0) {  // not a run's first item: the identity
-        A.pm[(size_t)it * kStatWarps + warp] = (MODE == kStochastic) ? -INFINITY : 0.f;
-        A.ps[(size_t)it * kStatWarps + warp] = (MODE == kStochastic) ? 0.f : __int_as_float(-1);
       }
       const T *src;
       if constexpr (VEC) {
@@ -469,6 +490,26 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
       }
     }
     if (cur_row >= 0) flush();
+    // the writes: each run's first item gets the run's statistics (those kept here), every other
+    // item the identity
+    wait_once();
+    if (lane == 0) {
+      int run = -1, prev = -1;
+      for (int it = i0; it < i1; ++it) {
+        const int r = it / A.nchunk;
+        const size_t at = (size_t)it * kStatWarps + warp;
+        if (r != prev) {
+          prev = r;
+          if (++run < kMaxRuns) {
+            A.pm[at] = runbuf[run][warp].x;
+            A.ps[at] = runbuf[run][warp].y;
+          }
+        } else {
+          A.pm[at] = (MODE == kStochastic) ? -INFINITY : 0.f;
+          A.ps[at] = (MODE == kStochastic) ? 0.f : __int_as_float(-1);
+        }
+      }
+    }
     if (bad) record(A.status, SV_ERR_NONFINITE);
     if (!ok) record(A.status, SV_ERR_TIMEOUT);
   }
@@ -490,7 +531,6 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(const StatsArgs A) 
 // identical decisions; for T > 0 the draw runs over the C vocabulary chunks.
 // ===========================================================================
 struct Smem {
-  uint64_t pair;  // phase 3 row pair
   float M[kMaxRows];  // per row, whole vocabulary
   float Z[kMaxRows];
   int am[kMaxRows];
@@ -502,6 +542,7 @@ struct Smem {
   int excl[kMaxQ];               // tree at T > 0: tokens rejected at the final node
   int nexcl;
   int cur;                       // tree at T > 0: the final node's row
+  uint64_t sub_full[kMaxSubStages];  // phase 3: ring of row-pair sub-chunks
   long long S[2];    // phase 3: this CTA's fixed-point weight sum per pass (cluster-visible)
   long long ll_buf[kWarps];
   long long P_owner, target;
@@ -515,7 +556,7 @@ struct Smem {
 
 template <typename T, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, const float *__restrict__ pm,
-                                                          const float *__restrict__ ps, int nchunk, int ring_bytes) {
+                                                          const float *__restrict__ ps, int nchunk) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -523,14 +564,16 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ Smem sm;
   extern __shared__ __align__(128) uint8_t dyn[];
-  uint8_t *ring = dyn;                                                   // phase 3: the row pair
-  long long *gmass = reinterpret_cast<long long *>(dyn + ring_bytes);  // phase 3: per-group mass
+  // phase 3: a ring of sub-chunk stages (target, then draft: kSub elements each), then the
+  // per-group masses
+  constexpr int kSubStages = sub_stages<T>();
+  uint8_t *sring = dyn;
+  long long *gmass = reinterpret_cast<long long *>(dyn + kRingBytes);
 
   // Before the grid-dependency wait this kernel reads only the call's own inputs (cu_q, draft
-  // tokens, uniforms, parents and logits), which the statistics kernel does not write: the kernel
-  // before that one on the stream has completed (the statistics kernel let this one launch only
-  // after its own wait), so they are final. Their latency then overlaps the statistics kernel's
-  // tail. The status word, the partials and every output are touched only after the wait.
+  // tokens, uniforms, parents and logits), which no kernel of the library writes, so their
+  // latency overlaps the statistics kernel's tail. The status word, the partials and every
+  // output are touched only after the wait.
   const int V = args.vocab;
   const int t0 = args.cu_q[b];
   const int n = args.cu_q[b + 1] - t0;
@@ -548,7 +591,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
   bool bad_token = false;
   if (valid) {
     if (tid == 0) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pair)) : "memory");
+      for (int st = 0; st < kSubStages; ++st)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.sub_full[st])) : "memory");
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // the sequence's small inputs into shared memory, so the serial scans below read no global memory
@@ -864,45 +908,13 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
     const float Mt = sm.M[dr], Md = resid ? sm.M[n + a] : 0.f;
     const float chi = args.coef, clo = args.coef_lo;
     const float ur = args.u_res[b];
-    const int pair_off = ((len * (int)sizeof(T) + 127) / 128) * 128;
-    const T *bt = reinterpret_cast<const T *>(ring);
-    const T *bd = reinterpret_cast<const T *>(ring + pair_off);
+    // this CTA's chunk of the row (pair) of the draw
+    const T *bt = trow + lo;
+    const T *bd = resid ? drow + lo : nullptr;
     const int ngroups = (len + kGroup - 1) / kGroup;
-
-    // ---- the row pair of the draw into shared memory ----
-    if (len > 0) {
-      if (VEC) {
-        if (tid == 0) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          const uint32_t bytes = static_cast<uint32_t>(len * sizeof(T));
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&sm.pair)),
-                       "r"(resid ? 2 * bytes : bytes)
-                       : "memory");
-          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                           smem_addr(ring)),
-                       "l"(trow + lo), "r"(bytes), "r"(smem_addr(&sm.pair))
-                       : "memory");
-          if (resid)
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_addr(ring + pair_off)),
-                "l"(drow + lo), "r"(bytes), "r"(smem_addr(&sm.pair))
-                : "memory");
-        }
-        if (ok && !mbar_wait_bounded(smem_addr(&sm.pair), 0)) {
-          ok = false;
-          record(args.status, SV_ERR_TIMEOUT);
-        }
-      } else {
-        T *wt = reinterpret_cast<T *>(ring);
-        T *wd = reinterpret_cast<T *>(ring + pair_off);
-        for (int k = tid; k < len; k += kThreads) {
-          wt[k] = trow[lo + k];
-          if (resid) wd[k] = drow[lo + k];
-        }
-      }
-    }
-    __syncthreads();
+    const int nsub = (len + kSub - 1) / kSub;
+    const uint32_t sub_bytes = kSub * sizeof(T);
+    int subs_done = 0;  // sub-chunks consumed so far (over both passes): ring stage and phase
 
     const float rho_hi = sm.rho_hi, rho_lo = sm.rho_lo;
 
@@ -911,12 +923,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
       const bool excl_pass = nexcl > 0 && pass == 0;
       // the eight weights of group g, in [0, 1]: proportional to max(0, p_v - q_v)
       // (scaled by Z_t), or to p_v
-      auto weightsf8 = [&](int g, float (&w)[kGroup]) {
-        float xt[kGroup];
-        group8<T>(bt, g, len, xt);
+      auto weights_of = [&](int g, const float (&xt)[kGroup], const float (&xd)[kGroup], float (&w)[kGroup]) {
         if (res_pass) {
-          float xd[kGroup];
-          group8<T>(bd, g, len, xd);
 #pragma unroll
           for (int k = 0; k < kGroup; ++k) {
             const float et = exp2_acc(xt[k] - Mt, chi, clo);
@@ -935,6 +943,24 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
           }
         }
       };
+      // ... read from global memory (the owner's one group)
+      // ... for the owner's one group: from the ring while the whole chunk stays in it (no stage
+      // was refilled), else from global memory
+      const int pass_base = subs_done;
+      auto weightsf8 = [&](int g, float (&w)[kGroup]) {
+        float xt[kGroup], xd[kGroup];
+        if (VEC && nsub <= kSubStages) {
+          const int i = g / (kSub / kGroup), gl = g - i * (kSub / kGroup);
+          const int n_i = min(kSub, len - i * kSub);
+          const uint8_t *stage = sring + ((pass_base + i) % kSubStages) * 2 * sub_bytes;
+          group8<T, true, false>(reinterpret_cast<const T *>(stage), gl, n_i, xt);
+          if (res_pass) group8<T, true, false>(reinterpret_cast<const T *>(stage + sub_bytes), gl, n_i, xd);
+        } else {
+          group8<T, VEC, true>(bt, g, len, xt);
+          if (res_pass) group8<T, VEC, true>(bd, g, len, xd);
+        }
+        weights_of(g, xt, xd, w);
+      };
       // ... as fixed point, one by one
       auto weights8 = [&](int g, long long (&w)[kGroup]) {
         float f[kGroup];
@@ -945,9 +971,9 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
       // ... and their fixed-point sum, equal to the sum of the values above: the 20-bit
       // halves of to_fix summed as float bit patterns (2^23 + integer, eight of them:
       // no carry leaves 32 bits), the offsets taken off once
-      auto mass8 = [&](int g) -> long long {
+      auto mass8 = [&](int g, const float (&xt)[kGroup], const float (&xd)[kGroup]) -> long long {
         float f[kGroup];
-        weightsf8(g, f);
+        weights_of(g, xt, xd, f);
         uint32_t sh = 0u, sl = 0u;
 #pragma unroll
         for (int k = 0; k < kGroup; ++k) {
@@ -962,15 +988,65 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
         sl -= static_cast<uint32_t>(kGroup) * 0x4B000000u;
         return (static_cast<long long>(sh) << 20) + static_cast<long long>(sl);
       };
-      // ---- pass B: each group's mass and this CTA's total ----
+      // ---- pass B: each group's mass and this CTA's total. The chunk streams through the
+      // ring in sub-chunks of kSub elements (two groups a thread): thread 0 keeps kSubStages of
+      // them in flight with bulk copies, refilling a stage once every thread has read it ----
       long long mass = 0;
-      if (ok) {
-        for (int g = tid; g < ngroups; g += kThreads) {
-          const long long m8 = mass8(g);
-          gmass[g] = m8;
-          mass += m8;
+      auto issue_sub = [&](int i) {  // sub-chunk i of this pass into its stage (thread 0, VEC)
+        const int st = (subs_done + i) % kSubStages;
+        const int e0 = i * kSub;
+        const uint32_t bytes = static_cast<uint32_t>(min(kSub, len - e0)) * sizeof(T);
+        uint8_t *dst = sring + st * 2 * sub_bytes;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the stage's earlier reads are done
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&sm.sub_full[st])),
+                     "r"(res_pass ? 2 * bytes : bytes)
+                     : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         smem_addr(dst)),
+                     "l"(bt + e0), "r"(bytes), "r"(smem_addr(&sm.sub_full[st]))
+                     : "memory");
+        if (res_pass)
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                           smem_addr(dst + sub_bytes)),
+                       "l"(bd + e0), "r"(bytes), "r"(smem_addr(&sm.sub_full[st]))
+                       : "memory");
+      };
+      if (ok && VEC && tid == 0)
+        for (int i = 0; i < min(nsub, kSubStages); ++i) issue_sub(i);
+      for (int i = 0; ok && i < nsub; ++i) {
+        const int st = (subs_done + i) % kSubStages;
+        const T *sbt = reinterpret_cast<const T *>(sring + st * 2 * sub_bytes);
+        const T *sbd = reinterpret_cast<const T *>(sring + st * 2 * sub_bytes + sub_bytes);
+        const int n_i = min(kSub, len - i * kSub);
+        if (VEC) {
+          if (!mbar_wait_bounded(smem_addr(&sm.sub_full[st]), ((subs_done + i) / kSubStages) & 1)) {
+            ok = false;
+            record(args.status, SV_ERR_TIMEOUT);
+          }
+        } else {
+          T *wt = const_cast<T *>(sbt), *wd = const_cast<T *>(sbd);
+          for (int k = tid; k < n_i; k += kThreads) {
+            wt[k] = bt[i * kSub + k];
+            if (res_pass) wd[k] = bd[i * kSub + k];
+          }
+          __syncthreads();
         }
+#pragma unroll
+        for (int h = 0; h < kSub / kGroup / kThreads; ++h) {
+          const int gl = tid + h * kThreads, g = i * (kSub / kGroup) + gl;  // this thread's groups
+          if (ok && gl * kGroup < n_i) {
+            float xt[kGroup], xd[kGroup];
+            group8<T, true, false>(sbt, gl, n_i, xt);
+            if (res_pass) group8<T, true, false>(sbd, gl, n_i, xd);
+            const long long m8 = mass8(g, xt, xd);
+            gmass[g] = m8;
+            mass += m8;
+          }
+        }
+        __syncthreads();  // every thread is done with the stage
+        if (ok && VEC && tid == 0 && i + kSubStages < nsub) issue_sub(i + kSubStages);
       }
+      subs_done += nsub;
       mass = block_sum_ll(mass, sm.ll_buf);
       if (tid == 0) sm.S[pass] = mass;
       cluster.sync();
@@ -1081,13 +1157,12 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
 }
 
 
-// Decision cluster size for T > 0: 8 CTAs once the batch alone covers the SMs
-// (16-CTA clusters cost more to place than their shorter chunks save: 39.5
-// against 41 us for 32 sequences at V = 128256), 16 below that; chunks of at
-// most kMaxChunk elements.
+// Decision cluster size for T > 0: 16 CTAs while 8 a sequence would leave SMs
+// idle, 8 while the batch's clusters fit about four CTAs an SM at once, 4 beyond
+// (so that large batches run in one wave); chunks of at most kMaxChunk elements.
 int pick_cluster(int batch, int vocab) {
   const int sms = num_sms();
-  int C = (batch * 8 < sms) ? 16 : 8;
+  int C = (batch * 8 < sms) ? 16 : (batch * 8 <= 4 * sms ? 8 : 4);
   while (C < 16 && (vocab + C - 1) / C > kMaxChunk) C *= 2;
   return C;
 }
@@ -1131,12 +1206,7 @@ cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int
   SamplerArgs da = a;
   da.chunk = ((a.vocab + C - 1) / C + 7) / 8 * 8;
   auto dkern = decide_kernel<T, VEC, MODE>;
-  int ring = 0, dyn = 0;
-  if (STOCH) {
-    const int pair = ((da.chunk * (int)sizeof(T) + 127) / 128) * 128;
-    ring = 2 * pair;
-    dyn = ring + (da.chunk + kGroup - 1) / kGroup * (int)sizeof(long long);
-  }
+  const int dyn = STOCH ? kRingBytes + (da.chunk + kGroup - 1) / kGroup * (int)sizeof(long long) : 0;
   e = cudaFuncSetAttribute(dkern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
   if (C > 8) {
@@ -1157,8 +1227,7 @@ cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, dkern, da, static_cast<const float *>(pm), static_cast<const float *>(ps), nchunk,
-                            ring);
+  return cudaLaunchKernelEx(&cfg, dkern, da, static_cast<const float *>(pm), static_cast<const float *>(ps), nchunk);
 }
 
 // rows 16-byte aligned: 1-D bulk copies (every item and chunk then starts on 16

@@ -38,10 +38,11 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 // writes any memory, before it reads anything an earlier kernel of the library
 // may write, and before any return: the earlier kernel has then completed and
 // its writes are visible, and, since every kernel waits before it can
-// complete, completion stays transitive along the stream. (A kernel may read
-// the call's own inputs before the wait: the kernel before the earlier one has
-// completed by then, since the earlier one let this one launch only after its
-// own wait.) grid_dependents_launch() lets the next kernel launch.
+// complete, completion stays transitive along the stream. Before the wait a
+// kernel may read what no kernel of the library writes (the call's own
+// inputs: whatever produced them is not a kernel of the library, so it let
+// the library's kernels start only once it had completed).
+// grid_dependents_launch() lets the next kernel launch.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependents_launch() {
