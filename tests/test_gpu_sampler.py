@@ -133,14 +133,26 @@ def test_tree_stochastic_many_small_trees():
 
 
 @pytest.mark.parametrize("V,dtype", [(5, "f32"), (4099, "bf16"), (20000, "f32"), (131072, "bf16"),
-                                     (200000, "bf16")])
+                                     (200000, "bf16"), (200000, "f32")])
 def test_vocab_sizes(V, dtype):
-    """Odd vocabularies (scalar loads), cluster of 8 and of 16, chunks of many items."""
+    """Odd vocabularies (scalar loads), cluster of 8 and of 16, chunks of many items; at
+    200000 f32 the decision chunk passes through its sub-chunk ring more than once."""
     case = W.custom(31, batch=6, ctx_lens=[4] * 6, n_q=[1, 2, 3, 5, 7, 9], num_q_heads=1, num_kv_heads=1,
                     head_dim=8, block_size=16, vocab=V, dtype=dtype, target_sigma=2.0, draft_coef=0.8,
                     draft_sigma=1.0, use_bank=V > 50000)
     _check(case)
     case.step.temperature = 0.0
+    _check(case)
+
+
+@pytest.mark.parametrize("V,dtype", [(40001, "f32"), (40003, "bf16")])
+def test_large_batch_clusters_of_four(V, dtype):
+    """160 sequences take 4-CTA decision clusters; with an odd vocabulary the chunks are
+    staged by scalar loads, and at f32 each chunk passes through the ring more than once.
+    Decisions, emitted tokens and accept counts equal the oracle's (near-ties aside)."""
+    case = W.custom(71, batch=160, ctx_lens=[4] * 160, n_q=[1, 2, 4, 6, 8] * 32, num_q_heads=1, num_kv_heads=1,
+                    head_dim=8, block_size=16, vocab=V, dtype=dtype, target_sigma=2.0, draft_coef=0.8,
+                    draft_sigma=1.0, use_bank=False)
     _check(case)
 
 
