@@ -875,8 +875,10 @@ __global__ void __launch_bounds__(F8 ? kThreads + kConvWarps * 32 : kThreads, kC
 // every piece's log-sum-exp and 32 partial outputs before it uses any (up to
 // four pieces; more go four at a time), so a merge costs about one round trip.
 __global__ void __launch_bounds__(128) attn_umma_combine(const UmmaParams P) {
-  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
+  // the next kernel may launch at once (it reads before its own wait only what no kernel of the
+  // library writes): the sampler's statistics can then start on the SMs the attention frees
   grid_dependents_launch();
+  grid_dependency_wait();  // the earlier kernel on the stream is complete and visible
   const AttnArgs &a = P.a;
   const int b = blockIdx.x, kvh = blockIdx.y / P.rb_max, rb = blockIdx.y % P.rb_max;
   const int tid = threadIdx.x;
