@@ -70,6 +70,9 @@ constexpr int kMaxQ = 64;
 constexpr int kMaxRows = 2 * kMaxQ;  // target + draft rows of one sequence
 constexpr int kMaxChunk = 32768;     // vocabulary elements per CTA
 constexpr int kGroup = 8;            // consecutive elements of a group
+// A group's slot in the decisions' shared per-group masses: one spare slot every eight, so that
+// the owner's threads, each summing eight consecutive groups, read eight different bank pairs
+__host__ __device__ constexpr int gpad(int g) { return g + (g >> 3); }
 constexpr int kSub = 4096;           // decisions: elements of a sub-chunk of the row pair (two groups a thread)
 constexpr int kRingBytes = 65536;    // decisions: the sub-chunk ring (target and draft halves)
 template <typename T>
@@ -1039,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
             group8<T, true, false>(sbt, gl, n_i, xt);
             if (res_pass) group8<T, true, false>(sbd, gl, n_i, xd);
             const long long m8 = mass8(g, xt, xd);
-            gmass[g] = m8;
+            gmass[gpad(g)] = m8;
             mass += m8;
           }
         }
@@ -1091,15 +1094,15 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
         long long local = 0;
         int last_g = -1;
         for (int g = g0; g < g1; ++g) {
-          local += gmass[g];
-          if (gmass[g] > 0) last_g = g;
+          local += gmass[gpad(g)];
+          if (gmass[gpad(g)] > 0) last_g = g;
         }
         long long seg_total;
         long long cum = P + block_excl_scan_ll(local, sm.ll_buf, &seg_total);
         if (last_g >= 0) atomicMax(&sm.y_last, last_g);
         if (P >= 0) {
           for (int g = g0; g < g1 && cum <= target; ++g) {
-            if (cum + gmass[g] > target) {  // the group whose prefix range holds the target
+            if (cum + gmass[gpad(g)] > target) {  // the group whose prefix range holds the target
               long long w[kGroup];
               weights8(g, w);
               long long c2 = cum;
@@ -1118,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
               atomicMin(&sm.y_hit, lo + y);
               break;
             }
-            cum += gmass[g];
+            cum += gmass[gpad(g)];
           }
         }
         __syncthreads();
@@ -1206,7 +1209,7 @@ cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int
   SamplerArgs da = a;
   da.chunk = ((a.vocab + C - 1) / C + 7) / 8 * 8;
   auto dkern = decide_kernel<T, VEC, MODE>;
-  const int dyn = STOCH ? kRingBytes + (da.chunk + kGroup - 1) / kGroup * (int)sizeof(long long) : 0;
+  const int dyn = STOCH ? kRingBytes + gpad((da.chunk + kGroup - 1) / kGroup) * (int)sizeof(long long) : 0;
   e = cudaFuncSetAttribute(dkern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
   if (C > 8) {
