@@ -134,18 +134,6 @@ __device__ __forceinline__ long long to_fix(float w) {
   return ((long long)(__float_as_int(h) - 0x4B000000) << 20) + (__float_as_int(l) - 0x4B000000);
 }
 
-__device__ long long block_sum_ll(long long x, long long *buf) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  if (lane == 0) buf[warp] = x;
-  __syncthreads();
-  long long t = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) t += buf[w];
-  __syncthreads();
-  return t;
-}
 
 __device__ long long block_excl_scan_ll(long long x, long long *buf, long long *total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -994,7 +982,6 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
       // ---- pass B: each group's mass and this CTA's total. The chunk streams through the
       // ring in sub-chunks of kSub elements (two groups a thread): thread 0 keeps kSubStages of
       // them in flight with bulk copies, refilling a stage once every thread has read it ----
-      long long mass = 0;
       auto issue_sub = [&](int i) {  // sub-chunk i of this pass into its stage (thread 0, VEC)
         const int st = (subs_done + i) % kSubStages;
         const int e0 = i * kSub;
@@ -1043,15 +1030,28 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
             if (res_pass) group8<T, true, false>(sbd, gl, n_i, xd);
             const long long m8 = mass8(g, xt, xd);
             gmass[gpad(g)] = m8;
-            mass += m8;
           }
         }
         __syncthreads();  // every thread is done with the stage
         if (ok && VEC && tid == 0 && i + kSubStages < nsub) issue_sub(i + kSubStages);
       }
       subs_done += nsub;
-      mass = block_sum_ll(mass, sm.ll_buf);
-      if (tid == 0) sm.S[pass] = mass;
+      // every CTA, before the cluster barrier: each thread's consecutive groups, their mass, its
+      // exclusive prefix within the CTA and the CTA's total, and the last group with mass, so
+      // that the owner needs no scan after the barrier
+      const int per = (ngroups + kThreads - 1) / kThreads;  // consecutive groups of this thread
+      const int g0 = min(ngroups, tid * per), g1 = min(ngroups, g0 + per);
+      long long local = 0;
+      int last_g = -1;
+      for (int g = g0; g < g1; ++g) {
+        local += gmass[gpad(g)];
+        if (gmass[gpad(g)] > 0) last_g = g;
+      }
+      if (tid == 0) sm.y_last = -1;
+      long long cta_total;
+      const long long excl = block_excl_scan_ll(local, sm.ll_buf, &cta_total);
+      if (last_g >= 0) atomicMax(&sm.y_last, last_g);
+      if (tid == 0) sm.S[pass] = cta_total;
       cluster.sync();
       if (warp == 0) {
         // the draw: the smallest v whose inclusive prefix exceeds u' * S
@@ -1081,25 +1081,14 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
           sm.Stot = S;
           sm.m2 = 0.f;  // stays 0 when rounding leaves no crossing
           sm.y_hit = INT_MAX;
-          sm.y_last = -1;
         }
       }
       __syncthreads();
       if (sm.fallback) continue;  // residual without mass: draw from p_a instead
       if (rank == sm.owner) {
-        // ---- the owner: scan the group masses in order, then the group of the crossing ----
+        // ---- the owner: the thread whose groups hold the crossing finds it ----
         const long long P = sm.P_owner, target = sm.target;
-        const int per = (ngroups + kThreads - 1) / kThreads;  // consecutive groups of this thread
-        const int g0 = min(ngroups, tid * per), g1 = min(ngroups, g0 + per);
-        long long local = 0;
-        int last_g = -1;
-        for (int g = g0; g < g1; ++g) {
-          local += gmass[gpad(g)];
-          if (gmass[gpad(g)] > 0) last_g = g;
-        }
-        long long seg_total;
-        long long cum = P + block_excl_scan_ll(local, sm.ll_buf, &seg_total);
-        if (last_g >= 0) atomicMax(&sm.y_last, last_g);
+        long long cum = P + excl;
         if (P >= 0) {
           for (int g = g0; g < g1 && cum <= target; ++g) {
             if (cum + gmass[gpad(g)] > target) {  // the group whose prefix range holds the target
