@@ -70,13 +70,13 @@ constexpr int kMaxQ = 64;
 constexpr int kMaxRows = 2 * kMaxQ;  // target + draft rows of one sequence
 constexpr int kMaxChunk = 32768;     // vocabulary elements per CTA
 constexpr int kGroup = 8;            // consecutive elements of a group
-// A group's slot in the decisions' shared per-group masses: one spare slot every eight, so that
-// the owner's threads, each summing eight consecutive groups, read eight different bank pairs
-__host__ __device__ constexpr int gpad(int g) { return g + (g >> 3); }
+// The decisions keep one fixed-point mass per unit of one group (8-CTA and larger clusters) or
+// two groups (4-CTA clusters, whose chunks are twice as long), in shared memory with one spare
+// slot every eight, so that the threads summing consecutive units read different bank pairs
+__host__ __device__ constexpr int upad(int u) { return u + (u >> 3); }
 constexpr int kSub = 4096;           // decisions: elements of a sub-chunk of the row pair (two groups a thread)
-constexpr int kRingBytes = 65536;    // decisions: the sub-chunk ring (target and draft halves)
-template <typename T>
-constexpr int sub_stages() { return kRingBytes / (2 * kSub * (int)sizeof(T)); }  // bf16: 4, fp32: 2
+constexpr int kRingBytes = 65536;    // decisions: the sub-chunk ring (target and draft halves), 8-CTA and
+                                     // larger clusters; half that at 4 CTAs, so that four fit an SM
 constexpr int kMaxSubStages = 4;
 
 // 2^x by the MUFU approximation (flush-to-zero; relative error about 2^-22)
@@ -545,7 +545,8 @@ struct Smem {
   int y_hit, y_last;
 };
 
-template <typename T, bool VEC, int MODE>
+// UG: groups of a mass unit (1, or 2 with the half ring of 4-CTA clusters)
+template <typename T, bool VEC, int MODE, int UG>
 __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, const float *__restrict__ pm,
                                                           const float *__restrict__ ps, int nchunk) {
   cg::cluster_group cluster = cg::this_cluster();
@@ -556,10 +557,14 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
   __shared__ Smem sm;
   extern __shared__ __align__(128) uint8_t dyn[];
   // phase 3: a ring of sub-chunk stages (target, then draft: kSub elements each), then the
-  // per-group masses
-  constexpr int kSubStages = sub_stages<T>();
+  // per-unit masses
+  static_assert(UG == 1 || UG == 2, "one or two groups a mass unit");
+  constexpr int kRing = kRingBytes / UG;
+  constexpr int kSubStages = kRing / (2 * kSub * (int)sizeof(T));  // bf16: 4 or 2, fp32: 2 or 1
+  static_assert(kSubStages >= 1 && kSubStages <= kMaxSubStages, "sub-chunk stages");
+  constexpr int ug = UG;
   uint8_t *sring = dyn;
-  long long *gmass = reinterpret_cast<long long *>(dyn + kRingBytes);
+  long long *gmass = reinterpret_cast<long long *>(dyn + kRing);
 
   // Before the grid-dependency wait this kernel reads only the call's own inputs (cu_q, draft
   // tokens, uniforms, parents and logits), which no kernel of the library writes, so their
@@ -1021,31 +1026,55 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
           }
           __syncthreads();
         }
+        // groups tid and tid + kThreads of the sub-chunk (consecutive threads read consecutive
+        // 16-byte pieces of the stage); the two groups of a unit are on adjacent lanes
+        static_assert(kSub == 2 * kGroup * kThreads, "two groups a thread and sub-chunk");
+        if constexpr (UG == 1) {
 #pragma unroll
-        for (int h = 0; h < kSub / kGroup / kThreads; ++h) {
-          const int gl = tid + h * kThreads, g = i * (kSub / kGroup) + gl;  // this thread's groups
-          if (ok && gl * kGroup < n_i) {
-            float xt[kGroup], xd[kGroup];
-            group8<T, true, false>(sbt, gl, n_i, xt);
-            if (res_pass) group8<T, true, false>(sbd, gl, n_i, xd);
-            const long long m8 = mass8(g, xt, xd);
-            gmass[gpad(g)] = m8;
+          for (int h = 0; h < 2; ++h) {
+            const int gl = tid + h * kThreads, g = i * (kSub / kGroup) + gl;
+            if (ok && gl * kGroup < n_i) {
+              float xt[kGroup], xd[kGroup];
+              group8<T, true, false>(sbt, gl, n_i, xt);
+              if (res_pass) group8<T, true, false>(sbd, gl, n_i, xd);
+              gmass[upad(g)] = mass8(g, xt, xd);
+            }
+          }
+        } else {
+          long long mh[2];  // both groups' masses first (independent chains), then the pair sums
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int gl = tid + h * kThreads, g = i * (kSub / kGroup) + gl;
+            mh[h] = 0;
+            if (ok && gl * kGroup < n_i) {
+              float xt[kGroup], xd[kGroup];
+              group8<T, true, false>(sbt, gl, n_i, xt);
+              if (res_pass) group8<T, true, false>(sbd, gl, n_i, xd);
+              mh[h] = mass8(g, xt, xd);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int gl = tid + h * kThreads, g = i * (kSub / kGroup) + gl;
+            const long long pair = mh[h] + __shfl_down_sync(0xffffffffu, mh[h], 1);
+            if (ok && gl * kGroup < n_i && (lane & 1) == 0) gmass[upad(g >> 1)] = pair;
           }
         }
         __syncthreads();  // every thread is done with the stage
         if (ok && VEC && tid == 0 && i + kSubStages < nsub) issue_sub(i + kSubStages);
       }
       subs_done += nsub;
-      // every CTA, before the cluster barrier: each thread's consecutive groups, their mass, its
-      // exclusive prefix within the CTA and the CTA's total, and the last group with mass, so
+      // every CTA, before the cluster barrier: each thread's consecutive units, their mass, its
+      // exclusive prefix within the CTA and the CTA's total, and the last unit with mass, so
       // that the owner needs no scan after the barrier
-      const int per = (ngroups + kThreads - 1) / kThreads;  // consecutive groups of this thread
-      const int g0 = min(ngroups, tid * per), g1 = min(ngroups, g0 + per);
+      const int nunits = (ngroups + ug - 1) / ug;
+      const int per = (nunits + kThreads - 1) / kThreads;  // consecutive units of this thread
+      const int u0 = min(nunits, tid * per), u1 = min(nunits, u0 + per);
       long long local = 0;
-      int last_g = -1;
-      for (int g = g0; g < g1; ++g) {
-        local += gmass[gpad(g)];
-        if (gmass[gpad(g)] > 0) last_g = g;
+      int last_g = -1;  // the last unit with mass
+      for (int u = u0; u < u1; ++u) {
+        local += gmass[upad(u)];
+        if (gmass[upad(u)] > 0) last_g = u;
       }
       if (tid == 0) sm.y_last = -1;
       long long cta_total;
@@ -1090,41 +1119,44 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(SamplerArgs args, cons
         const long long P = sm.P_owner, target = sm.target;
         long long cum = P + excl;
         if (P >= 0) {
-          for (int g = g0; g < g1 && cum <= target; ++g) {
-            if (cum + gmass[gpad(g)] > target) {  // the group whose prefix range holds the target
-              long long w[kGroup];
-              weights8(g, w);
+          for (int u = u0; u < u1 && cum <= target; ++u) {
+            if (cum + gmass[upad(u)] > target) {  // the unit whose prefix range holds the target
               long long c2 = cum;
-              int y = g * kGroup + kGroup - 1;
+              int y = -1;
+              for (int g = ug * u; g < min(ug * u + ug, ngroups) && y < 0; ++g) {  // its groups in order
+                long long w[kGroup];
+                weights8(g, w);
 #pragma unroll
-              for (int k = 0; k < kGroup; ++k) {
-                c2 += w[k];
-                if (c2 > target) {
-                  y = g * kGroup + k;
-                  // distance of u' S from the chosen interval's edges, on the normalised CDF
-                  const long long below = target - (c2 - w[k]), above = c2 - target;
-                  sm.m2 = (float)((double)(below < above ? below : above) / (double)sm.Stot);
-                  break;
+                for (int k = 0; k < kGroup; ++k) {
+                  c2 += w[k];
+                  if (y < 0 && c2 > target) {
+                    y = g * kGroup + k;
+                    // distance of u' S from the chosen interval's edges, on the normalised CDF
+                    const long long below = target - (c2 - w[k]), above = c2 - target;
+                    sm.m2 = (float)((double)(below < above ? below : above) / (double)sm.Stot);
+                  }
                 }
               }
+              if (y < 0) y = min(ug * u + ug, ngroups) * kGroup - 1;
               atomicMin(&sm.y_hit, lo + y);
               break;
             }
-            cum += gmass[gpad(g)];
+            cum += gmass[upad(u)];
           }
         }
         __syncthreads();
         if (tid == 0) {
           int y = sm.y_hit;
           if (y == INT_MAX) {  // u' at or past the end: the last token with mass
-            const int g = sm.y_last;
-            y = lo + max(0, g) * kGroup;
-            if (g >= 0) {
-              long long w[kGroup];
-              weights8(g, w);
-              for (int k = 0; k < kGroup; ++k)
-                if (w[k] > 0) y = lo + g * kGroup + k;
-            }
+            const int u = sm.y_last;
+            y = lo + max(0, ug * u) * kGroup;
+            if (u >= 0)
+              for (int g = ug * u; g < min(ug * u + ug, ngroups); ++g) {
+                long long w[kGroup];
+                weights8(g, w);
+                for (int k = 0; k < kGroup; ++k)
+                  if (w[k] > 0) y = lo + g * kGroup + k;
+              }
           }
           int32_t *o = args.out_tok + (size_t)b * args.max_q;
           if constexpr (MODE == kTreeStochastic) {
@@ -1157,6 +1189,37 @@ int pick_cluster(int batch, int vocab) {
   int C = (batch * 8 < sms) ? 16 : (batch * 8 <= 4 * sms ? 8 : 4);
   while (C < 16 && (vocab + C - 1) / C > kMaxChunk) C *= 2;
   return C;
+}
+
+template <typename T, bool VEC, int MODE, int UG>
+cudaError_t launch_decide(const SamplerArgs &a, float *pm, float *ps, int nchunk, int C, cudaStream_t st) {
+  constexpr bool STOCH = MODE == kStochastic || MODE == kTreeStochastic;
+  SamplerArgs da = a;
+  da.chunk = ((a.vocab + C - 1) / C + 7) / 8 * 8;
+  auto dkern = decide_kernel<T, VEC, MODE, UG>;
+  const int units = ((da.chunk + kGroup - 1) / kGroup + UG - 1) / UG;
+  const int dyn = STOCH ? kRingBytes / UG + upad(units) * (int)sizeof(long long) : 0;
+  cudaError_t e = cudaFuncSetAttribute(dkern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  if (e != cudaSuccess) return e;
+  if (C > 8) {
+    e = cudaFuncSetAttribute(dkern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, a.batch, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, dkern, da, static_cast<const float *>(pm), static_cast<const float *>(ps), nchunk);
 }
 
 template <typename T, bool VEC, int MODE>
@@ -1195,31 +1258,10 @@ cudaError_t launch_t(const SamplerArgs &a, float *pm, float *ps, int nchunk, int
   // ---- decisions ----
   constexpr bool STOCH = MODE == kStochastic || MODE == kTreeStochastic;
   const int C = STOCH ? pick_cluster(a.batch, a.vocab) : 1;
-  SamplerArgs da = a;
-  da.chunk = ((a.vocab + C - 1) / C + 7) / 8 * 8;
-  auto dkern = decide_kernel<T, VEC, MODE>;
-  const int dyn = STOCH ? kRingBytes + gpad((da.chunk + kGroup - 1) / kGroup) * (int)sizeof(long long) : 0;
-  e = cudaFuncSetAttribute(dkern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-  if (e != cudaSuccess) return e;
-  if (C > 8) {
-    e = cudaFuncSetAttribute(dkern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
+  if constexpr (STOCH) {
+    if (C < 8) return launch_decide<T, VEC, MODE, 2>(a, pm, ps, nchunk, C, st);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, a.batch, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = dyn;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, dkern, da, static_cast<const float *>(pm), static_cast<const float *>(ps), nchunk);
+  return launch_decide<T, VEC, MODE, 1>(a, pm, ps, nchunk, C, st);
 }
 
 // rows 16-byte aligned: 1-D bulk copies (every item and chunk then starts on 16
