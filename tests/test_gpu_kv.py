@@ -46,6 +46,53 @@ def test_append_rollback_small_exact(make):
     assert_kv_equal(kv, okv)
 
 
+@pytest.mark.parametrize("batch,n,heads,head_dim", [
+    (1500, 2, 1, 32),   # the bookkeeping CTA's scans take two passes of 1024 threads
+    (2100, 1, 1, 32),   # more sequences than the scatter stages cu_q for (it reads cu_q from global)
+    (64, 64, 8, 128),   # 4096 rows of the longest chains
+], ids=["1500-seqs", "2100-seqs", "4096-rows"])
+def test_append_large_batches(batch, n, heads, head_dim):
+    """Large batches pop the same blocks in the same order and write the same bytes as the oracle."""
+    rng = np.random.default_rng(batch)
+    ctx = rng.integers(0, 100, batch).astype(np.int32)
+    case = W.custom(11, batch=batch, ctx_lens=ctx, n_q=[n] * batch, num_q_heads=heads, num_kv_heads=heads,
+                    head_dim=head_dim, block_size=16, vocab=16, use_bank=False)
+    kv, d, buf = upload(case)
+    okv = oracle.OracleKV(case.state)
+    S.append(kv, d, buf)
+    assert okv.append(case.step) is None
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    assert_kv_equal(kv, okv)
+    acc = _accepts(rng, case.step.n_q)
+    buf.accept.copy_(torch.from_numpy(acc))
+    S.rollback(kv, d, buf)
+    okv.rollback(case.step, acc)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 0
+    assert_kv_equal(kv, okv, pools=False)
+
+
+@pytest.mark.parametrize("batch,n", [(3, 5), (64, 64)], ids=["small", "4096-rows"])
+def test_bad_popped_id_is_all_or_nothing(batch, n):
+    """An id out of range among those about to be popped: SV_ERR_BAD_BLOCK_ID and nothing written."""
+    case = W.custom(12, batch=batch, ctx_lens=[16] * batch, n_q=[n] * batch, num_q_heads=8, num_kv_heads=8,
+                    head_dim=128, block_size=16, vocab=16, use_bank=False)
+    st = case.state
+    nb = st.k_pool.shape[0]
+    st.free_list[st.free_top - 2] = nb + 5  # the second id to be popped
+    kv, d, buf = upload(case)
+    before = kv_host(kv)
+    kbefore = kv.k_pool.clone()
+    S.append(kv, d, buf)
+    torch.cuda.synchronize()
+    assert status_of(buf) == 6  # SV_ERR_BAD_BLOCK_ID
+    after = kv_host(kv)
+    for k in before:
+        np.testing.assert_array_equal(np.asarray(before[k]), np.asarray(after[k]))
+    assert torch.equal(kbefore, kv.k_pool)
+
+
 @pytest.mark.parametrize("name", ["llama8b", "llama70b"])
 def test_append_rollback_full_size(name):
     case = W.CONFIGS[name]()
